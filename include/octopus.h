@@ -1,0 +1,249 @@
+/* octopus.h -- C ABI of liboctopus: packed DAG attention over a paged, refcounted KV pool.
+ *
+ * The operations follow the Octopus project page (shatianming5.github.io/octopus):
+ *   - "Architecture & Co-Design", item 01 (Runtime): server-resident radix cursors;
+ *   - item 02 (Memory): zero-copy KV mount of a sibling span into attention layers at the
+ *     monotonic position offset s(c'_B) = max(p_B, e_A + 1), allocating 0 new KV pages;
+ *   - item 03 (Training): one unpadded 1D packed forward/backward pass with
+ *     single-ownership masking, reader gradients routed into the producer's KV;
+ *   - the five-primitives table (fork, read_thread, rewind, wait, done).
+ *
+ * Conventions
+ *   - Every call returns an int status (OCTO_OK = 0).  Out-parameters are written only on
+ *     success.  No C++ exception crosses this boundary.
+ *   - Handles are opaque.  A pool and its plans are not thread-safe: one host thread at a
+ *     time per pool.
+ *   - Device memory for tensors (K/V pools, Q, O, LSE, dO, dQ, dK, dV, workspaces) is
+ *     allocated and owned by the caller and passed as raw device pointers.  The library
+ *     owns the host metadata of a pool and the device metadata arrays of a plan.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Kernels are enqueued asynchronously on it.  octo_pack_tree and octo_decode_plan
+ *     synchronise the stream once (to size the tile list); the attention calls never do.
+ *   - Cursor ids are segment ids: the n-th segment created by octo_root / octo_fork /
+ *     octo_rewind in a pool has id n.
+ *   - Sizes: a pool holds at most 2^31-1 tokens per plan; page_size <= 128; head_dim is
+ *     64 or 128; n_q_heads a multiple of n_kv_heads.
+ */
+#ifndef OCTOPUS_H
+#define OCTOPUS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+enum {
+  OCTO_OK = 0,
+  OCTO_EINVAL = 1,   /* bad argument, out-of-range span, or a mount that would show a token twice */
+  OCTO_ENOMEM = 2,   /* the pool has no free page for an append (nothing is changed) */
+  OCTO_ESTATE = 3,   /* cursor is done, rewound away from, released, or freed */
+  OCTO_ECUDA = 4,    /* a CUDA call failed; see octo_last_cuda_error() */
+  OCTO_ETIMEOUT = 5, /* a bounded device wait expired; the kernel returned early */
+  OCTO_ENOTSUP = 6   /* shape or dtype this build has no kernel for */
+};
+
+enum { OCTO_DTYPE_F32 = 0, OCTO_DTYPE_BF16 = 1 };
+
+typedef struct octo_pool_s* octo_pool_t;
+typedef struct octo_plan_s* octo_plan_t;
+typedef int32_t octo_cursor_t;
+
+/* Pool description.  k_pool / v_pool: device arrays [num_pages][n_kv_heads][page_size]
+ * [head_dim] of `dtype`, owned by the caller, alive as long as the pool.  octo_append
+ * writes appended K/V rows into them; the attention calls read whatever pool arrays they
+ * are given, which must have this layout (so one pool's page tables can serve the K/V of
+ * several layers). */
+typedef struct {
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t dtype;
+  void* k_pool;
+  void* v_pool;
+} octo_pool_desc;
+
+/* One block of the block-sparse schedule: query tile q_tile against the slots of
+ * physical page kv_page that one source (src = -1: the tile's own tree path; src >= 0:
+ * the mount with that id) makes visible.  Tile row r (0-based) sees page slot j iff
+ *     r >= q_lo  &&  kv_lo <= j < kv_hi  &&  (!(flags & 1) || j <= r + diag).
+ * 24 bytes, naturally aligned. */
+typedef struct {
+  uint32_t q_tile;
+  uint32_t kv_page;
+  uint16_t kv_lo;
+  uint16_t kv_hi;
+  uint16_t q_lo;
+  uint16_t flags;
+  int32_t diag;
+  int32_t src;
+} octo_entry;
+
+/* Segment record returned by octo_seg_query.  flags: bit0 live cursor, bit1 pinned
+ * (done), bit2 frozen (done), bit3 rewound away from, bit4 freed. */
+typedef struct {
+  int32_t parent;   /* segment it continues from, -1 for a root */
+  int32_t fork;     /* tokens of the parent it sees */
+  int32_t len;      /* own tokens */
+  int32_t n_pages;  /* own pages */
+  int32_t refcount; /* live cursor + live children + mounts reading it + pin */
+  int32_t p_next;   /* position the next appended token gets */
+  int32_t flags;
+} octo_seg_info;
+
+typedef struct {
+  int64_t n_rows;      /* packed query rows (decode plan: one per cursor) */
+  int64_t n_tiles;
+  int64_t n_entries;
+  int64_t n_segments;  /* packed segments */
+  int64_t pairs;       /* visible (row, key) pairs: the useful work of one head */
+  int32_t bm;          /* rows per q-tile */
+  int32_t page_size;
+  int32_t max_tile_entries;
+  int32_t max_page_entries;
+  int32_t n_touched_pages; /* pages some entry reads */
+  int32_t is_decode;
+} octo_plan_info_t;
+
+/* ---- pool (host metadata; primitives table of the project page) ---- */
+
+/* Creates a pool.  All pages start free.  EINVAL on a bad description. */
+int octo_pool_create(const octo_pool_desc* desc, octo_pool_t* out);
+int octo_pool_destroy(octo_pool_t pool);
+
+/* New root segment with a live cursor; positions start at 0. */
+int octo_root(octo_pool_t pool, octo_cursor_t* out);
+
+/* Appends n tokens to the cursor's segment.  Pages are taken lowest-free-id first as the
+ * segment needs them; a segment's tokens fill its own pages in order.  pos_out (host,
+ * n entries, may be NULL) receives each token's position: the cursor's next position,
+ * which then advances by one.  k, v: device [n][n_kv_heads][head_dim] of the pool dtype,
+ * copied into the pool arrays on `stream`; both NULL = metadata only.
+ * ENOMEM if the free pages do not suffice (nothing changes), ESTATE if the cursor is
+ * frozen, rewound away from or released. */
+int octo_append(octo_pool_t pool, octo_cursor_t cur, int32_t n, const void* k, const void* v,
+                void* stream, int32_t* pos_out);
+
+/* fork: n children that each see the parent's current tokens and the mounts the parent
+ * holds now (O(1): no page is allocated or copied; the parent's refcount grows by n).
+ * Each child starts on a fresh page and at the parent's next position.  out: n ids. */
+int octo_fork(octo_pool_t pool, octo_cursor_t parent, int32_t n, octo_cursor_t* out);
+
+/* read_thread: mounts the producer's own tokens [a, b) into the reader's attention
+ * context from the reader's next token on (point m = reader's current length); later
+ * children of the reader inherit it.  No page is allocated.  The reader's next position
+ * becomes max(p_B, e_A + 1) with p_B its next position before the mount and
+ * e_A = pos(producer, b-1) + 1.  new_pos (may be NULL) receives it.  EINVAL if
+ * 0 <= a < b <= len(producer) fails or if any token of the span is already in the
+ * reader's context (its own path, or an earlier mount it sees). */
+int octo_mount(octo_pool_t pool, octo_cursor_t reader, octo_cursor_t producer, int32_t a,
+               int32_t b, int32_t* new_pos);
+
+/* rewind: a continuation segment that sees the first k tokens of `cur` (and the mounts
+ * with point <= k); its next position is that of token k.  The cursor moves to the
+ * continuation (returned in out); the old segment keeps its tail as a dead-end leaf
+ * (still packed and trained) until released with its continuation. */
+int octo_rewind(octo_pool_t pool, octo_cursor_t cur, int32_t k, octo_cursor_t* out);
+
+/* done: freezes the segment (no more appends, forks or mounts into it) and pins its
+ * pages (+1 refcount) so that they stay readable by mounts after the cursor is
+ * released.  octo_unpin drops the pin. */
+int octo_done(octo_pool_t pool, octo_cursor_t cur);
+int octo_unpin(octo_pool_t pool, octo_cursor_t cur);
+
+/* Drops the cursor's reference.  A segment whose refcount reaches 0 is freed: its pages
+ * return to the pool and its references on its parent and on the producers it mounted
+ * are dropped in turn. */
+int octo_release(octo_pool_t pool, octo_cursor_t cur);
+
+int octo_pool_info(octo_pool_t pool, int32_t* n_segments, int32_t* free_pages,
+                   int32_t* n_mounts);
+/* pos (len entries) and pages (n_pages entries) are optional host outputs. */
+int octo_seg_query(octo_pool_t pool, octo_cursor_t seg, octo_seg_info* info, int32_t* pos,
+                   int32_t* pages);
+
+/* ---- plans (item 03: compile the tree and its mount edges into one packed pass) ---- */
+
+/* Packs every live segment descending from the given roots, in (root order, segment id)
+ * order, unpadded: row_base = exclusive scan of the segment lengths.  Each segment's
+ * rows are cut into q-tiles of bm rows (the last one ragged); the GPU compiler emits, per
+ * tile, one entry per (page, source) block of visible keys, in the order those keys
+ * first appear in the context of the tile's last row, then a kv-page-major view (CSC)
+ * for the backward pass.  Synchronises `stream` once.  1 <= bm <= 128 (multiples of 16
+ * for the tensor-core kernels: bm = 128 is what they run). */
+int octo_pack_tree(octo_pool_t pool, const octo_cursor_t* roots, int32_t n_roots, int32_t bm,
+                   void* stream, octo_plan_t* out);
+
+/* Decode plan: one row per cursor -- the cursor's last token -- against its whole
+ * context (prefix pages, own pages, mounted spans).  Same entry format, one tile per
+ * cursor.  Synchronises `stream` once. */
+int octo_decode_plan(octo_pool_t pool, const octo_cursor_t* cursors, int32_t n, void* stream,
+                     octo_plan_t* out);
+
+int octo_plan_info(octo_plan_t plan, octo_plan_info_t* info);
+
+/* Copies the plan to host buffers (each may be NULL); synchronous.  Sizes: seg_order,
+ * seg_row_base [n_segments]; row_pos [n_rows]; tile_seg, tile_t0, tile_rows [n_tiles];
+ * tile_off [n_tiles+1]; entries, csc_perm [n_entries]; page_off [num_pages+1]. */
+int octo_plan_copy_out(octo_plan_t plan, int32_t* seg_order, int32_t* seg_row_base,
+                       int32_t* row_pos, int32_t* tile_seg, int32_t* tile_t0,
+                       int32_t* tile_rows, int32_t* tile_off, octo_entry* entries,
+                       int32_t* csc_perm, int32_t* page_off);
+int octo_plan_destroy(octo_plan_t plan);
+
+/* ---- attention (device, async on stream) ---- */
+
+/* Forward over a packed plan.  For query head h the kv head is h / (n_q_heads /
+ * n_kv_heads).  q, o: [n_rows][n_q_heads][head_dim] of the pool dtype; lse: fp32
+ * [n_q_heads][n_rows], natural log of the softmax denominator of the scaled scores.
+ * k_pool / v_pool NULL = the pool's own arrays.  scale multiplies q.k (1/sqrt(d) is
+ * the usual choice). */
+int octo_attn_fwd(octo_plan_t plan, int32_t n_q_heads, const void* q, const void* k_pool,
+                  const void* v_pool, void* o, float* lse, float scale, void* stream);
+
+/* Workspace bytes octo_attn_bwd needs for this plan and head count. */
+size_t octo_attn_bwd_workspace_size(octo_plan_t plan, int32_t n_q_heads);
+
+/* Backward of octo_attn_fwd given o, lse and dout (same layouts as the forward).
+ * dq: fp32 [n_rows][n_q_heads][head_dim].  dk_pool, dv_pool: fp32, pool-shaped
+ * [num_pages][n_kv_heads][page_size][head_dim]; every page some entry of the plan reads
+ * is overwritten with the sum, over every reader row and the query heads of its group,
+ * of that key's gradient (slots no row sees get 0); other pages are not touched.  The
+ * sums are taken in a fixed order without atomics, so results are deterministic. */
+int octo_attn_bwd(octo_plan_t plan, int32_t n_q_heads, const void* q, const void* k_pool,
+                  const void* v_pool, const void* o, const float* lse, const void* dout,
+                  float* dq, float* dk_pool, float* dv_pool, float scale, void* ws,
+                  size_t ws_bytes, void* stream);
+
+/* Workspace bytes octo_decode needs. */
+size_t octo_decode_workspace_size(octo_plan_t plan, int32_t n_q_heads);
+
+/* Paged decode over a decode plan: for cursor i and query head h, out[i][h] =
+ * softmax(scale * q[i][h] . K_ctx) V_ctx over the cursor's context (its last token
+ * included).  q, out: [n][n_q_heads][head_dim] of the pool dtype; lse: fp32
+ * [n][n_q_heads] (may be NULL). */
+int octo_decode(octo_plan_t plan, int32_t n_q_heads, const void* q, const void* k_pool,
+                const void* v_pool, void* out, float* lse, float scale, void* ws,
+                size_t ws_bytes, void* stream);
+
+/* ---- diagnostics ---- */
+const char* octo_strerror(int status);
+int octo_last_cuda_error(void);   /* last cudaError_t seen by the library */
+/* Waits for the stream, then returns the device status word of the pool's plans
+ * (OCTO_ETIMEOUT if a bounded wait expired) and clears it. */
+int octo_sync(octo_plan_t plan, void* stream);
+/* Which kernel family octo_attn_fwd / bwd / decode will use for this plan:
+ * 0 = CUDA-core (SIMT) kernels, 1 = tcgen05 tensor-core kernels.  which: 0 fwd, 1 bwd,
+ * 2 decode. */
+int octo_kernel_path(octo_plan_t plan, int32_t n_q_heads, int32_t which);
+/* Number of kernels the library has enqueued in this process so far (all pools, all
+ * streams).  The difference across a region counts the region's launches. */
+int64_t octo_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* OCTOPUS_H */

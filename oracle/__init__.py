@@ -62,7 +62,9 @@ def _load():
         L.orc_seg_pages.argtypes = [P, I, IP]
         L.orc_mount_info.argtypes = [P, I, IP]
         L.orc_pack.restype = P
-        L.orc_pack.argtypes = [P, IP, I, I, IP]
+        L.orc_pack.argtypes = [P, IP, I, I, I, IP]
+        L.orc_plan_total_pairs.restype = ctypes.c_longlong
+        L.orc_plan_total_pairs.argtypes = [P]
         L.orc_plan_delete.argtypes = [P]
         L.orc_plan_size.restype = ctypes.c_longlong
         L.orc_plan_size.argtypes = [P, I]
@@ -244,10 +246,12 @@ class Oracle:
         self._L.orc_token_owner(self.h, _ip(seg), _ip(idx))
         return seg[:n], idx[:n]
 
-    def pack(self, roots, bm):
+    def pack(self, roots, bm, tile_stride=1):
+        """Packs the trees of `roots`; with tile_stride > 1 only every tile_stride-th
+        tile gets its entries derived (the others are left empty)."""
         st = ctypes.c_int()
         r = np.ascontiguousarray(roots, dtype=np.int32)
-        h = self._L.orc_pack(self.h, _ip(r), len(r), bm, ctypes.byref(st))
+        h = self._L.orc_pack(self.h, _ip(r), len(r), bm, tile_stride, ctypes.byref(st))
         if not h:
             raise OracleError(st.value, "pack")
         return OraclePlan(self, h, bm)
@@ -323,6 +327,9 @@ class OraclePlan:
         if st != OK:
             raise OracleError(st, "bwd")
         return dQ, dK, dV
+
+    def total_pairs(self):
+        return int(self.orc._L.orc_plan_total_pairs(self.h))
 
     def row_context(self, r):
         n = self.orc._L.orc_row_context(self.h, r, None, None, 0)

@@ -96,18 +96,32 @@ struct Oracle {
       if (mt.producer == s && !segs[mt.reader].freed) r++;
     return r;
   }
+  // A segment stays allocated while a live cursor or a pin needs it, directly or through
+  // the prefix it shares (parent) or a span it mounted (producer).  Reachability is
+  // recomputed from scratch by fixpoint iteration.
   void collect() {
-    bool again = true;
-    while (again) {
-      again = false;
-      for (int s = 0; s < (int)segs.size(); s++) {
-        if (!segs[s].freed && refcount(s) == 0) {
-          for (int p : segs[s].pages) used[p] = 0;
-          segs[s].freed = true;
-          again = true;
-        }
+    std::vector<char> need(segs.size(), 0);
+    for (size_t s = 0; s < segs.size(); s++)
+      if (!segs[s].freed && (segs[s].cursor || segs[s].pinned)) need[s] = 1;
+    bool grew = true;
+    while (grew) {
+      grew = false;
+      for (size_t s = 0; s < segs.size(); s++) {
+        if (!need[s]) continue;
+        int par = segs[s].parent;
+        if (par >= 0 && !need[par] && !segs[par].freed) { need[par] = 1; grew = true; }
+        for (const Mount& mt : mounts)
+          if (mt.reader == (int)s && !need[mt.producer] && !segs[mt.producer].freed) {
+            need[mt.producer] = 1;
+            grew = true;
+          }
       }
     }
+    for (size_t s = 0; s < segs.size(); s++)
+      if (!segs[s].freed && !need[s]) {
+        for (int p : segs[s].pages) used[p] = 0;
+        segs[s].freed = true;
+      }
   }
   int free_count() const {
     int n = 0;
@@ -171,6 +185,7 @@ struct Oracle {
 struct Plan {
   const Oracle* o;
   int bm;
+  int tile_stride = 1;   // derive the entries of every tile_stride-th tile only
   std::vector<int> seg_order, seg_row_base;    // packed segments and first packed row
   std::vector<int> row_seg, row_idx, row_pos;  // per packed row
   std::vector<int> tile_seg, tile_t0, tile_rows;
@@ -200,6 +215,10 @@ int derive_tiles(Plan& pl) {
       pl.tile_seg.push_back(s);
       pl.tile_t0.push_back(t0);
       pl.tile_rows.push_back(rows);
+      if (tile % pl.tile_stride != 0) {
+        pl.tile_off.push_back((int)pl.entries.size());
+        continue;
+      }
       // groups in first-appearance order within the last row's context
       std::vector<std::pair<int, int>> keys;  // (page, src)
       std::map<std::pair<int, int>, int> key_index;
@@ -492,13 +511,14 @@ int orc_mount_info(void* h, int i, int* info) {
 }
 
 // ---- packing ----
-void* orc_pack(void* h, const int* roots, int n_roots, int bm, int* status) {
+void* orc_pack(void* h, const int* roots, int n_roots, int bm, int tile_stride, int* status) {
   Oracle* o = static_cast<Oracle*>(h);
   *status = ORC_OK;
   if (bm <= 0 || n_roots < 0) { *status = ORC_EINVAL; return nullptr; }
   Plan* pl = new Plan();
   pl->o = o;
   pl->bm = bm;
+  pl->tile_stride = tile_stride < 1 ? 1 : tile_stride;
   for (int ri = 0; ri < n_roots; ri++) {
     int r = roots[ri];
     if (!o->valid_seg(r) || o->segs[r].parent != -1) { *status = ORC_EINVAL; delete pl; return nullptr; }
@@ -525,6 +545,24 @@ void* orc_pack(void* h, const int* roots, int n_roots, int bm, int* status) {
   int st = derive_tiles(*pl);
   if (st != ORC_OK) { *status = st; delete pl; return nullptr; }
   return pl;
+}
+
+// Visible (row, key) pairs of the whole plan: the length of every packed row's context.
+long long orc_plan_total_pairs(void* p) {
+  Plan* pl = static_cast<Plan*>(p);
+  long long n = 0;
+  for (int s : pl->seg_order) {
+    std::vector<CtxItem> ctx = pl->o->full_ctx(s);
+    int len = (int)pl->o->segs[s].tok.size();
+    std::vector<long long> at(len + 1, 0);
+    for (const CtxItem& c : ctx) at[c.from] += 1;
+    long long run = 0;
+    for (int i = 0; i < len; i++) {
+      run += at[i];
+      n += run;
+    }
+  }
+  return n;
 }
 
 void orc_plan_delete(void* p) { delete static_cast<Plan*>(p); }

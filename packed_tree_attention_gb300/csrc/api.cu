@@ -1,0 +1,91 @@
+// Attention entry points: argument checks and dispatch between the tensor-core kernels
+// (bf16, head_dim 128, page 64, q-tile 128) and the CUDA-core kernels (everything else).
+
+#include "internal.h"
+
+namespace octo {
+int fwd_simt(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const void* v, void* o, float* lse,
+             float scale, bool decode, cudaStream_t s);
+int bwd_simt(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const void* v, const void* o,
+             const float* lse, const void* dout, float* dq, float* dk, float* dv, float scale, void* ws,
+             cudaStream_t s);
+}  // namespace octo
+
+namespace {
+
+int check_heads(const octo_plan_s* p, int32_t Hq) {
+  const int32_t Hkv = p->pool->desc.n_kv_heads;
+  if (Hq <= 0 || Hq % Hkv != 0 || Hq > 65535) return OCTO_EINVAL;
+  return OCTO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int octo_kernel_path(octo_plan_t plan, int32_t n_q_heads, int32_t which) {
+  if (!plan) return -1;
+  (void)n_q_heads;
+  (void)which;
+  return 0;
+}
+
+int octo_attn_fwd(octo_plan_t plan, int32_t Hq, const void* q, const void* k_pool, const void* v_pool, void* o,
+                  float* lse, float scale, void* stream) {
+  if (!plan || plan->info.is_decode) return OCTO_EINVAL;
+  if (int st = check_heads(plan, Hq)) return st;
+  if (plan->info.n_rows > 0 && (!q || !o || !lse)) return OCTO_EINVAL;
+  const void* k = k_pool ? k_pool : plan->pool->desc.k_pool;
+  const void* v = v_pool ? v_pool : plan->pool->desc.v_pool;
+  if (plan->info.n_entries > 0 && (!k || !v)) return OCTO_EINVAL;
+  return octo::fwd_simt(plan, Hq, q, k, v, o, lse, scale, false, (cudaStream_t)stream);
+}
+
+size_t octo_attn_bwd_workspace_size(octo_plan_t plan, int32_t Hq) {
+  if (!plan || Hq <= 0) return 0;
+  return octo::align_up((size_t)plan->info.n_rows * Hq * sizeof(float), 256);
+}
+
+int octo_attn_bwd(octo_plan_t plan, int32_t Hq, const void* q, const void* k_pool, const void* v_pool, const void* o,
+                  const float* lse, const void* dout, float* dq, float* dk_pool, float* dv_pool, float scale,
+                  void* ws, size_t ws_bytes, void* stream) {
+  if (!plan || plan->info.is_decode) return OCTO_EINVAL;
+  if (int st = check_heads(plan, Hq)) return st;
+  if (plan->info.n_rows > 0 && (!q || !o || !lse || !dout || !dq)) return OCTO_EINVAL;
+  if (plan->info.n_touched_pages > 0 && (!dk_pool || !dv_pool)) return OCTO_EINVAL;
+  if (ws_bytes < octo_attn_bwd_workspace_size(plan, Hq) || (ws_bytes > 0 && !ws && plan->info.n_rows > 0))
+    return OCTO_EINVAL;
+  const void* k = k_pool ? k_pool : plan->pool->desc.k_pool;
+  const void* v = v_pool ? v_pool : plan->pool->desc.v_pool;
+  if (plan->info.n_entries > 0 && (!k || !v)) return OCTO_EINVAL;
+  return octo::bwd_simt(plan, Hq, q, k, v, o, lse, dout, dq, dk_pool, dv_pool, scale, ws, (cudaStream_t)stream);
+}
+
+size_t octo_decode_workspace_size(octo_plan_t plan, int32_t Hq) {
+  if (!plan || Hq <= 0) return 0;
+  return 0;
+}
+
+int octo_decode(octo_plan_t plan, int32_t Hq, const void* q, const void* k_pool, const void* v_pool, void* out,
+                float* lse, float scale, void* ws, size_t ws_bytes, void* stream) {
+  if (!plan || !plan->info.is_decode) return OCTO_EINVAL;
+  if (int st = check_heads(plan, Hq)) return st;
+  if (plan->info.n_rows > 0 && (!q || !out)) return OCTO_EINVAL;
+  if (ws_bytes < octo_decode_workspace_size(plan, Hq)) return OCTO_EINVAL;
+  (void)ws;
+  const void* k = k_pool ? k_pool : plan->pool->desc.k_pool;
+  const void* v = v_pool ? v_pool : plan->pool->desc.v_pool;
+  if (plan->info.n_entries > 0 && (!k || !v)) return OCTO_EINVAL;
+  return octo::fwd_simt(plan, Hq, q, k, v, out, lse, scale, true, (cudaStream_t)stream);
+}
+
+int octo_sync(octo_plan_t plan, void* stream) {
+  if (!plan) return OCTO_EINVAL;
+  OCTO_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  int32_t st = 0;
+  OCTO_CUDA(cudaMemcpy(&st, plan->pool->d_status, 4, cudaMemcpyDeviceToHost));
+  if (st != 0) OCTO_CUDA(cudaMemset(plan->pool->d_status, 0, 4));
+  return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,675 @@
+// DAG -> block-sparse tile list compiler (K0).
+//
+// Octopus project page, "Architecture & Co-Design" item 03: the trainer compiles the
+// branched tree and its live KV mount edges into one unpadded 1D forward/backward pass.
+// Here that compilation runs on the GPU:
+//
+//   layout   packed segments -> row_base (exclusive scan of lengths), q-tiles of bm rows
+//            per segment, and the position id of every packed row (the segment's start
+//            position plus its index plus the jumps of its own mounts at m <= index;
+//            item 02's s = max(p_B, e_A + 1) is applied on the host when mounting)
+//   count    one warp per q-tile walks the tile's tree path from the root down and
+//            counts (page, source) blocks
+//   scan     entries per tile -> tile_off
+//   fill     the same walk writes the entries, in the order their keys first appear in
+//            the context of the tile's last row
+//   csc      entries grouped by kv page, each page's list in entry order
+//
+// Order of a segment X's contribution to a context (tokens [0, L) of X, mounts of X with
+// point m <= mcap): a mount at point m is placed right before X's token m, so its pages
+// come after X's pages [0, ceil(m/P)) and before the rest.  An ancestor contributes its
+// first f tokens and the mounts it held when the child on the path was created with
+// m <= f; the tile's own segment contributes tokens [0, t1) and its mounts with m <= t1-1.
+
+#include <algorithm>
+#include <cstring>
+#include <numeric>
+
+#include "internal.h"
+
+namespace octo {
+namespace {
+
+constexpr int kMaxDepth = 64;
+constexpr int kSortCap = 32768;   // max entries per kv page the CSC sort handles
+
+struct WalkArgs {
+  const DevSeg* segs;
+  const int32_t* pages;
+  const DevMount* mounts;
+  int32_t P;
+};
+
+__device__ __forceinline__ int32_t cdiv(int32_t a, int32_t b) { return (a + b - 1) / b; }
+
+// Walks one tile [t0, t1) of segment S.  In count mode returns the number of entries;
+// in fill mode writes them to out[0..n).  All 32 lanes call it with the same arguments.
+template <bool FILL>
+__device__ int32_t walk_tile(const WalkArgs& w, int32_t tile, int32_t S, int32_t t0, int32_t t1,
+                             octo_entry* out, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int32_t P = w.P;
+  int32_t chain[kMaxDepth];
+  int depth = 0;
+  for (int32_t x = S; x >= 0; x = w.segs[x].parent) {
+    if (depth == kMaxDepth) {
+      if (lane == 0) atomicExch(status, OCTO_ENOTSUP);
+      return 0;
+    }
+    chain[depth++] = x;
+  }
+  int32_t n = 0;  // entries emitted so far (uniform across lanes)
+  for (int lvl = depth - 1; lvl >= 0; lvl--) {
+    const int32_t X = chain[lvl];
+    const DevSeg sx = w.segs[X];
+    const bool own = (lvl == 0);
+    int32_t L, mcap, before;
+    if (own) {
+      L = t1;
+      mcap = t1 - 1;
+      before = 0x7fffffff;
+    } else {
+      const DevSeg& child = w.segs[chain[lvl - 1]];
+      L = child.fork;
+      mcap = child.fork;
+      before = child.created_lo;
+    }
+    const int32_t npages = cdiv(L, P);
+    int32_t next_page = 0;
+    // path pages [lo, hi) of X
+    auto emit_pages = [&](int32_t lo, int32_t hi) {
+      int32_t cnt = hi - lo;
+      if (cnt <= 0) return;
+      if (FILL) {
+        for (int32_t k = lane; k < cnt; k += 32) {
+          int32_t pi = lo + k;
+          int32_t ps = pi * P;
+          octo_entry e;
+          e.q_tile = (uint32_t)tile;
+          e.kv_page = (uint32_t)w.pages[sx.page_off + pi];
+          e.kv_lo = 0;
+          e.src = -1;
+          if (own) {
+            int32_t kv_hi = min(P, t1 - ps);
+            int32_t q_lo = max(0, ps - t0);
+            int32_t dv = t0 - ps;
+            bool causal = (q_lo + dv) < (kv_hi - 1);
+            e.kv_hi = (uint16_t)kv_hi;
+            e.q_lo = (uint16_t)q_lo;
+            e.flags = causal ? 1 : 0;
+            e.diag = causal ? dv : 0;
+          } else {
+            e.kv_hi = (uint16_t)min(P, L - ps);
+            e.q_lo = 0;
+            e.flags = 0;
+            e.diag = 0;
+          }
+          out[n + k] = e;
+        }
+      }
+      n += cnt;
+    };
+    for (int32_t mi = 0; mi < sx.mount_cnt; mi++) {
+      const DevMount M = w.mounts[sx.mount_off + mi];
+      if (M.m > mcap || (!own && M.created >= before)) continue;
+      int32_t upto = cdiv(M.m, P);
+      if (upto > next_page) {
+        emit_pages(next_page, upto);
+        next_page = upto;
+      }
+      const DevSeg sa = w.segs[M.producer];
+      int32_t pa = M.a / P, pb = (M.b - 1) / P;
+      int32_t cnt = pb - pa + 1;
+      if (FILL) {
+        int32_t q_lo = (own && M.m > t0) ? M.m - t0 : 0;
+        for (int32_t k = lane; k < cnt; k += 32) {
+          int32_t pj = pa + k;
+          octo_entry e;
+          e.q_tile = (uint32_t)tile;
+          e.kv_page = (uint32_t)w.pages[sa.page_off + pj];
+          e.kv_lo = (uint16_t)(max(M.a, pj * P) - pj * P);
+          e.kv_hi = (uint16_t)(min(M.b, (pj + 1) * P) - pj * P);
+          e.q_lo = (uint16_t)q_lo;
+          e.flags = 0;
+          e.diag = 0;
+          e.src = M.id;
+          out[n + k] = e;
+        }
+      }
+      n += cnt;
+    }
+    emit_pages(next_page, npages);
+  }
+  return n;
+}
+
+__global__ void k_layout(const DevSeg* __restrict__ segs, const int32_t* __restrict__ seg_order, int32_t n_segs,
+                         int32_t bm, int32_t* __restrict__ seg_row_base, int32_t* __restrict__ seg_tile_base) {
+  // single block: exclusive scans of segment lengths and tile counts
+  __shared__ int32_t warp_a[32], warp_b[32];
+  __shared__ int32_t carry_a, carry_b;
+  if (threadIdx.x == 0) carry_a = carry_b = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int32_t base = 0; base < n_segs; base += blockDim.x) {
+    int32_t i = base + threadIdx.x;
+    int32_t a = 0, b = 0;
+    if (i < n_segs) {
+      a = segs[seg_order[i]].len;
+      b = cdiv(a, bm);
+    }
+    int32_t sa = a, sb = b;
+    for (int o = 1; o < 32; o <<= 1) {
+      int32_t ya = __shfl_up_sync(0xffffffffu, sa, o), yb = __shfl_up_sync(0xffffffffu, sb, o);
+      if (lane >= o) sa += ya, sb += yb;
+    }
+    if (lane == 31) warp_a[wid] = sa, warp_b[wid] = sb;
+    __syncthreads();
+    if (wid == 0) {
+      int32_t va = lane < (int)(blockDim.x >> 5) ? warp_a[lane] : 0;
+      int32_t vb = lane < (int)(blockDim.x >> 5) ? warp_b[lane] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        int32_t ya = __shfl_up_sync(0xffffffffu, va, o), yb = __shfl_up_sync(0xffffffffu, vb, o);
+        if (lane >= o) va += ya, vb += yb;
+      }
+      warp_a[lane] = va;
+      warp_b[lane] = vb;
+    }
+    __syncthreads();
+    int32_t pa = (wid ? warp_a[wid - 1] : 0) + sa - a + carry_a;
+    int32_t pb = (wid ? warp_b[wid - 1] : 0) + sb - b + carry_b;
+    if (i < n_segs) {
+      seg_row_base[i] = pa;
+      seg_tile_base[i] = pb;
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) {
+      carry_a = pa + a;
+      carry_b = pb + b;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) seg_tile_base[n_segs] = carry_b;
+}
+
+// one block per packed segment: tile table and row positions
+__global__ void k_tiles(const DevSeg* __restrict__ segs, const DevMount* __restrict__ mounts,
+                        const int32_t* __restrict__ seg_order, const int32_t* __restrict__ seg_row_base,
+                        const int32_t* __restrict__ seg_tile_base, int32_t bm, int32_t* __restrict__ tile_seg,
+                        int32_t* __restrict__ tile_t0, int32_t* __restrict__ tile_rows,
+                        int32_t* __restrict__ tile_row0, int32_t* __restrict__ row_pos) {
+  const int32_t si = blockIdx.x;
+  const int32_t S = seg_order[si];
+  const DevSeg s = segs[S];
+  const int32_t r0 = seg_row_base[si], tb = seg_tile_base[si];
+  for (int32_t t = threadIdx.x; t < cdiv(s.len, bm); t += blockDim.x) {
+    tile_seg[tb + t] = S;
+    tile_t0[tb + t] = t * bm;
+    tile_rows[tb + t] = min(bm, s.len - t * bm);
+    tile_row0[tb + t] = r0 + t * bm;
+  }
+  for (int32_t i = threadIdx.x; i < s.len; i += blockDim.x) {
+    int32_t p = s.p0 + i;
+    for (int32_t k = 0; k < s.mount_cnt; k++) {
+      const DevMount& M = mounts[s.mount_off + k];
+      if (M.m <= i) p += M.jump;
+    }
+    row_pos[r0 + i] = p;
+  }
+}
+
+// decode: one single-row tile per cursor (its last token)
+__global__ void k_decode_tiles(const DevSeg* __restrict__ segs, const DevMount* __restrict__ mounts,
+                               const int32_t* __restrict__ cursors, int32_t n, int32_t* __restrict__ tile_seg,
+                               int32_t* __restrict__ tile_t0, int32_t* __restrict__ tile_rows,
+                               int32_t* __restrict__ tile_row0, int32_t* __restrict__ row_pos,
+                               int32_t* __restrict__ seg_row_base) {
+  int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const DevSeg s = segs[cursors[i]];
+  int32_t last = s.len - 1;
+  tile_seg[i] = cursors[i];
+  tile_t0[i] = last;
+  tile_rows[i] = 1;
+  tile_row0[i] = i;
+  seg_row_base[i] = i;
+  int32_t p = s.p0 + last;
+  for (int32_t k = 0; k < s.mount_cnt; k++) {
+    const DevMount& M = mounts[s.mount_off + k];
+    if (M.m <= last) p += M.jump;
+  }
+  row_pos[i] = p;
+}
+
+__global__ void k_count(WalkArgs w, const int32_t* __restrict__ tile_seg, const int32_t* __restrict__ tile_t0,
+                        const int32_t* __restrict__ tile_rows, int32_t n_tiles, int32_t* __restrict__ cnt,
+                        int32_t* status) {
+  int32_t tile = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (tile >= n_tiles) return;
+  int32_t t0 = tile_t0[tile];
+  int32_t c = walk_tile<false>(w, tile, tile_seg[tile], t0, t0 + tile_rows[tile], nullptr, status);
+  if ((threadIdx.x & 31) == 0) cnt[tile] = c;
+}
+
+__global__ void k_fill(WalkArgs w, const int32_t* __restrict__ tile_seg, const int32_t* __restrict__ tile_t0,
+                       const int32_t* __restrict__ tile_rows, int32_t n_tiles, const int32_t* __restrict__ tile_off,
+                       octo_entry* __restrict__ entries, int32_t* status) {
+  int32_t tile = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (tile >= n_tiles) return;
+  int32_t t0 = tile_t0[tile];
+  walk_tile<true>(w, tile, tile_seg[tile], t0, t0 + tile_rows[tile], entries + tile_off[tile], status);
+}
+
+// exclusive scan of in[0..n) into out[0..n], out[n] = total; optional max of in
+__global__ void k_scan(const int32_t* __restrict__ in, int32_t n, int32_t* __restrict__ out,
+                       int32_t* __restrict__ max_out) {
+  __shared__ int32_t warp_s[32], warp_m[32];
+  __shared__ int32_t carry, mx;
+  if (threadIdx.x == 0) carry = 0, mx = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int32_t base = 0; base < n; base += blockDim.x) {
+    int32_t i = base + threadIdx.x;
+    int32_t v = i < n ? in[i] : 0;
+    int32_t s = v, m = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      int32_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    }
+    if (lane == 31) warp_s[wid] = s;
+    if (lane == 0) warp_m[wid] = m;
+    __syncthreads();
+    if (wid == 0) {
+      int nw = blockDim.x >> 5;
+      int32_t x = lane < nw ? warp_s[lane] : 0;
+      int32_t y = lane < nw ? warp_m[lane] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        int32_t z = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += z;
+        y = max(y, __shfl_xor_sync(0xffffffffu, y, o));
+      }
+      warp_s[lane] = x;
+      if (lane == 0) mx = max(mx, y);
+    }
+    __syncthreads();
+    int32_t excl = (wid ? warp_s[wid - 1] : 0) + s - v + carry;
+    if (i < n) out[i] = excl;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = excl + v;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    out[n] = carry;
+    if (max_out) *max_out = mx;
+  }
+}
+
+// per entry: kv-page histogram and visible pair count
+__global__ void k_page_hist(const octo_entry* __restrict__ entries, int64_t n, const int32_t* __restrict__ tile_rows,
+                            int32_t* __restrict__ page_cnt, unsigned long long* __restrict__ pairs) {
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  unsigned long long pr = 0;
+  if (i < n) {
+    octo_entry e = entries[i];
+    atomicAdd(&page_cnt[e.kv_page], 1);
+    int32_t rows = tile_rows[e.q_tile];
+    if (!(e.flags & 1)) {
+      pr = (unsigned long long)(rows - e.q_lo) * (unsigned long long)(e.kv_hi - e.kv_lo);
+    } else {
+      for (int32_t r = e.q_lo; r < rows; r++) {
+        int32_t hi = min((int32_t)e.kv_hi, r + e.diag + 1);
+        if (hi > e.kv_lo) pr += (unsigned long long)(hi - e.kv_lo);
+      }
+    }
+  }
+  for (int o = 16; o; o >>= 1) pr += __shfl_xor_sync(0xffffffffu, pr, o);
+  if ((threadIdx.x & 31) == 0 && pr) atomicAdd(pairs, pr);
+}
+
+__global__ void k_csc_scatter(const octo_entry* __restrict__ entries, int64_t n, const int32_t* __restrict__ page_off,
+                              int32_t* __restrict__ page_fill, int32_t* __restrict__ csc) {
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  int32_t p = entries[i].kv_page;
+  int32_t slot = atomicAdd(&page_fill[p], 1);
+  csc[page_off[p] + slot] = (int32_t)i;
+}
+
+// one block per touched page: sort its CSC slice ascending (bitonic in shared memory)
+__global__ void k_csc_sort(const int32_t* __restrict__ touched, const int32_t* __restrict__ page_off,
+                           int32_t* __restrict__ csc, int32_t cap) {
+  extern __shared__ int32_t sm[];
+  int32_t p = touched[blockIdx.x];
+  int32_t lo = page_off[p], n = page_off[p + 1] - lo;
+  if (n <= 1) return;
+  int32_t m = 1;
+  while (m < n) m <<= 1;
+  for (int32_t i = threadIdx.x; i < m; i += blockDim.x) sm[i] = i < n ? csc[lo + i] : 0x7fffffff;
+  __syncthreads();
+  for (int32_t k = 2; k <= m; k <<= 1) {
+    for (int32_t j = k >> 1; j > 0; j >>= 1) {
+      for (int32_t i = threadIdx.x; i < m; i += blockDim.x) {
+        int32_t l = i ^ j;
+        if (l > i) {
+          bool up = (i & k) == 0;
+          int32_t a = sm[i], b = sm[l];
+          if ((a > b) == up) {
+            sm[i] = b;
+            sm[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int32_t i = threadIdx.x; i < n; i += blockDim.x) csc[lo + i] = sm[i];
+  (void)cap;
+}
+
+// touched pages (ascending) by compaction of page_off differences; single block
+__global__ void k_touched(const int32_t* __restrict__ page_off, int32_t num_pages, int32_t* __restrict__ touched,
+                          int32_t* __restrict__ n_out) {
+  __shared__ int32_t warp_s[32];
+  __shared__ int32_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int32_t base = 0; base < num_pages; base += blockDim.x) {
+    int32_t i = base + threadIdx.x;
+    int32_t v = (i < num_pages && page_off[i + 1] > page_off[i]) ? 1 : 0;
+    int32_t s = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      int32_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane == 31) warp_s[wid] = s;
+    __syncthreads();
+    if (wid == 0) {
+      int nw = blockDim.x >> 5;
+      int32_t x = lane < nw ? warp_s[lane] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        int32_t z = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += z;
+      }
+      warp_s[lane] = x;
+    }
+    __syncthreads();
+    int32_t excl = (wid ? warp_s[wid - 1] : 0) + s - v + carry;
+    if (v) touched[excl] = i;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = excl + v;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *n_out = carry;
+}
+
+template <typename T>
+int dalloc(octo_plan_s* pl, T** ptr, size_t n, cudaStream_t s) {
+  void* p = nullptr;
+  OCTO_CUDA(cudaMallocAsync(&p, std::max<size_t>(n, 1) * sizeof(T), s));
+  pl->allocs.push_back(p);
+  *ptr = (T*)p;
+  return OCTO_OK;
+}
+
+}  // namespace
+
+#define OCTO_TRY(x)                 \
+  do {                              \
+    int _s = (x);                   \
+    if (_s != OCTO_OK) {            \
+      octo_plan_destroy(pl);        \
+      return _s;                    \
+    }                               \
+  } while (0)
+
+int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t* seg_order_host, int32_t n_segs,
+                 bool is_decode, int32_t bm, cudaStream_t s, octo_plan_s** out) {
+  const int32_t P = pool->desc.page_size;
+  const int32_t nseg_all = (int32_t)pool->segs.size();
+  // ---- host mirror of the pool metadata ----
+  std::vector<DevSeg> hseg(nseg_all);
+  std::vector<int32_t> hpages;
+  std::vector<DevMount> hmounts;
+  for (int32_t i = 0; i < nseg_all; i++) {
+    const Segment& g = pool->segs[i];
+    DevSeg d;
+    d.parent = g.parent;
+    d.fork = g.fork;
+    d.len = g.len;
+    d.page_off = (int32_t)hpages.size();
+    d.mount_off = (int32_t)hmounts.size();
+    d.mount_cnt = (int32_t)g.mounts.size();
+    d.p0 = g.p0;
+    d.created_lo = (int32_t)g.created;
+    hpages.insert(hpages.end(), g.pages.begin(), g.pages.end());
+    for (int32_t mid : g.mounts) {
+      const MountRec& m = pool->mounts[mid];
+      hmounts.push_back({m.m, (int32_t)m.created, m.producer, m.a, m.b, mid, m.jump, 0});
+    }
+    hseg[i] = d;
+  }
+  if (!pool->d_status) {
+    OCTO_CUDA(cudaMalloc(&pool->d_status, sizeof(int32_t) * 4));
+    OCTO_CUDA(cudaMemset(pool->d_status, 0, sizeof(int32_t) * 4));
+  }
+  octo_plan_s* pl = new octo_plan_s();
+  pl->pool = pool;
+  pl->num_pages = pool->desc.num_pages;
+  std::memset(&pl->info, 0, sizeof(pl->info));
+  pl->info.bm = bm;
+  pl->info.page_size = P;
+  pl->info.is_decode = is_decode ? 1 : 0;
+  int64_t n_rows = 0, n_tiles = 0;
+  if (is_decode) {
+    n_rows = n_tiles = n_segs;
+  } else {
+    for (int32_t i = 0; i < n_segs; i++) {
+      int32_t L = pool->segs[seg_order_host[i]].len;
+      n_rows += L;
+      n_tiles += (L + bm - 1) / bm;
+    }
+  }
+  if (n_rows > INT32_MAX / 2 || n_tiles > INT32_MAX / 2) {
+    delete pl;
+    return OCTO_EINVAL;
+  }
+  pl->info.n_rows = n_rows;
+  pl->info.n_tiles = n_tiles;
+  pl->info.n_segments = n_segs;
+
+  DevSeg* d_segs;
+  int32_t *d_pages, *d_seg_tile_base, *d_cnt, *d_scratch, *d_status;
+  DevMount* d_mounts;
+  OCTO_TRY(dalloc(pl, &d_segs, hseg.size(), s));
+  OCTO_TRY(dalloc(pl, &d_pages, hpages.size(), s));
+  OCTO_TRY(dalloc(pl, &d_mounts, hmounts.size(), s));
+  OCTO_TRY(dalloc(pl, &pl->seg_order, n_segs, s));
+  OCTO_TRY(dalloc(pl, &pl->seg_row_base, n_segs, s));
+  OCTO_TRY(dalloc(pl, &d_seg_tile_base, n_segs + 1, s));
+  OCTO_TRY(dalloc(pl, &pl->row_pos, n_rows, s));
+  OCTO_TRY(dalloc(pl, &pl->tile_seg, n_tiles, s));
+  OCTO_TRY(dalloc(pl, &pl->tile_t0, n_tiles, s));
+  OCTO_TRY(dalloc(pl, &pl->tile_rows, n_tiles, s));
+  OCTO_TRY(dalloc(pl, &pl->tile_row0, n_tiles, s));
+  OCTO_TRY(dalloc(pl, &pl->tile_off, n_tiles + 1, s));
+  OCTO_TRY(dalloc(pl, &d_cnt, std::max<int64_t>(n_tiles, pl->num_pages), s));
+  OCTO_TRY(dalloc(pl, &d_scratch, 8, s));
+  OCTO_TRY(dalloc(pl, &pl->page_off, (size_t)pl->num_pages + 1, s));
+  OCTO_TRY(dalloc(pl, &pl->touched, (size_t)pl->num_pages, s));
+  d_status = d_scratch;  // [0] status, [1] max tile entries, [2] max page entries, [3] touched, [4..5] pairs
+  OCTO_TRY(cuda_status(cudaMemsetAsync(d_scratch, 0, 8 * sizeof(int32_t), s)));
+  OCTO_TRY(cuda_status(cudaMemcpyAsync(d_segs, hseg.data(), hseg.size() * sizeof(DevSeg), cudaMemcpyHostToDevice, s)));
+  if (!hpages.empty())
+    OCTO_TRY(cuda_status(cudaMemcpyAsync(d_pages, hpages.data(), hpages.size() * 4, cudaMemcpyHostToDevice, s)));
+  if (!hmounts.empty())
+    OCTO_TRY(cuda_status(
+        cudaMemcpyAsync(d_mounts, hmounts.data(), hmounts.size() * sizeof(DevMount), cudaMemcpyHostToDevice, s)));
+  const int32_t* order_src = is_decode ? tile_segs_host : seg_order_host;
+  if (n_segs > 0)
+    OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->seg_order, order_src, n_segs * 4, cudaMemcpyHostToDevice, s)));
+
+  // ---- layout ----
+  if (is_decode) {
+    if (n_segs > 0) {
+      k_decode_tiles<<<(n_segs + 255) / 256, 256, 0, s>>>(d_segs, d_mounts, pl->seg_order, n_segs, pl->tile_seg,
+                                                         pl->tile_t0, pl->tile_rows, pl->tile_row0, pl->row_pos,
+                                                         pl->seg_row_base);
+      count_launch();
+    }
+  } else {
+    k_layout<<<1, 1024, 0, s>>>(d_segs, pl->seg_order, n_segs, bm, pl->seg_row_base, d_seg_tile_base);
+    count_launch();
+    if (n_segs > 0) {
+      k_tiles<<<n_segs, 256, 0, s>>>(d_segs, d_mounts, pl->seg_order, pl->seg_row_base, d_seg_tile_base, bm,
+                                     pl->tile_seg, pl->tile_t0, pl->tile_rows, pl->tile_row0, pl->row_pos);
+      count_launch();
+    }
+  }
+  WalkArgs w{d_segs, d_pages, d_mounts, P};
+  const int wpb = 8;  // warps per block
+  int grid_t = (int)((n_tiles + wpb - 1) / wpb);
+  if (n_tiles > 0) {
+    k_count<<<grid_t, 32 * wpb, 0, s>>>(w, pl->tile_seg, pl->tile_t0, pl->tile_rows, (int32_t)n_tiles, d_cnt,
+                                        d_status);
+    count_launch();
+  }
+  k_scan<<<1, 1024, 0, s>>>(d_cnt, (int32_t)n_tiles, pl->tile_off, d_scratch + 1);
+  count_launch();
+  OCTO_TRY(cuda_status(cudaGetLastError()));
+  int32_t hs[2];
+  int32_t n_entries = 0;
+  OCTO_TRY(cuda_status(cudaMemcpyAsync(&n_entries, pl->tile_off + n_tiles, 4, cudaMemcpyDeviceToHost, s)));
+  OCTO_TRY(cuda_status(cudaMemcpyAsync(hs, d_scratch, 8, cudaMemcpyDeviceToHost, s)));
+  OCTO_TRY(cuda_status(cudaStreamSynchronize(s)));
+  if (hs[0] != OCTO_OK) {
+    octo_plan_destroy(pl);
+    return hs[0];
+  }
+  pl->info.n_entries = n_entries;
+  pl->info.max_tile_entries = hs[1];
+  OCTO_TRY(dalloc(pl, &pl->entries, n_entries, s));
+  OCTO_TRY(dalloc(pl, &pl->csc_perm, n_entries, s));
+  if (n_tiles > 0) {
+    k_fill<<<grid_t, 32 * wpb, 0, s>>>(w, pl->tile_seg, pl->tile_t0, pl->tile_rows, (int32_t)n_tiles, pl->tile_off,
+                                       pl->entries, d_status);
+    count_launch();
+  }
+  // ---- CSC ----
+  OCTO_TRY(cuda_status(cudaMemsetAsync(d_cnt, 0, (size_t)pl->num_pages * 4, s)));
+  if (n_entries > 0) {
+    k_page_hist<<<(n_entries + 255) / 256, 256, 0, s>>>(pl->entries, n_entries, pl->tile_rows, d_cnt,
+                                                        (unsigned long long*)(d_scratch + 4));
+    count_launch();
+  }
+  k_scan<<<1, 1024, 0, s>>>(d_cnt, pl->num_pages, pl->page_off, d_scratch + 2);
+  count_launch();
+  OCTO_TRY(cuda_status(cudaMemsetAsync(d_cnt, 0, (size_t)pl->num_pages * 4, s)));
+  if (n_entries > 0) {
+    k_csc_scatter<<<(n_entries + 255) / 256, 256, 0, s>>>(pl->entries, n_entries, pl->page_off, d_cnt,
+                                                          pl->csc_perm);
+    count_launch();
+  }
+  k_touched<<<1, 1024, 0, s>>>(pl->page_off, pl->num_pages, pl->touched, d_scratch + 3);
+  count_launch();
+  OCTO_TRY(cuda_status(cudaGetLastError()));
+  int32_t hs2[6];
+  OCTO_TRY(cuda_status(cudaMemcpyAsync(hs2, d_scratch, 24, cudaMemcpyDeviceToHost, s)));
+  OCTO_TRY(cuda_status(cudaStreamSynchronize(s)));
+  pl->info.max_page_entries = hs2[2];
+  pl->info.n_touched_pages = hs2[3];
+  unsigned long long pairs;
+  std::memcpy(&pairs, &hs2[4], 8);
+  pl->info.pairs = (int64_t)pairs;
+  if (hs2[2] > kSortCap) {
+    octo_plan_destroy(pl);
+    return OCTO_ENOTSUP;
+  }
+  if (hs2[3] > 0 && hs2[2] > 1) {
+    int32_t m = 1;
+    while (m < hs2[2]) m <<= 1;
+    size_t smem = (size_t)m * 4;
+    if (smem > 48 * 1024) OCTO_TRY(cuda_status(cudaFuncSetAttribute(k_csc_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)));
+    k_csc_sort<<<hs2[3], 512, smem, s>>>(pl->touched, pl->page_off, pl->csc_perm, m);
+    count_launch();
+  }
+  OCTO_TRY(cuda_status(cudaGetLastError()));
+  // scratch buffers no longer needed
+  *out = pl;
+  return OCTO_OK;
+}
+
+}  // namespace octo
+
+extern "C" {
+
+int octo_pack_tree(octo_pool_t pool, const octo_cursor_t* roots, int32_t n_roots, int32_t bm, void* stream,
+                   octo_plan_t* out) {
+  if (!pool || !out || n_roots < 0 || (n_roots > 0 && !roots) || bm < 1 || bm > 128) return OCTO_EINVAL;
+  const int32_t nseg = (int32_t)pool->segs.size();
+  std::vector<int32_t> root_of(nseg, -1);
+  for (int32_t i = 0; i < nseg; i++) {
+    // segments are created after their parents, so the parent's root is known
+    const octo::Segment& g = pool->segs[i];
+    root_of[i] = g.parent < 0 ? i : root_of[g.parent];
+  }
+  std::vector<int32_t> order;
+  for (int32_t ri = 0; ri < n_roots; ri++) {
+    int32_t r = roots[ri];
+    if (r < 0 || r >= nseg || pool->segs[r].freed || pool->segs[r].parent != -1) return OCTO_EINVAL;
+    for (int32_t k = 0; k < ri; k++)
+      if (roots[k] == r) return OCTO_EINVAL;
+    for (int32_t i = 0; i < nseg; i++)
+      if (root_of[i] == r && !pool->segs[i].freed) order.push_back(i);
+  }
+  return octo::compile_plan(pool, nullptr, order.data(), (int32_t)order.size(), false, bm, (cudaStream_t)stream, out);
+}
+
+int octo_decode_plan(octo_pool_t pool, const octo_cursor_t* cursors, int32_t n, void* stream, octo_plan_t* out) {
+  if (!pool || !out || n < 0 || (n > 0 && !cursors)) return OCTO_EINVAL;
+  for (int32_t i = 0; i < n; i++) {
+    int32_t c = cursors[i];
+    if (c < 0 || c >= (int32_t)pool->segs.size() || pool->segs[c].freed) return OCTO_EINVAL;
+    if (pool->segs[c].len == 0) return OCTO_EINVAL;
+  }
+  return octo::compile_plan(pool, cursors, nullptr, n, true, 1, (cudaStream_t)stream, out);
+}
+
+int octo_plan_info(octo_plan_t plan, octo_plan_info_t* info) {
+  if (!plan || !info) return OCTO_EINVAL;
+  *info = plan->info;
+  return OCTO_OK;
+}
+
+int octo_plan_copy_out(octo_plan_t pl, int32_t* seg_order, int32_t* seg_row_base, int32_t* row_pos, int32_t* tile_seg,
+                       int32_t* tile_t0, int32_t* tile_rows, int32_t* tile_off, octo_entry* entries, int32_t* csc_perm,
+                       int32_t* page_off) {
+  if (!pl) return OCTO_EINVAL;
+  const octo_plan_info_t& I = pl->info;
+  auto cp = [](void* dst, const void* src, size_t bytes) -> int {
+    if (!dst || bytes == 0) return OCTO_OK;
+    return octo::cuda_status(cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost));
+  };
+  int st;
+  if ((st = cp(seg_order, pl->seg_order, I.n_segments * 4))) return st;
+  if ((st = cp(seg_row_base, pl->seg_row_base, I.n_segments * 4))) return st;
+  if ((st = cp(row_pos, pl->row_pos, I.n_rows * 4))) return st;
+  if ((st = cp(tile_seg, pl->tile_seg, I.n_tiles * 4))) return st;
+  if ((st = cp(tile_t0, pl->tile_t0, I.n_tiles * 4))) return st;
+  if ((st = cp(tile_rows, pl->tile_rows, I.n_tiles * 4))) return st;
+  if ((st = cp(tile_off, pl->tile_off, (I.n_tiles + 1) * 4))) return st;
+  if ((st = cp(entries, pl->entries, I.n_entries * sizeof(octo_entry)))) return st;
+  if ((st = cp(csc_perm, pl->csc_perm, I.n_entries * 4))) return st;
+  if ((st = cp(page_off, pl->page_off, ((size_t)pl->num_pages + 1) * 4))) return st;
+  return OCTO_OK;
+}
+
+int octo_plan_destroy(octo_plan_t pl) {
+  if (!pl) return OCTO_EINVAL;
+  for (void* p : pl->allocs) cudaFree(p);
+  delete pl;
+  return OCTO_OK;
+}
+
+}  // extern "C"

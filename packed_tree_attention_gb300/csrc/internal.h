@@ -1,0 +1,108 @@
+// Internal structures shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <set>
+#include <vector>
+
+#include "../../include/octopus.h"
+
+namespace octo {
+
+// ---- host metadata of one segment (a maximal run of tokens owned by one branch) ----
+struct Segment {
+  int32_t parent = -1;
+  int32_t fork = 0;          // parent tokens it sees
+  int64_t created = 0;       // op sequence number
+  int32_t len = 0;
+  int32_t p0 = 0;            // position of its first token (before own mounts at m = 0)
+  int32_t p_next = 0;
+  int32_t refcount = 1;
+  bool cursor = true, pinned = false, frozen = false, dead = false, freed = false;
+  std::vector<int32_t> pages;
+  std::vector<int32_t> pos;
+  std::vector<int32_t> mounts;  // ids of the mounts this segment reads, creation order
+};
+
+struct MountRec {
+  int32_t reader, m, producer, a, b;
+  int32_t jump;     // position jump the mount applied: new p - old p (>= 0)
+  int64_t created;
+};
+
+// Device-side mirror of the pool metadata used by the compiler kernels.
+struct DevSeg {
+  int32_t parent, fork, len, page_off;   // page_off: first own page in dev pages[]
+  int32_t mount_off, mount_cnt;          // own mounts in dev mounts[]
+  int32_t p0;
+  int32_t created_lo;                    // creation sequence (fits 31 bits per pool)
+};
+struct DevMount {
+  int32_t m, created, producer, a, b, id, jump, pad;
+};
+
+}  // namespace octo
+
+struct octo_pool_s {
+  octo_pool_desc desc;
+  std::vector<octo::Segment> segs;
+  std::vector<octo::MountRec> mounts;
+  std::set<int32_t> free_pages;
+  int64_t seq = 0;
+  int32_t* d_status = nullptr;   // device status word (bounded waits), shared by plans
+};
+
+struct octo_plan_s {
+  octo_pool_s* pool;
+  octo_plan_info_t info;
+  int32_t num_pages;
+  // device arrays (owned)
+  int32_t* seg_order = nullptr;      // [n_segments]
+  int32_t* seg_row_base = nullptr;   // [n_segments]
+  int32_t* row_pos = nullptr;        // [n_rows]
+  int32_t* tile_seg = nullptr;       // [n_tiles] segment id
+  int32_t* tile_t0 = nullptr;        // [n_tiles] first own row index of the segment
+  int32_t* tile_rows = nullptr;      // [n_tiles]
+  int32_t* tile_row0 = nullptr;      // [n_tiles] first packed row
+  int32_t* tile_off = nullptr;       // [n_tiles+1]
+  octo_entry* entries = nullptr;     // [n_entries]
+  int32_t* csc_perm = nullptr;       // [n_entries]
+  int32_t* page_off = nullptr;       // [num_pages+1]
+  int32_t* touched = nullptr;        // [n_touched_pages] pages with >= 1 entry, ascending
+  int32_t* tile_order = nullptr;     // [n_tiles] tiles by descending entry count (scheduling)
+  int32_t* page_order = nullptr;     // [n_touched] touched pages by descending entry count
+  std::vector<void*> allocs;
+};
+
+namespace octo {
+
+extern thread_local int g_last_cuda_error;
+void count_launch(int n = 1);
+
+inline int cuda_status(cudaError_t e) {
+  if (e != cudaSuccess) {
+    g_last_cuda_error = (int)e;
+    return OCTO_ECUDA;
+  }
+  return OCTO_OK;
+}
+
+#define OCTO_CUDA(call)                                   \
+  do {                                                    \
+    int _st = ::octo::cuda_status(call);                  \
+    if (_st != OCTO_OK) return _st;                       \
+  } while (0)
+
+// kernels launched by the host pool code
+int launch_append_rows(const octo_pool_desc& d, const int32_t* d_dst_rows, int32_t n, const void* k,
+                       const void* v, cudaStream_t s);
+
+// plan compilation (compile.cu)
+int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t* seg_order, int32_t n_segs,
+                 bool is_decode, int32_t bm, cudaStream_t s, octo_plan_s** out);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace octo

@@ -414,3 +414,80 @@ def make_tensors(ep: Episode, Hq: int, Hkv: int, d: int, dtype: str, scale: floa
 def make_decode_q(n: int, Hq: int, d: int, dtype: str, scale: float, seed: int) -> np.ndarray:
     rng = np.random.default_rng(np.random.PCG64(seed + 0xDEC0DE))
     return _draw(rng, (n, Hq, d), scale, dtype)
+
+
+# --------------------------------------------------------------------------------------
+# counter-based generator for large workloads
+# --------------------------------------------------------------------------------------
+# Large benchmark tensors (hundreds of millions of values) are drawn from a counter-based
+# generator so that the GPU can fill them in place while the CPU side evaluates exactly
+# the same values for the few rows it checks.  Element e of stream s is
+#     x = (sum of twelve 16-bit uniforms) / 65536 - 6
+# (the classic twelve-uniform approximation of a unit normal: mean 0, variance 1), the
+# uniforms taken from the MurmurHash3 32-bit finalizer applied to (s, e, k).  Only
+# integer operations and exact power-of-two scalings are involved, so torch on any
+# device produces identical bits; values are then scaled by a power of two and rounded
+# to the stored dtype.
+
+_M32 = 0xFFFFFFFF
+_GOLD = 0x9E3779B9
+
+
+def _mul32(h, c):
+    lo = h & 0xFFFF
+    hi = h >> 16
+    return (lo * c + ((hi * (c & 0xFFFF)) << 16)) & _M32
+
+
+def _fmix32(h):
+    h = h ^ (h >> 16)
+    h = _mul32(h, 0x85EBCA6B)
+    h = h ^ (h >> 13)
+    h = _mul32(h, 0xC2B2AE35)
+    return h ^ (h >> 16)
+
+
+def hash_normal(stream: int, index, scale: float = 1.0):
+    """Values of stream `stream` at int64 element indices `index` (a torch tensor on any
+    device).  Returns float32 (scale must be a power of two for bit-identity)."""
+    import torch
+    e = index.to(torch.int64)
+    seed = ((stream * _GOLD) ^ 0x5BD1E995) & _M32
+    base = _fmix32((e & _M32) ^ _fmix32(((e >> 32) + seed) & _M32))
+    acc = torch.zeros_like(e)
+    for k in range(6):
+        u = _fmix32((base + (k + 1) * _GOLD) & _M32)
+        acc = acc + (u & 0xFFFF) + (u >> 16)
+    x = (acc - 6 * 65536).to(torch.float32) * (1.0 / 65536.0)
+    return x * scale
+
+
+def hash_fill(stream: int, shape, dtype, device, scale: float = 1.0, row_start: int = 0, chunk_rows: int = 65536):
+    """A tensor of `shape` whose flat element i holds hash_normal(stream, row_start *
+    row_size + i) * scale, rounded to dtype.  Filled in row chunks to bound memory."""
+    import torch
+    out = torch.empty(shape, dtype=dtype, device=device)
+    rows = shape[0]
+    row_size = 1
+    for s in shape[1:]:
+        row_size *= s
+    flat = out.view(rows, row_size)
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        idx = torch.arange((row_start + r0) * row_size, (row_start + r1) * row_size, device=device,
+                           dtype=torch.int64)
+        flat[r0:r1] = hash_normal(stream, idx, scale).view(r1 - r0, row_size).to(dtype)
+    return out
+
+
+def hash_rows(stream: int, rows, row_size: int, dtype, scale: float = 1.0):
+    """CPU values of selected rows (numpy int array of row ids) of a hash_fill tensor:
+    float64 array [len(rows), row_size] holding the dtype-rounded values."""
+    import torch
+    r = torch.as_tensor(np.asarray(rows, dtype=np.int64))
+    idx = (r[:, None] * row_size + torch.arange(row_size, dtype=torch.int64)[None, :]).reshape(-1)
+    x = hash_normal(stream, idx, scale).to(dtype).to(torch.float64)
+    return x.view(len(rows), row_size).numpy()
+
+
+STREAM_K, STREAM_V, STREAM_Q, STREAM_DO, STREAM_DECODE_Q = 1, 2, 3, 4, 5

@@ -1,0 +1,132 @@
+"""Test helpers: replay a synth.Episode into the library pool and into the oracle, and
+compare their outputs.  Test infrastructure only."""
+from __future__ import annotations
+
+import re
+import os
+
+import numpy as np
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# tolerances of the parity bar: |err| <= atol + rtol * |ref|
+TOL = {"f32": (1e-5, 1e-5), "bf16": (2e-2, 2e-2)}
+
+
+def header_symbols():
+    txt = open(os.path.join(ROOT, "include", "octopus.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(octo_[a-z_0-9]+)\s*\(", txt)))
+
+
+def replay_host(pool, ep):
+    """Replays the op log into a library pool without K/V (metadata only)."""
+    for op in ep.ops:
+        k = op[0]
+        if k == "root":
+            pool.root()
+        elif k == "append":
+            pool.append(op[1], op[2])
+        elif k == "fork":
+            pool.fork(op[1], op[2])
+        elif k == "mount":
+            pool.mount(*op[1:])
+        elif k == "rewind":
+            pool.rewind(op[1], op[2])
+        elif k == "done":
+            pool.done(op[1])
+        elif k == "release":
+            pool.release(op[1])
+        elif k == "unpin":
+            pool.unpin(op[1])
+
+
+def replay_device(pool, ep, K_dev, V_dev, stream=None):
+    """Replays the op log into a library pool, appending each token's K/V rows from
+    device tensors K_dev/V_dev [T, Hkv, d] (append order)."""
+    t = 0
+    for op in ep.ops:
+        k = op[0]
+        if k == "append":
+            _, c, n = op
+            pool.append(c, n, K_dev[t:t + n], V_dev[t:t + n], stream=stream)
+            t += n
+        elif k == "root":
+            pool.root()
+        elif k == "fork":
+            pool.fork(op[1], op[2])
+        elif k == "mount":
+            pool.mount(*op[1:])
+        elif k == "rewind":
+            pool.rewind(op[1], op[2])
+        elif k == "done":
+            pool.done(op[1])
+        elif k == "release":
+            pool.release(op[1])
+        elif k == "unpin":
+            pool.unpin(op[1])
+
+
+def compare_pools(pool, orc):
+    assert pool.info()["n_segments"] == orc.n_segments
+    assert pool.info()["free_pages"] == orc.free_pages()
+    assert pool.info()["n_mounts"] == orc.n_mounts
+    for s in range(orc.n_segments):
+        a, b = pool.seg_info(s), orc.seg_info(s)
+        assert a == b, (s, a, b)
+        assert np.array_equal(pool.seg_pos(s), orc.seg_pos(s)), s
+        assert np.array_equal(pool.seg_pages(s), orc.seg_pages(s)), s
+
+
+def oracle_entries(opl):
+    return opl.entries.astype(np.int64)
+
+
+def product_entries(ent):
+    return np.stack([ent[f].astype(np.int64) for f in ("q_tile", "kv_page", "kv_lo", "kv_hi", "q_lo", "flags",
+                                                         "diag", "src")], axis=1) if len(ent) else \
+        np.zeros((0, 8), dtype=np.int64)
+
+
+def compare_plans(gp, opl):
+    """Bit-exact comparison of a library plan (copy_out dict) with an oracle plan."""
+    assert np.array_equal(gp["seg_order"], opl.seg_order)
+    assert np.array_equal(gp["seg_row_base"], opl.seg_row_base)
+    assert np.array_equal(gp["row_pos"], opl.row_pos)
+    assert np.array_equal(gp["tile_seg"], opl.tile_seg)
+    assert np.array_equal(gp["tile_t0"], opl.tile_t0)
+    assert np.array_equal(gp["tile_rows"], opl.tile_rows)
+    assert np.array_equal(gp["tile_off"], opl.tile_off)
+    pe, oe = product_entries(gp["entries"]), oracle_entries(opl)
+    assert pe.shape == oe.shape, (pe.shape, oe.shape)
+    if not np.array_equal(pe, oe):
+        bad = np.nonzero((pe != oe).any(1))[0][:5]
+        raise AssertionError("entries differ at %s:\nlib %s\noracle %s" % (bad, pe[bad], oe[bad]))
+    assert np.array_equal(gp["csc_perm"], opl.csc_perm)
+    assert np.array_equal(gp["page_off"], opl.page_off)
+
+
+def assert_close(got, ref, dtype, what=""):
+    atol, rtol = TOL[dtype]
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(got - ref)
+    bound = atol + rtol * np.abs(ref)
+    bad = err > bound
+    if bad.any():
+        i = np.argmax(err - bound)
+        raise AssertionError("%s: %d of %d outside |err| <= %g + %g|ref|; worst at %s: got %r ref %r" % (
+            what, int(bad.sum()), bad.size, atol, rtol, np.unravel_index(i, got.shape), got.flat[i], ref.flat[i]))
+
+
+def packed(t, seg_order, arr):
+    if len(seg_order) == 0:
+        return arr[:0]
+    return np.concatenate([arr[t.seg_off[s]:t.seg_off[s + 1]] for s in seg_order], axis=0)
+
+
+def pool_pages_needed(ep):
+    P = ep.page_size
+    return sum((L + P - 1) // P for L in ep.length) + 4

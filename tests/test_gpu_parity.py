@@ -1,0 +1,253 @@
+"""GPU parity: the library's plans, forward, backward and decode against the fp64 oracle
+on the same seeded inputs, through the C ABI.  Plans and pool tables are compared bit for
+bit; values within |err| <= 1e-5 + 1e-5|ref| (fp32 pools) or 2e-2 + 2e-2|ref| (bf16)."""
+import math
+
+import numpy as np
+import pytest
+
+import synth
+from helpers import (assert_close, compare_plans, compare_pools, packed, pool_pages_needed, product_entries,
+                     replay_device)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import packed_tree_attention_gb300 as pta
+    pta.load()
+    return pta
+
+
+class Run:
+    """An episode replayed into both the oracle and the library, with its tensors."""
+
+    def __init__(self, lib, oracle_mod, ep, Hq, Hkv, d, dtype, seed, bm=None, npages=None, with_kv=True):
+        self.ep, self.Hq, self.Hkv, self.d, self.dtype = ep, Hq, Hkv, d, dtype
+        P = ep.page_size
+        self.P = P
+        self.npages = npages or pool_pages_needed(ep)
+        self.t = synth.make_tensors(ep, Hq, Hkv, d, dtype, 1.0 if dtype == "f32" else 0.5, seed)
+        tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+        self.tdt = tdt
+        dev = "cuda"
+        self.kpool = torch.zeros((self.npages, Hkv, P, d), dtype=tdt, device=dev)
+        self.vpool = torch.zeros_like(self.kpool)
+        self.pool = lib.Pool(self.npages, P, Hkv, d, lib.DTYPE_F32 if dtype == "f32" else lib.DTYPE_BF16,
+                             self.kpool, self.vpool)
+        K = torch.from_numpy(self.t.K).to(dev).to(tdt)
+        V = torch.from_numpy(self.t.V).to(dev).to(tdt)
+        replay_device(self.pool, ep, K, V)
+        torch.cuda.synchronize()
+        self.orc = oracle_mod.Oracle(P, self.npages, Hkv, d)
+        self.orc.replay(ep, self.t.K.astype(np.float64), self.t.V.astype(np.float64))
+        self.scale = 1.0 / math.sqrt(d)
+
+    def pack(self, bm, tile_stride=1):
+        self.bm = bm
+        self.plan = self.pool.pack_tree(self.ep.roots, bm)
+        self.opl = self.orc.pack(self.ep.roots, bm, tile_stride)
+        self.Q = packed(self.t, self.opl.seg_order, self.t.Q)
+        self.dO = packed(self.t, self.opl.seg_order, self.t.dO)
+        return self.plan, self.opl
+
+    def dev(self, a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda().to(self.tdt)
+
+    def fwd(self):
+        N = self.plan.info["n_rows"]
+        q = self.dev(self.Q)
+        o = torch.empty((N, self.Hq, self.d), dtype=self.tdt, device="cuda")
+        lse = torch.empty((self.Hq, N), dtype=torch.float32, device="cuda")
+        self.plan.attn_fwd(self.Hq, q, o, lse, self.scale)
+        self.plan.sync()
+        self.q_dev, self.o_dev, self.lse_dev = q, o, lse
+        return o.float().cpu().numpy(), lse.cpu().numpy()
+
+    def bwd(self):
+        N = self.plan.info["n_rows"]
+        do = self.dev(self.dO)
+        dq = torch.empty((N, self.Hq, self.d), dtype=torch.float32, device="cuda")
+        dk = torch.full((self.npages, self.Hkv, self.P, self.d), float("nan"), device="cuda")
+        dv = torch.full_like(dk, float("nan"))
+        ws = torch.empty(max(1, self.plan.attn_bwd_workspace_size(self.Hq)), dtype=torch.uint8, device="cuda")
+        self.plan.attn_bwd(self.Hq, self.q_dev, self.o_dev, self.lse_dev, do, dq, dk, dv, self.scale, ws)
+        self.plan.sync()
+        return dq.cpu().numpy(), dk.cpu().numpy(), dv.cpu().numpy()
+
+    def token_slots(self):
+        seg, idx = self.orc.token_owner()
+        pages = {s: self.orc.seg_pages(s) for s in set(seg.tolist())}
+        page = np.array([pages[s][i // self.P] for s, i in zip(seg.tolist(), idx.tolist())], dtype=np.int64)
+        return page, idx % self.P
+
+
+# ------------------------------------------------------------------ plans, bit-exact
+@pytest.mark.parametrize("seed", range(12))
+def test_plan_random(lib, oracle_mod, seed):
+    P = [4, 8, 16, 64][seed % 4]
+    bm = [16, 32, 64, 128, 1, 48][seed % 6]
+    ep = synth.random_dag(300 + seed, page_size=P, max_segments=14, max_len=[40, 90, 200][seed % 3],
+                          n_roots=1 + seed % 3)
+    r = Run(lib, oracle_mod, ep, 2, 1, 64, "f32", seed)
+    compare_pools(r.pool, r.orc)
+    plan, opl = r.pack(bm)
+    compare_plans(plan.copy_out(), opl)
+    assert plan.info["pairs"] == opl.pairs == opl.total_pairs()
+
+
+@pytest.mark.parametrize("bm", [32, 128])
+def test_plan_tiny(lib, oracle_mod, bm):
+    ep = synth.make_preset("tiny")
+    r = Run(lib, oracle_mod, ep, 1, 1, 64, "f32", 0)
+    plan, opl = r.pack(bm)
+    compare_plans(plan.copy_out(), opl)
+    assert plan.info["pairs"] == 7488
+
+
+def test_plan_tree_fwd_full(lib, oracle_mod):
+    ep = synth.make_preset("tree_fwd")
+    r = Run(lib, oracle_mod, ep, 16, 4, 128, "bf16", 0)
+    plan, opl = r.pack(128)
+    compare_plans(plan.copy_out(), opl)
+    assert plan.info["pairs"] == opl.pairs
+
+
+@pytest.mark.parametrize("name,stride", [("episode", 7), ("decode", 97)])
+def test_plan_full_size_sampled(lib, oracle_mod, name, stride):
+    """Full-size episodes: every tile's layout, positions and the total pair count are
+    compared; entries on a sample of tiles the oracle derives one by one."""
+    ep = synth.make_preset(name, seed=0)
+    r = Run(lib, oracle_mod, ep, 1, 1, 64, "f32", 0)   # K/V values do not matter for plans
+    plan, opl = r.pack(128, tile_stride=stride)
+    gp = plan.copy_out()
+    for k in ("seg_order", "seg_row_base", "row_pos", "tile_seg", "tile_t0", "tile_rows"):
+        assert np.array_equal(gp[k], getattr(opl, k)), k
+    assert plan.info["pairs"] == opl.total_pairs()
+    pe = product_entries(gp["entries"])
+    ot = opl.tile_off
+    oe = opl.entries.astype(np.int64)
+    for t in range(0, len(gp["tile_rows"]), stride):
+        mine = pe[gp["tile_off"][t]:gp["tile_off"][t + 1]]
+        want = oe[ot[t]:ot[t + 1]]
+        assert np.array_equal(mine, want), t
+    # CSC: every page's list is its entries in increasing entry order
+    perm, poff = gp["csc_perm"], gp["page_off"]
+    assert np.array_equal(np.sort(perm), np.arange(len(perm)))
+    pages = pe[perm, 1]
+    assert np.all(np.diff(pages) >= 0)
+    same = pages[1:] == pages[:-1]
+    assert np.all(np.diff(perm)[same] > 0)
+    assert np.array_equal(np.bincount(pe[:, 1], minlength=r.npages), np.diff(poff))
+
+
+def test_decode_plan(lib, oracle_mod):
+    ep = synth.random_dag(77, page_size=16, max_segments=14, max_len=70)
+    r = Run(lib, oracle_mod, ep, 4, 2, 64, "f32", 1)
+    curs = [s for s in range(r.orc.n_segments) if r.orc.seg_info(s)["len"] > 0]
+    dp = r.pool.decode_plan(curs)
+    gp = dp.copy_out()
+    # a decode row is the last row of its segment: its context is that row's context,
+    # so its entries are the oracle's entries of a one-row tile -- compare by pairs
+    opl = r.orc.pack(ep.roots, 1)
+    rows = {int(s): int(b) + r.orc.seg_info(int(s))["len"] - 1 for s, b in zip(opl.seg_order, opl.seg_row_base)}
+    oe = opl.entries.astype(np.int64)
+    pe = product_entries(gp["entries"])
+    for i, c in enumerate(curs):
+        t = rows[c]           # bm = 1: tile index == packed row
+        want = oe[opl.tile_off[t]:opl.tile_off[t + 1]].copy()
+        mine = pe[gp["tile_off"][i]:gp["tile_off"][i + 1]].copy()
+        want[:, 0] = 0
+        mine[:, 0] = 0
+        assert np.array_equal(mine, want), c
+        assert gp["row_pos"][i] == opl.row_pos[t]
+
+
+# ------------------------------------------------------------------ values
+def _check_fwd_bwd(r, do_bwd=True):
+    O, LSE = r.fwd()
+    Oo, Lo = r.opl.fwd(r.Q.astype(np.float64), r.scale, nthreads=8)
+    assert_close(O, Oo, r.dtype, "O")
+    assert_close(LSE, Lo, r.dtype, "LSE")
+    if not do_bwd:
+        return
+    dq, dk, dv = r.bwd()
+    dQo, dKo, dVo = r.opl.bwd(r.Q.astype(np.float64), r.dO.astype(np.float64), r.scale, nthreads=8)
+    assert_close(dq, dQo, r.dtype, "dQ")
+    page, slot = r.token_slots()
+    assert_close(dk[page, :, slot, :], dKo, r.dtype, "dK")
+    assert_close(dv[page, :, slot, :], dVo, r.dtype, "dV")
+    # slots of touched pages that hold no token read by any row are zero
+    gp = r.plan.copy_out()
+    touched = np.nonzero(np.diff(gp["page_off"]))[0]
+    mask = np.zeros((r.npages, r.P), dtype=bool)
+    mask[page, slot] = True
+    for p in touched:
+        for j in np.nonzero(~mask[p])[0]:
+            assert np.all(dk[p, :, j] == 0) and np.all(dv[p, :, j] == 0)
+
+
+def test_tiny_fp32(lib, oracle_mod):
+    r = Run(lib, oracle_mod, synth.make_preset("tiny"), 1, 1, 64, "f32", 0)
+    r.pack(32)
+    _check_fwd_bwd(r)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_fp32(lib, oracle_mod, seed):
+    P = [8, 16][seed % 2]
+    ep = synth.random_dag(400 + seed, page_size=P, max_segments=12, max_len=90, n_roots=1 + seed % 2)
+    r = Run(lib, oracle_mod, ep, [2, 4][seed % 2], [1, 2][seed % 2], [64, 128][seed % 2], "f32", seed)
+    r.pack([32, 16, 128][seed % 3])
+    _check_fwd_bwd(r)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_bf16_gqa(lib, oracle_mod, seed):
+    """bf16, 16 q heads over 4 kv heads, head_dim 128, page 64, q-tile 128: several tiles
+    per segment, ragged tails, partial pages, mounts, rewinds."""
+    ep = synth.random_dag(500 + seed, page_size=64, max_segments=10, max_len=400, n_roots=1 + seed % 2)
+    r = Run(lib, oracle_mod, ep, 16, 4, 128, "bf16", seed)
+    r.pack(128)
+    _check_fwd_bwd(r)
+
+
+def test_tree_fwd_sampled_rows(lib, oracle_mod):
+    """The full-size bf16 tree (fwd only): all outputs computed; the oracle checks a
+    seeded sample of rows, covering every segment's first, last and mounted rows."""
+    ep = synth.make_preset("tree_fwd")
+    r = Run(lib, oracle_mod, ep, 16, 4, 128, "bf16", 0)
+    r.pack(128)
+    O, LSE = r.fwd()
+    rng = np.random.default_rng(0)
+    rows = set(rng.integers(0, r.plan.info["n_rows"], 48).tolist())
+    for s, b in zip(r.opl.seg_order, r.opl.seg_row_base):
+        L = r.orc.seg_info(int(s))["len"]
+        rows.update([int(b), int(b) + L - 1, int(b) + min(L - 1, 4096)])
+    rows = np.array(sorted(rows), dtype=np.int32)
+    Oo, Lo = r.opl.fwd(r.Q.astype(np.float64), r.scale, rows=rows, nthreads=8)
+    assert_close(O[rows], Oo[rows], "bf16", "O")
+    assert_close(LSE[:, rows], Lo[:, rows], "bf16", "LSE")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_values(lib, oracle_mod, dtype):
+    ep = synth.random_dag(91, page_size=16 if dtype == "f32" else 64, max_segments=14, max_len=300)
+    Hq, Hkv, d = (4, 2, 64) if dtype == "f32" else (16, 4, 128)
+    r = Run(lib, oracle_mod, ep, Hq, Hkv, d, dtype, 3)
+    curs = [s for s in range(r.orc.n_segments) if r.orc.seg_info(s)["len"] > 0]
+    q = synth.make_decode_q(len(curs), Hq, d, dtype, 0.5, 9)
+    dp = r.pool.decode_plan(curs)
+    out = torch.empty((len(curs), Hq, d), dtype=r.tdt, device="cuda")
+    lse = torch.empty((len(curs), Hq), dtype=torch.float32, device="cuda")
+    ws_n = dp.decode_workspace_size(Hq)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device="cuda")
+    dp.decode(Hq, r.dev(q), out, lse, r.scale, ws, ws_n)
+    dp.sync()
+    want, wl = r.orc.decode(curs, q.astype(np.float64), r.scale)
+    assert_close(out.float().cpu().numpy(), want, dtype, "decode out")
+    assert_close(lse.cpu().numpy(), wl, dtype, "decode lse")

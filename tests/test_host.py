@@ -1,0 +1,117 @@
+"""Host-side tests (no GPU): the C-ABI library loads and exports every symbol the
+header declares, and its pool metadata (pages, refcounts, positions, cursor states,
+error codes) matches the oracle's independent model bit for bit."""
+import numpy as np
+import pytest
+
+import synth
+from helpers import compare_pools, header_symbols, replay_host
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import packed_tree_attention_gb300 as pta
+    pta.load()
+    return pta
+
+
+def test_exports_every_header_symbol(lib):
+    L = lib.load()
+    syms = header_symbols()
+    assert len(syms) >= 20
+    for s in syms:
+        assert hasattr(L, s), s
+    assert set(syms) == set(lib.SYMBOLS)
+
+
+def test_strerror(lib):
+    L = lib.load()
+    for code in range(7):
+        assert L.octo_strerror(code)
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_pool_matches_oracle(lib, oracle_mod, seed):
+    ep = synth.random_dag(seed, page_size=[4, 8, 16][seed % 3], max_segments=12, max_len=60,
+                          n_roots=1 + seed % 2)
+    npages = sum((L + ep.page_size - 1) // ep.page_size for L in ep.length) + 3
+    pool = lib.Pool(npages, ep.page_size, 2, 64, lib.DTYPE_F32)
+    orc = oracle_mod.Oracle(ep.page_size, npages, 2, 64)
+    replay_host(pool, ep)
+    orc.replay(ep)
+    compare_pools(pool, orc)
+    # now release everything in a seeded order, comparing after each step
+    rng = np.random.default_rng(seed)
+    live = [s for s in range(orc.n_segments) if orc.seg_info(s)["flags"] & 1]
+    rng.shuffle(live)
+    for c in live:
+        assert pool.release(c, check=False) == orc.release(c, check=False)
+        compare_pools(pool, orc)
+    pinned = [s for s in range(orc.n_segments) if orc.seg_info(s)["flags"] & 2]
+    for c in pinned:
+        assert pool.unpin(c, check=False) == orc.unpin(c, check=False)
+        compare_pools(pool, orc)
+    assert pool.info()["free_pages"] == npages
+
+
+def test_presets_match_oracle(lib, oracle_mod):
+    for name in ("tiny", "tree_fwd", "episode", "decode"):
+        ep = synth.make_preset(name, seed=1)
+        npages = sum((L + ep.page_size - 1) // ep.page_size for L in ep.length) + 1
+        pool = lib.Pool(npages, ep.page_size, 1, 64, lib.DTYPE_F32)
+        orc = oracle_mod.Oracle(ep.page_size, npages, 1, 64)
+        replay_host(pool, ep)
+        orc.replay(ep)
+        compare_pools(pool, orc)
+
+
+def test_error_codes_match_oracle(lib, oracle_mod):
+    """Invalid operations give the same status on both sides and change nothing."""
+    rng = np.random.default_rng(0)
+    for trial in range(40):
+        ep = synth.random_dag(1000 + trial, page_size=4, max_segments=8, max_len=20)
+        npages = sum((L + 3) // 4 for L in ep.length) + 2
+        pool = lib.Pool(npages, 4, 1, 64, lib.DTYPE_F32)
+        orc = oracle_mod.Oracle(4, npages, 1, 64)
+        replay_host(pool, ep)
+        orc.replay(ep)
+        n = orc.n_segments
+        for _ in range(30):
+            kind = rng.integers(0, 6)
+            c = int(rng.integers(-1, n + 1))
+            if kind == 0:
+                p = int(rng.integers(-1, n + 1))
+                a = int(rng.integers(-2, 25)); b = int(rng.integers(-2, 25))
+                r1 = pool.mount(c, p, a, b, check=False)
+                r2 = orc.mount(c, p, a, b, check=False)
+            elif kind == 1:
+                k = int(rng.integers(-2, 25))
+                r1 = pool.rewind(c, k, check=False)
+                r2 = orc.rewind(c, k, check=False)
+            elif kind == 2:
+                nn = int(rng.integers(0, 12))
+                r1 = pool.append(c, nn, check=False)
+                r2 = orc.append(c, nn, check=False)
+            elif kind == 3:
+                r1 = pool.done(c, check=False); r2 = orc.done(c, check=False)
+            elif kind == 4:
+                r1 = pool.release(c, check=False); r2 = orc.release(c, check=False)
+            else:
+                r1 = pool.unpin(c, check=False); r2 = orc.unpin(c, check=False)
+            assert r1 == r2, (kind, c, r1, r2)
+            compare_pools(pool, orc)
+
+
+def test_append_all_or_nothing(lib, oracle_mod):
+    pool = lib.Pool(3, 4, 1, 64, lib.DTYPE_F32)
+    orc = oracle_mod.Oracle(4, 3, 1, 64)
+    for x in (pool, orc):
+        r = x.root()
+        x.append(r, 10)
+    assert pool.append(0, 3, check=False) == lib.ENOMEM
+    assert orc.append(0, 3, check=False) == oracle_mod.ENOMEM
+    compare_pools(pool, orc)
+    assert pool.append(0, 2, check=False) == lib.OK
+    orc.append(0, 2)
+    compare_pools(pool, orc)
+
