@@ -70,7 +70,7 @@ def _load():
         L.orc_plan_size.argtypes = [P, I]
         L.orc_plan_arrays.argtypes = [P] + [IP] * 10
         L.orc_fwd.argtypes = [P, I, DP, ctypes.c_double, IP, I, DP, DP, I]
-        L.orc_bwd.argtypes = [P, I, DP, DP, ctypes.c_double, UP, UP, DP, DP, DP, I]
+        L.orc_bwd.argtypes = [P, I, DP, DP, ctypes.c_double, UP, UP, DP, DP, DP, I, I]
         L.orc_decode.argtypes = [P, IP, I, I, DP, ctypes.c_double, DP, DP]
         L.orc_row_context.argtypes = [P, I, IP, IP, I]
         L.orc_token_owner.argtypes = [P, IP, IP]
@@ -311,7 +311,7 @@ class OraclePlan:
             raise OracleError(st, "fwd")
         return O, LSE
 
-    def bwd(self, Q, dO, scale, need_dq=None, need_dkdv=None, nthreads=0):
+    def bwd(self, Q, dO, scale, need_dq=None, need_dkdv=None, nthreads=0, partial=False):
         """Returns dQ [N,Hq,d] and dK, dV per token id [T,Hkv,d]."""
         Q = np.ascontiguousarray(Q, dtype=np.float64)
         dO = np.ascontiguousarray(dO, dtype=np.float64)
@@ -323,7 +323,7 @@ class OraclePlan:
         nq = None if need_dq is None else np.ascontiguousarray(need_dq, dtype=np.uint8)
         nk = None if need_dkdv is None else np.ascontiguousarray(need_dkdv, dtype=np.uint8)
         st = self.orc._L.orc_bwd(self.h, Hq, _dp(Q), _dp(dO), scale, _up(nq), _up(nk),
-                                 _dp(dQ), _dp(dK), _dp(dV), nthreads)
+                                 _dp(dQ), _dp(dK), _dp(dV), nthreads, 1 if partial else 0)
         if st != OK:
             raise OracleError(st, "bwd")
         return dQ, dK, dV

@@ -647,11 +647,12 @@ int orc_fwd(void* p, int Hq, const double* Q, double scale, const int* rows, int
 
 // Backward.  dQ: [N, Hq, d] for rows with need_dq[r]; dK, dV: [T, Hkv, d] per token id,
 // the adjoint of every copied context entry summed back onto its owner token, for
-// tokens with need_dkdv[t] (null = all).  Rows are processed in packed order and the
+// tokens with need_dkdv[t] (null = all).  With `partial`, only the need_dq rows are
+// processed and dK/dV hold their contributions alone (used to time a row sample).  Rows are processed in packed order and the
 // sums are taken in that order, one kv head at a time.
 int orc_bwd(void* p, int Hq, const double* Q, const double* dO, double scale,
             const unsigned char* need_dq, const unsigned char* need_dkdv,
-            double* dQ, double* dK, double* dV, int nthreads) {
+            double* dQ, double* dK, double* dV, int nthreads, int partial) {
   Plan* pl = static_cast<Plan*>(p);
   const Oracle& o = *pl->o;
   if (Hq % o.Hkv) return ORC_EINVAL;
@@ -664,6 +665,7 @@ int orc_bwd(void* p, int Hq, const double* Q, const double* dO, double scale,
   std::vector<char> need_row(N, 0);
   for (long long r = 0; r < N; r++) {
     if (need_dq == nullptr || need_dq[r]) { need_row[r] = 1; continue; }
+    if (partial) continue;   // dK/dV from the dq rows only (a sample of the full sums)
     if (need_dkdv == nullptr) { need_row[r] = 1; continue; }
     const std::vector<CtxItem>& ctx = ctxs.at(pl->row_seg[r]);
     for (const CtxItem& c : ctx)
