@@ -110,8 +110,10 @@ typedef struct {
 
 /* ---- pool (host metadata; primitives table of the project page) ---- */
 
-/* Creates a pool.  All pages start free.  EINVAL on a bad description. */
+/* Creates a pool.  All pages start free.  EINVAL on a bad description.  No device
+ * memory is touched until the first plan is compiled. */
 int octo_pool_create(const octo_pool_desc* desc, octo_pool_t* out);
+/* Destroys the pool (waits for the device first).  Its plans must be destroyed before. */
 int octo_pool_destroy(octo_pool_t pool);
 
 /* New root segment with a live cursor; positions start at 0. */
@@ -192,6 +194,9 @@ int octo_plan_copy_out(octo_plan_t plan, int32_t* seg_order, int32_t* seg_row_ba
                        int32_t* row_pos, int32_t* tile_seg, int32_t* tile_t0,
                        int32_t* tile_rows, int32_t* tile_off, octo_entry* entries,
                        int32_t* csc_perm, int32_t* page_off);
+/* Frees the plan's device arrays in stream order on the stream of the last call that
+ * used the plan, so it may be called while that work is still running; work using the
+ * plan on any other stream must have completed. */
 int octo_plan_destroy(octo_plan_t plan);
 
 /* ---- attention (device, async on stream) ---- */

@@ -1,6 +1,8 @@
 // Attention entry points: argument checks and dispatch between the tensor-core kernels
 // (bf16, head_dim 128, page 64, q-tile 128) and the CUDA-core kernels (everything else).
 
+#include <cstdlib>
+
 #include "internal.h"
 
 namespace octo {
@@ -9,9 +11,23 @@ int fwd_simt(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, con
 int bwd_simt(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const void* v, const void* o,
              const float* lse, const void* dout, float* dq, float* dk, float* dv, float scale, void* ws,
              cudaStream_t s);
+bool fwd_tc_supported(const octo_plan_s* p, int32_t Hq);
+int fwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const void* v, void* o, float* lse,
+           float scale, cudaStream_t s);
 }  // namespace octo
 
 namespace {
+
+// OCTO_DISABLE_TC=1 routes every call to the CUDA-core kernels (a diagnostic for
+// comparing the two kernel families on the same shapes).
+bool tc_disabled() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("OCTO_DISABLE_TC");
+    v = (e && *e && *e != '0') ? 1 : 0;
+  }
+  return v == 1;
+}
 
 int check_heads(const octo_plan_s* p, int32_t Hq) {
   const int32_t Hkv = p->pool->desc.n_kv_heads;
@@ -24,9 +40,9 @@ int check_heads(const octo_plan_s* p, int32_t Hq) {
 extern "C" {
 
 int octo_kernel_path(octo_plan_t plan, int32_t n_q_heads, int32_t which) {
-  if (!plan) return -1;
-  (void)n_q_heads;
-  (void)which;
+  if (!plan || check_heads(plan, n_q_heads)) return -1;
+  if (tc_disabled()) return 0;
+  if (which == 0) return octo::fwd_tc_supported(plan, n_q_heads) ? 1 : 0;
   return 0;
 }
 
@@ -38,6 +54,9 @@ int octo_attn_fwd(octo_plan_t plan, int32_t Hq, const void* q, const void* k_poo
   const void* k = k_pool ? k_pool : plan->pool->desc.k_pool;
   const void* v = v_pool ? v_pool : plan->pool->desc.v_pool;
   if (plan->info.n_entries > 0 && (!k || !v)) return OCTO_EINVAL;
+  plan->last_stream = (cudaStream_t)stream;
+  if (!tc_disabled() && octo::fwd_tc_supported(plan, Hq))
+    return octo::fwd_tc(plan, Hq, q, k, v, o, lse, scale, (cudaStream_t)stream);
   return octo::fwd_simt(plan, Hq, q, k, v, o, lse, scale, false, (cudaStream_t)stream);
 }
 
@@ -58,6 +77,7 @@ int octo_attn_bwd(octo_plan_t plan, int32_t Hq, const void* q, const void* k_poo
   const void* k = k_pool ? k_pool : plan->pool->desc.k_pool;
   const void* v = v_pool ? v_pool : plan->pool->desc.v_pool;
   if (plan->info.n_entries > 0 && (!k || !v)) return OCTO_EINVAL;
+  plan->last_stream = (cudaStream_t)stream;
   return octo::bwd_simt(plan, Hq, q, k, v, o, lse, dout, dq, dk_pool, dv_pool, scale, ws, (cudaStream_t)stream);
 }
 
@@ -76,6 +96,7 @@ int octo_decode(octo_plan_t plan, int32_t Hq, const void* q, const void* k_pool,
   const void* k = k_pool ? k_pool : plan->pool->desc.k_pool;
   const void* v = v_pool ? v_pool : plan->pool->desc.v_pool;
   if (plan->info.n_entries > 0 && (!k || !v)) return OCTO_EINVAL;
+  plan->last_stream = (cudaStream_t)stream;
   return octo::fwd_simt(plan, Hq, q, k, v, out, lse, scale, true, (cudaStream_t)stream);
 }
 

@@ -1,0 +1,431 @@
+// Packed DAG attention forward on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// Octopus project page, "Architecture & Co-Design" item 03: one unpadded 1D pass over
+// the packed tree; every row attends to its ancestor path and its mounted spans.  The
+// compiled plan lists, per 128-row q-tile, the (page, source) blocks of visible keys;
+// this kernel runs them as a block-sparse flash-attention forward.
+//
+// One CTA = one q-tile x two query heads of one kv-head group (GQA: the pair shares each
+// K/V page it loads).  Warp roles (384 threads):
+//   warp 0      TMA producer: Q once (2 heads x 128 rows x 128 d), then K and V of each
+//               entry's page through a 3-stage ring
+//   warp 1      MMA issuer (one thread): S_h = Q_h K^T (M128 N64 K16 x8) and
+//               O_h += P_h V (M128 N128 K16 x4), accumulators in TMEM
+//   warp 2      TMEM allocator (512 columns: O_0, O_1, S_0, S_1)
+//   warps 4-7   softmax of head 0, warps 8-11 softmax of head 1: one row per thread,
+//               S read with tcgen05.ld, mask from the entry rectangle, online softmax
+//               in the log2 domain with lazy rescaling (O is rescaled in TMEM only when
+//               the running max grows by more than 2^8), P written to shared memory in
+//               the 128-byte-swizzled K-major layout the MMA reads
+// The two heads' softmax warpgroups run half an entry apart, so the tensor core
+// alternates between them.  Every mbarrier wait is bounded; on expiry the kernel
+// records OCTO_ETIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace octo {
+namespace {
+
+using namespace tc;
+
+constexpr int kNS = 3;
+constexpr int kThreads = 384;
+constexpr uint32_t kQBytes = 2 * 2 * 128 * 128;     // 2 heads x 2 chunks x 128 rows x 128 B
+constexpr uint32_t kKVStage = 2 * 2 * 64 * 128;     // K + V, 2 chunks x 64 rows x 128 B each
+constexpr uint32_t kPBytes = 2 * 128 * 128;         // 2 heads x 128 rows x 128 B
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffKV = kOffQ + kQBytes;
+constexpr uint32_t kOffP = kOffKV + kNS * kKVStage;
+constexpr uint32_t kOffBar = kOffP + kPBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+
+constexpr uint32_t kIdS = idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t kIdO = idesc_bf16(128, 128, 0, 1);
+
+struct FwdTcParams {
+  const int32_t* tile_off;
+  const int32_t* tile_rows;
+  const int32_t* tile_row0;
+  const octo_entry* entries;
+  __nv_bfloat16* o;
+  float* lse;
+  int64_t n_rows;
+  int32_t Hq, Hkv, G;
+  float scale_log2;
+  int32_t* status;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t kv_full[kNS];
+  uint64_t kv_empty[kNS];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int32_t abort;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* B, int32_t* status) {
+  for (uint32_t i = 0; i < kSpinLimit; i++) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 1023) == 1023 && B->abort) return false;
+  }
+  B->abort = 1;
+  atomicExch(status, OCTO_ETIMEOUT);
+  return false;
+}
+
+// the same wait in every lane of a warp, with a warp-uniform result (the tcgen05
+// .sync.aligned loads and stores that follow need the whole warp)
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Bars* B, int32_t* status) {
+  return __all_sync(0xffffffffu, wait_or_abort(bar, parity, B, status));
+}
+
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+             const __grid_constant__ CUtensorMap tmV, FwdTcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* B = reinterpret_cast<Bars*>(smem + kOffBar);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int32_t HP = p.G >> 1;
+  const int32_t hp = blockIdx.x % HP;
+  const int32_t g = (blockIdx.x / HP) % p.Hkv;
+  const int32_t tile = blockIdx.x / (HP * p.Hkv);
+  const int32_t h0 = g * p.G + 2 * hp;
+  const int32_t e0 = p.tile_off[tile];
+  const int32_t n = p.tile_off[tile + 1] - e0;
+  const int32_t rows = p.tile_rows[tile];
+  const int32_t row0 = p.tile_row0[tile];
+
+  if (threadIdx.x == 0) {
+    mbar_init(&B->q_full, 1);
+    for (int s = 0; s < kNS; s++) {
+      mbar_init(&B->kv_full[s], 1);
+      mbar_init(&B->kv_empty[s], 1);
+    }
+    for (int h = 0; h < 2; h++) {
+      mbar_init(&B->s_full[h], 1);
+      mbar_init(&B->s_free[h], 128);
+      mbar_init(&B->p_full[h], 128);
+      mbar_init(&B->o_done[h], 1);
+    }
+    mbar_init(&B->drain, 1);
+    B->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&B->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = B->tmem_base;
+
+  const uint32_t sQ = smem_u32(smem + kOffQ);
+  const uint32_t sKV = smem_u32(smem + kOffKV);
+  const uint32_t sP = smem_u32(smem + kOffP);
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && n > 0) {
+      prefetch_map(&tmQ);
+      prefetch_map(&tmK);
+      prefetch_map(&tmV);
+      mbar_expect_tx(&B->q_full, kQBytes);
+      for (int hh = 0; hh < 2; hh++)
+        for (int c = 0; c < 2; c++)
+          tma_load_3d(smem + kOffQ + (hh * 2 + c) * 16384, &tmQ, &B->q_full, c * 64, h0 + hh, row0);
+      int32_t issued = 0;
+      for (int32_t j = 0; j < n; j++) {
+        const int st = j % kNS;
+        if (j >= kNS && !wait_or_abort(&B->kv_empty[st], ((j / kNS) - 1) & 1, B, p.status)) break;
+        const octo_entry e = p.entries[e0 + j];
+        const int32_t krow = (int32_t)((e.kv_page * (uint32_t)p.Hkv + (uint32_t)g) * 64u);
+        uint8_t* kd = smem + kOffKV + st * kKVStage;
+        mbar_expect_tx(&B->kv_full[st], kKVStage);
+        tma_load_2d(kd, &tmK, &B->kv_full[st], 0, krow);
+        tma_load_2d(kd + 8192, &tmK, &B->kv_full[st], 64, krow);
+        tma_load_2d(kd + 16384, &tmV, &B->kv_full[st], 0, krow);
+        tma_load_2d(kd + 24576, &tmV, &B->kv_full[st], 64, krow);
+        issued = j + 1;
+      }
+      // drain: every copy this thread started has landed before the CTA may exit
+      mbar_wait(&B->q_full, 0, p.status, OCTO_ETIMEOUT);
+      for (int32_t j = max(0, issued - kNS); j < issued; j++)
+        mbar_wait(&B->kv_full[j % kNS], (j / kNS) & 1, p.status, OCTO_ETIMEOUT);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && n > 0) {
+      auto issue_S = [&](int hh, int st) {
+        const uint32_t d = tbase + 256 + hh * 64;
+        const uint32_t qa = sQ + hh * 32768;
+        const uint32_t kb = sKV + st * kKVStage;
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) {
+          uint64_t a = desc_sw128(qa + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+          uint64_t b = desc_sw128(kb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+          mma_f16_ss(d, a, b, kIdS, kk > 0);
+        }
+        mma_commit(&B->s_full[hh]);
+      };
+      auto issue_PV = [&](int hh, int st, bool first) {
+        const uint32_t d = tbase + hh * 128;
+        const uint32_t pa = sP + hh * 16384;
+        const uint32_t vb = sKV + st * kKVStage + 16384;
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++) {
+          uint64_t a = desc_sw128(pa + kk * 32, 16, 1024);
+          uint64_t b = desc_sw128(vb + kk * 2048, 8192, 1024);
+          mma_f16_ss(d, a, b, kIdO, (!first || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&B->o_done[hh]);
+      };
+      bool ok = wait_or_abort(&B->q_full, 0, B, p.status) && wait_or_abort(&B->kv_full[0], 0, B, p.status);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0, 0);
+        issue_S(1, 0);
+      }
+      for (int32_t j = 0; ok && j < n; j++) {
+        const int st = j % kNS;
+        const int st2 = (j + 1) % kNS;
+        if (!(ok = wait_or_abort(&B->p_full[0], j & 1, B, p.status))) break;
+        tc_fence_after();
+        issue_PV(0, st, j == 0);
+        if (j + 1 < n) {
+          if (!(ok = wait_or_abort(&B->kv_full[st2], ((j + 1) / kNS) & 1, B, p.status))) break;
+          if (!(ok = wait_or_abort(&B->s_free[0], j & 1, B, p.status))) break;
+          tc_fence_after();
+          issue_S(0, st2);
+        }
+        if (!(ok = wait_or_abort(&B->p_full[1], j & 1, B, p.status))) break;
+        tc_fence_after();
+        issue_PV(1, st, j == 0);
+        mma_commit(&B->kv_empty[st]);
+        if (j + 1 < n) {
+          if (!(ok = wait_or_abort(&B->s_free[1], j & 1, B, p.status))) break;
+          tc_fence_after();
+          issue_S(1, st2);
+        }
+      }
+      // drain: all MMAs this thread issued are complete before TMEM is released
+      mma_commit(&B->drain);
+      mbar_wait(&B->drain, 0, p.status, OCTO_ETIMEOUT);
+    }
+  } else if (warp >= 4) {
+    // ---------------- softmax warpgroups ----------------
+    const int hh = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tbase + lane_off + 256 + hh * 64;
+    const uint32_t tO = tbase + lane_off + hh * 128;
+    const uint32_t prow = sP + hh * 16384 + r * 128;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int32_t j = 0; j < n; j++) {
+      const octo_entry e = p.entries[e0 + j];
+      if (!(ok = warp_wait(&B->s_full[hh], j & 1, B, p.status))) break;
+      tc_fence_after();
+      uint32_t s0[32], s1[32];
+      tmem_ld32(tS, s0);
+      tmem_ld32(tS + 32, s1);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&B->s_free[hh]);
+      float x[64];
+#pragma unroll
+      for (int i = 0; i < 32; i++) {
+        x[i] = __uint_as_float(s0[i]) * p.scale_log2;
+        x[32 + i] = __uint_as_float(s1[i]) * p.scale_log2;
+      }
+      const bool full = e.q_lo == 0 && e.kv_lo == 0 && e.kv_hi == 64 && !(e.flags & 1);
+      if (!full) {
+        const int lo = r < (int)e.q_lo ? 64 : (int)e.kv_lo;
+        int hi = e.kv_hi;
+        if (e.flags & 1) hi = min(hi, r + e.diag + 1);
+#pragma unroll
+        for (int i = 0; i < 64; i++)
+          if (i < lo || i >= hi) x[i] = -INFINITY;
+      }
+      float mc = x[0];
+#pragma unroll
+      for (int i = 1; i < 64; i++) mc = fmaxf(mc, x[i]);
+      bool need = false;
+      float factor = 1.f;
+      if (j == 0) {
+        m_used = mc;
+      } else if (mc > m_used + 8.f) {
+        factor = ex2(m_used - mc);
+        l *= factor;
+        m_used = mc;
+        need = true;
+      }
+      const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+      uint32_t pk[32];
+      float ls = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; i++) {
+        float a = ex2(x[2 * i] - msub), b = ex2(x[2 * i + 1] - msub);
+        ls += a + b;
+        pk[i] = pack_bf16(a, b);
+      }
+      l += ls;
+      // PV of the previous entry must be done before P or O is overwritten
+      if (j > 0) {
+        if (!(ok = warp_wait(&B->o_done[hh], (j - 1) & 1, B, p.status))) break;
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int c = 0; c < 4; c++) {
+          uint32_t ov[32];
+          tmem_ld32(tO + c * 32, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i++) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * factor);
+          tmem_st32(tO + c * 32, ov);
+        }
+        tmem_wait_st();
+      }
+#pragma unroll
+      for (int c = 0; c < 8; c++)
+        st_shared_v4(prow + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&B->p_full[hh]);
+    }
+    // ---------------- epilogue ----------------
+    if (ok && n > 0 && warp_wait(&B->o_done[hh], (n - 1) & 1, B, p.status)) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const int h = h0 + hh;
+      const int64_t row = (int64_t)row0 + r;
+      __nv_bfloat16* orow = p.o + (row * p.Hq + h) * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; c++) {
+        uint32_t ov[32];
+        tmem_ld32(tO + c * 32, ov);
+        tmem_wait_ld();
+        if (r < rows) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; q4++) {
+            uint32_t w[4];
+#pragma unroll
+            for (int t = 0; t < 4; t++)
+              w[t] = pack_bf16(__uint_as_float(ov[q4 * 8 + 2 * t]) * inv, __uint_as_float(ov[q4 * 8 + 2 * t + 1]) * inv);
+            st_global_v4(orow + c * 32 + q4 * 8, w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      if (r < rows) {
+        const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+        p.lse[(int64_t)h * p.n_rows + row] = (msub + lg2(l)) * 0.69314718055994531f;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tbase, 512);
+}
+
+}  // namespace
+
+// ---- host ----
+int encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, uint32_t rank, void* base, const uint64_t* dims,
+                const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz) {
+  using Fn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*, const cuuint64_t*,
+                          const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                          CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static Fn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !ptr)
+      return OCTO_ECUDA;
+    fn = reinterpret_cast<Fn>(ptr);
+  }
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, dt, rank, base, dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? OCTO_OK : OCTO_EINVAL;
+}
+
+bool fwd_tc_supported(const octo_plan_s* p, int32_t Hq) {
+  const octo_pool_desc& d = p->pool->desc;
+  const int32_t G = Hq / d.n_kv_heads;
+  return d.dtype == OCTO_DTYPE_BF16 && d.head_dim == 128 && d.page_size == 64 && p->info.bm == 128 &&
+         !p->info.is_decode && (G % 2) == 0;
+}
+
+int fwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const void* v, void* o, float* lse,
+           float scale, cudaStream_t s) {
+  const octo_pool_desc& d = p->pool->desc;
+  const int64_t N = p->info.n_rows;
+  if (N == 0 || p->info.n_tiles == 0) return OCTO_OK;
+  if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)o) & 15) return OCTO_EINVAL;
+  CUtensorMap mq, mk, mv;
+  {
+    uint64_t dims[3] = {128, (uint64_t)Hq, (uint64_t)N};
+    uint64_t str[2] = {128 * 2, (uint64_t)Hq * 128 * 2};
+    uint32_t box[3] = {64, 1, 128};
+    if (int st = encode_tmap(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, str, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+      return st;
+  }
+  {
+    uint64_t dims[2] = {128, (uint64_t)d.num_pages * d.n_kv_heads * 64};
+    uint64_t str[1] = {128 * 2};
+    uint32_t box[2] = {64, 64};
+    if (int st = encode_tmap(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(k), dims, str, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+      return st;
+    if (int st = encode_tmap(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(v), dims, str, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+      return st;
+  }
+  FwdTcParams prm;
+  prm.tile_off = p->tile_off;
+  prm.tile_rows = p->tile_rows;
+  prm.tile_row0 = p->tile_row0;
+  prm.entries = p->entries;
+  prm.o = (__nv_bfloat16*)o;
+  prm.lse = lse;
+  prm.n_rows = N;
+  prm.Hq = Hq;
+  prm.Hkv = d.n_kv_heads;
+  prm.G = Hq / d.n_kv_heads;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.status = p->pool->d_status;
+  static bool attr = false;
+  if (!attr) {
+    OCTO_CUDA(cudaFuncSetAttribute(k_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
+    attr = true;
+  }
+  const int64_t grid = p->info.n_tiles * d.n_kv_heads * (prm.G / 2);
+  if (grid > INT32_MAX) return OCTO_EINVAL;
+  k_fwd_tc<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, prm);
+  count_launch();
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace octo

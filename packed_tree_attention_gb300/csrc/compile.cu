@@ -456,6 +456,7 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
   }
   octo_plan_s* pl = new octo_plan_s();
   pl->pool = pool;
+  pl->last_stream = s;
   pl->num_pages = pool->desc.num_pages;
   std::memset(&pl->info, 0, sizeof(pl->info));
   pl->info.bm = bm;
@@ -667,7 +668,9 @@ int octo_plan_copy_out(octo_plan_t pl, int32_t* seg_order, int32_t* seg_row_base
 
 int octo_plan_destroy(octo_plan_t pl) {
   if (!pl) return OCTO_EINVAL;
-  for (void* p : pl->allocs) cudaFree(p);
+  // stream-ordered: the arrays go back to the pool only after the work already enqueued
+  // on the plan's last stream has finished with them
+  for (void* p : pl->allocs) cudaFreeAsync(p, pl->last_stream);
   delete pl;
   return OCTO_OK;
 }

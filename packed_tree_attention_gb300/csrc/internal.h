@@ -74,6 +74,7 @@ struct octo_plan_s {
   int32_t* tile_order = nullptr;     // [n_tiles] tiles by descending entry count (scheduling)
   int32_t* page_order = nullptr;     // [n_touched] touched pages by descending entry count
   std::vector<void*> allocs;
+  cudaStream_t last_stream = nullptr;  // stream of the last call that used the plan
 };
 
 namespace octo {

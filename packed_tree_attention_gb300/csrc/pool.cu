@@ -169,7 +169,10 @@ int octo_pool_create(const octo_pool_desc* desc, octo_pool_t* out) {
 
 int octo_pool_destroy(octo_pool_t p) {
   if (!p) return OCTO_EINVAL;
-  if (p->d_status) cudaFree(p->d_status);
+  if (p->d_status) {
+    cudaDeviceSynchronize();   // no kernel of this pool may still use the status word
+    cudaFree(p->d_status);
+  }
   delete p;
   return OCTO_OK;
 }
