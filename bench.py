@@ -98,6 +98,23 @@ class ClockSampler:
                 "samples": len(sms)}
 
 
+def rank_seed(seed, rank):
+    """Each rank runs its own episode: the units (episodes) are independent, so the
+    data path has no collective."""
+    return seed + rank
+
+
+def max_over_ranks(value, dist):
+    """The job's step time is the slowest rank's."""
+    if dist is None:
+        return value
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def unique_tokens(entries, num_pages, P):
     seen = np.zeros((num_pages, P), dtype=bool)
     for lo in range(P):
@@ -222,7 +239,7 @@ def run_ours(args, rank, world, dist):
     pta.load()
     stream = torch.cuda.current_stream()
     hbm, bf16, bf16s, peak_src = peaks()
-    seed = args.seed + rank
+    seed = rank_seed(args.seed, rank)
 
     # ---------------- training leg: episode fwd + bwd ----------------
     ep, pool, kp, vp, cfg = build_episode(pta, torch, args.workload, seed, dev)
@@ -274,11 +291,7 @@ def run_ours(args, rank, world, dist):
     path_fwd = recs[0][4].kernel_path(Hq, 0)
     path_bwd = recs[0][4].kernel_path(Hq, 1)
     del recs
-    ms_step = total_ms / args.steps
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / args.steps, dist)
     value = world * (fwd_flops + bwd_flops) / (ms_step * 1e-3) / 1e12
     fwd_ms = statistics.mean(per["fwd"])
     bwd_ms = statistics.mean(per["bwd"])
@@ -314,11 +327,7 @@ def run_ours(args, rank, world, dist):
 
         e2e_steps = max(1, min(args.steps, 3))
         e_ms, _ = timed(torch, stream, e2e_step, e2e_steps, 1, dist)
-        e_ms /= e2e_steps
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms / e2e_steps, dist)
         h2d = sum(x.numel() * x.element_size() for x in (hq, hdo, hk, hv))
         d2h = sum(x.numel() * x.element_size() for x in (hdq, hdk, hdv))
         e2e = {"value": world * (fwd_flops + bwd_flops) / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",

@@ -12,6 +12,14 @@ int bwd_simt(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, con
              const float* lse, const void* dout, float* dq, float* dk, float* dv, float scale, void* ws,
              cudaStream_t s);
 bool fwd_tc_supported(const octo_plan_s* p, int32_t Hq);
+bool bwd_tc_supported(const octo_plan_s* p, int32_t Hq);
+bool decode_split_supported(const octo_plan_s* p, int32_t Hq);
+size_t decode_split_workspace(const octo_plan_s* p, int32_t Hq);
+int decode_split(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const void* v, void* out, float* lse,
+                 float scale, void* ws, cudaStream_t s);
+int bwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const void* v, const void* o,
+           const float* lse, const void* dout, float* dq, float* dk, float* dv, float scale, void* ws,
+           cudaStream_t s);
 int fwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const void* v, void* o, float* lse,
            float scale, cudaStream_t s);
 }  // namespace octo
@@ -41,8 +49,11 @@ extern "C" {
 
 int octo_kernel_path(octo_plan_t plan, int32_t n_q_heads, int32_t which) {
   if (!plan || check_heads(plan, n_q_heads)) return -1;
+  if (which == 2) return octo::decode_split_supported(plan, n_q_heads) ? 2 : 0;
   if (tc_disabled()) return 0;
   if (which == 0) return octo::fwd_tc_supported(plan, n_q_heads) ? 1 : 0;
+  if (which == 1) return octo::bwd_tc_supported(plan, n_q_heads) ? 1 : 0;
+  if (which == 2) return octo::decode_split_supported(plan, n_q_heads) ? 2 : 0;
   return 0;
 }
 
@@ -78,12 +89,14 @@ int octo_attn_bwd(octo_plan_t plan, int32_t Hq, const void* q, const void* k_poo
   const void* v = v_pool ? v_pool : plan->pool->desc.v_pool;
   if (plan->info.n_entries > 0 && (!k || !v)) return OCTO_EINVAL;
   plan->last_stream = (cudaStream_t)stream;
+  if (!tc_disabled() && octo::bwd_tc_supported(plan, Hq))
+    return octo::bwd_tc(plan, Hq, q, k, v, o, lse, dout, dq, dk_pool, dv_pool, scale, ws, (cudaStream_t)stream);
   return octo::bwd_simt(plan, Hq, q, k, v, o, lse, dout, dq, dk_pool, dv_pool, scale, ws, (cudaStream_t)stream);
 }
 
 size_t octo_decode_workspace_size(octo_plan_t plan, int32_t Hq) {
-  if (!plan || Hq <= 0) return 0;
-  return 0;
+  if (!plan || check_heads(plan, Hq)) return 0;
+  return octo::decode_split_supported(plan, Hq) ? octo::decode_split_workspace(plan, Hq) : 0;
 }
 
 int octo_decode(octo_plan_t plan, int32_t Hq, const void* q, const void* k_pool, const void* v_pool, void* out,
@@ -92,11 +105,14 @@ int octo_decode(octo_plan_t plan, int32_t Hq, const void* q, const void* k_pool,
   if (int st = check_heads(plan, Hq)) return st;
   if (plan->info.n_rows > 0 && (!q || !out)) return OCTO_EINVAL;
   if (ws_bytes < octo_decode_workspace_size(plan, Hq)) return OCTO_EINVAL;
-  (void)ws;
   const void* k = k_pool ? k_pool : plan->pool->desc.k_pool;
   const void* v = v_pool ? v_pool : plan->pool->desc.v_pool;
   if (plan->info.n_entries > 0 && (!k || !v)) return OCTO_EINVAL;
   plan->last_stream = (cudaStream_t)stream;
+  if (octo::decode_split_supported(plan, Hq)) {
+    if (!ws && plan->info.n_rows > 0) return OCTO_EINVAL;
+    return octo::decode_split(plan, Hq, q, k, v, out, lse, scale, ws, (cudaStream_t)stream);
+  }
   return octo::fwd_simt(plan, Hq, q, k, v, out, lse, scale, true, (cudaStream_t)stream);
 }
 

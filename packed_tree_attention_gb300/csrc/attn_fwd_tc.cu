@@ -49,6 +49,7 @@ struct FwdTcParams {
   const int32_t* tile_off;
   const int32_t* tile_rows;
   const int32_t* tile_row0;
+  const int32_t* tile_order;
   const octo_entry* entries;
   __nv_bfloat16* o;
   float* lse;
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t HP = p.G >> 1;
   const int32_t hp = blockIdx.x % HP;
   const int32_t g = (blockIdx.x / HP) % p.Hkv;
-  const int32_t tile = blockIdx.x / (HP * p.Hkv);
+  const int32_t tile = p.tile_order[blockIdx.x / (HP * p.Hkv)];
   const int32_t h0 = g * p.G + 2 * hp;
   const int32_t e0 = p.tile_off[tile];
   const int32_t n = p.tile_off[tile + 1] - e0;
@@ -374,7 +375,7 @@ bool fwd_tc_supported(const octo_plan_s* p, int32_t Hq) {
   const octo_pool_desc& d = p->pool->desc;
   const int32_t G = Hq / d.n_kv_heads;
   return d.dtype == OCTO_DTYPE_BF16 && d.head_dim == 128 && d.page_size == 64 && p->info.bm == 128 &&
-         !p->info.is_decode && (G % 2) == 0;
+         !p->info.is_decode && (G % 2) == 0 && p->tile_order;
 }
 
 int fwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -407,6 +408,7 @@ int fwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const
   prm.tile_off = p->tile_off;
   prm.tile_rows = p->tile_rows;
   prm.tile_row0 = p->tile_row0;
+  prm.tile_order = p->tile_order;
   prm.entries = p->entries;
   prm.o = (__nv_bfloat16*)o;
   prm.lse = lse;

@@ -596,7 +596,64 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
     count_launch();
   }
   OCTO_TRY(cuda_status(cudaGetLastError()));
-  // scratch buffers no longer needed
+  // ---- launch orders: heaviest tiles / pages first (longest-processing-time first) ----
+  {
+    std::vector<int32_t> toff(n_tiles + 1), poff((size_t)pl->num_pages + 1);
+    OCTO_TRY(cuda_status(cudaMemcpyAsync(toff.data(), pl->tile_off, (n_tiles + 1) * 4, cudaMemcpyDeviceToHost, s)));
+    OCTO_TRY(cuda_status(
+        cudaMemcpyAsync(poff.data(), pl->page_off, ((size_t)pl->num_pages + 1) * 4, cudaMemcpyDeviceToHost, s)));
+    OCTO_TRY(cuda_status(cudaStreamSynchronize(s)));
+    std::vector<int32_t> tord(n_tiles), pord;
+    for (int64_t t = 0; t < n_tiles; t++) tord[t] = (int32_t)t;
+    std::stable_sort(tord.begin(), tord.end(),
+                     [&](int32_t a, int32_t b) { return toff[a + 1] - toff[a] > toff[b + 1] - toff[b]; });
+    for (int32_t pg = 0; pg < pl->num_pages; pg++)
+      if (poff[pg + 1] > poff[pg]) pord.push_back(pg);
+    std::stable_sort(pord.begin(), pord.end(),
+                     [&](int32_t a, int32_t b) { return poff[a + 1] - poff[a] > poff[b + 1] - poff[b]; });
+    OCTO_TRY(dalloc(pl, &pl->tile_order, n_tiles, s));
+    OCTO_TRY(dalloc(pl, &pl->page_order, pord.size(), s));
+    if (n_tiles > 0)
+      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->tile_order, tord.data(), n_tiles * 4, cudaMemcpyHostToDevice, s)));
+    if (!pord.empty())
+      OCTO_TRY(
+          cuda_status(cudaMemcpyAsync(pl->page_order, pord.data(), pord.size() * 4, cudaMemcpyHostToDevice, s)));
+    // decode plans: split each cursor's entries into runs of kSplitEntries
+    std::vector<int32_t> sp_tile, sp_e0, sp_e1, sp_order, cur0(n_tiles + 1, 0);
+    if (is_decode) {
+      int32_t max_k = 0;
+      for (int64_t t = 0; t < n_tiles; t++) {
+        cur0[t] = (int32_t)sp_tile.size();
+        int32_t k = 0;
+        for (int32_t e = toff[t]; e < toff[t + 1]; e += kSplitEntries, k++) {
+          sp_tile.push_back((int32_t)t);
+          sp_e0.push_back(e);
+          sp_e1.push_back(std::min(e + kSplitEntries, toff[t + 1]));
+        }
+        max_k = std::max(max_k, k);
+      }
+      cur0[n_tiles] = (int32_t)sp_tile.size();
+      for (int32_t k = 0; k < max_k; k++)
+        for (int64_t t = 0; t < n_tiles; t++)
+          if (cur0[t] + k < cur0[t + 1]) sp_order.push_back(cur0[t] + k);
+      pl->n_splits = (int32_t)sp_tile.size();
+      OCTO_TRY(dalloc(pl, &pl->split_tile, sp_tile.size(), s));
+      OCTO_TRY(dalloc(pl, &pl->split_e0, sp_tile.size(), s));
+      OCTO_TRY(dalloc(pl, &pl->split_e1, sp_tile.size(), s));
+      OCTO_TRY(dalloc(pl, &pl->split_order, sp_tile.size(), s));
+      OCTO_TRY(dalloc(pl, &pl->cur_split0, cur0.size(), s));
+      if (!sp_tile.empty()) {
+        size_t b = sp_tile.size() * 4;
+        OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_tile, sp_tile.data(), b, cudaMemcpyHostToDevice, s)));
+        OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_e0, sp_e0.data(), b, cudaMemcpyHostToDevice, s)));
+        OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_e1, sp_e1.data(), b, cudaMemcpyHostToDevice, s)));
+        OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_order, sp_order.data(), b, cudaMemcpyHostToDevice, s)));
+      }
+      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->cur_split0, cur0.data(), cur0.size() * 4, cudaMemcpyHostToDevice, s)));
+    }
+    // the host vectors are pageable and go out of scope
+    OCTO_TRY(cuda_status(cudaStreamSynchronize(s)));
+  }
   *out = pl;
   return OCTO_OK;
 }

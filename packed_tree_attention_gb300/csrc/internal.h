@@ -73,6 +73,13 @@ struct octo_plan_s {
   int32_t* touched = nullptr;        // [n_touched_pages] pages with >= 1 entry, ascending
   int32_t* tile_order = nullptr;     // [n_tiles] tiles by descending entry count (scheduling)
   int32_t* page_order = nullptr;     // [n_touched] touched pages by descending entry count
+  // decode plans: runs of up to kSplitEntries entries of one cursor (split-KV)
+  int32_t n_splits = 0;
+  int32_t* split_tile = nullptr;     // [n_splits] cursor (tile) of the split
+  int32_t* split_e0 = nullptr;       // [n_splits] first entry
+  int32_t* split_e1 = nullptr;       // [n_splits] one past the last entry
+  int32_t* split_order = nullptr;    // [n_splits] launch order: split index within cursor, then cursor
+  int32_t* cur_split0 = nullptr;     // [n_tiles+1] first split of each cursor
   std::vector<void*> allocs;
   cudaStream_t last_stream = nullptr;  // stream of the last call that used the plan
 };
@@ -103,6 +110,8 @@ int launch_append_rows(const octo_pool_desc& d, const int32_t* d_dst_rows, int32
 // plan compilation (compile.cu)
 int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t* seg_order, int32_t n_segs,
                  bool is_decode, int32_t bm, cudaStream_t s, octo_plan_s** out);
+
+constexpr int32_t kSplitEntries = 32;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
