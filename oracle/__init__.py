@@ -75,6 +75,7 @@ def _load():
         L.orc_row_context.argtypes = [P, I, IP, IP, I]
         L.orc_token_owner.argtypes = [P, IP, IP]
         L.orc_num_tokens.argtypes = [P]
+        L.orc_set_kv.argtypes = [P, I, IP, DP, DP]
         _lib = L
     return _lib
 
@@ -238,6 +239,12 @@ class Oracle:
         out = np.zeros(5, dtype=np.int32)
         self._chk(self._L.orc_mount_info(self.h, i, _ip(out)), "mount_info")
         return tuple(out.tolist())
+
+    def set_kv(self, tokens, k, v):
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        k = np.ascontiguousarray(k, dtype=np.float64)
+        v = np.ascontiguousarray(v, dtype=np.float64)
+        self._chk(self._L.orc_set_kv(self.h, len(t), _ip(t), _dp(k), _dp(v)), "set_kv")
 
     def token_owner(self):
         n = self.n_tokens

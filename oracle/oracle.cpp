@@ -469,6 +469,21 @@ int orc_unpin(void* h, int c) {
   return ORC_OK;
 }
 
+// Overwrites the K/V rows of the given tokens (k, v: [n, Hkv, d]); lets a caller that
+// appended without values supply only the rows a sampled check reads.
+int orc_set_kv(void* h, int n, const int* tokens, const double* k, const double* v) {
+  Oracle* o = static_cast<Oracle*>(h);
+  const size_t row = (size_t)o->Hkv * o->d;
+  for (int i = 0; i < n; i++) {
+    if (tokens[i] < 0 || tokens[i] >= (int)o->tok_seg.size()) return ORC_EINVAL;
+    for (size_t j = 0; j < row; j++) {
+      o->K[(size_t)tokens[i] * row + j] = k[(size_t)i * row + j];
+      o->V[(size_t)tokens[i] * row + j] = v[(size_t)i * row + j];
+    }
+  }
+  return ORC_OK;
+}
+
 int orc_num_segments(void* h) { return (int)static_cast<Oracle*>(h)->segs.size(); }
 int orc_free_pages(void* h) { return static_cast<Oracle*>(h)->free_count(); }
 int orc_num_mounts(void* h) { return (int)static_cast<Oracle*>(h)->mounts.size(); }
@@ -662,14 +677,23 @@ int orc_bwd(void* p, int Hq, const double* Q, const double* dO, double scale,
   std::map<int, std::vector<CtxItem>> ctxs;
   for (int s : pl->seg_order) ctxs[s] = o.full_ctx(s);
   // which rows are needed: dq rows, plus every row whose context holds a needed token
+  // (a row of segment s sees the context items with from <= its index, so it needs the
+  // earliest `from` of a needed token in s's context)
   std::vector<char> need_row(N, 0);
+  std::map<int, int> first_need;   // segment -> smallest own-row index that sees a needed token
+  if (!partial && need_dkdv != nullptr) {
+    for (int s : pl->seg_order) {
+      int mf = 0x7fffffff;
+      for (const CtxItem& c : ctxs.at(s))
+        if (need_dkdv[c.token]) mf = std::min(mf, c.from);
+      first_need[s] = mf;
+    }
+  }
   for (long long r = 0; r < N; r++) {
     if (need_dq == nullptr || need_dq[r]) { need_row[r] = 1; continue; }
     if (partial) continue;   // dK/dV from the dq rows only (a sample of the full sums)
     if (need_dkdv == nullptr) { need_row[r] = 1; continue; }
-    const std::vector<CtxItem>& ctx = ctxs.at(pl->row_seg[r]);
-    for (const CtxItem& c : ctx)
-      if (c.from <= pl->row_idx[r] && need_dkdv[c.token]) { need_row[r] = 1; break; }
+    if (pl->row_idx[r] >= first_need.at(pl->row_seg[r])) need_row[r] = 1;
   }
   if (dK) std::fill(dK, dK + T * Hkv * d, 0.0);
   if (dV) std::fill(dV, dV + T * Hkv * d, 0.0);

@@ -509,3 +509,25 @@ def test_mount_validation(oracle_mod):
     o.done(a)
     assert o.append(a, 1, check=False) == oracle_mod.ESTATE
     assert o.mount(kid, a, 1, 2, check=False) == E
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_subset_backward_matches_full(oracle_mod, seed):
+    """The sampled modes (a token subset for dK/dV, a row subset for dQ) give exactly the
+    full backward's values on that subset."""
+    ep = synth.random_dag(600 + seed, page_size=8, max_segments=10, max_len=50)
+    Hq, Hkv, d = 4, 2, 8
+    t = synth.make_tensors(ep, Hq, Hkv, d, "f32", 1.0, seed)
+    o = _replay(oracle_mod, ep, Hkv, d, t.K.astype(np.float64), t.V.astype(np.float64))
+    pl = o.pack(ep.roots, 16)
+    Q = _packed(t, pl.seg_order, t.Q).astype(np.float64)
+    dO = _packed(t, pl.seg_order, t.dO).astype(np.float64)
+    dQ, dK, dV = pl.bwd(Q, dO, 0.5)
+    rng = np.random.default_rng(seed)
+    T, N = o.n_tokens, pl.n_rows
+    tok = rng.random(T) < 0.2
+    rows = rng.random(N) < 0.2
+    dQs, dKs, dVs = pl.bwd(Q, dO, 0.5, need_dq=rows.astype(np.uint8), need_dkdv=tok.astype(np.uint8))
+    np.testing.assert_array_equal(dQs[rows], dQ[rows])
+    np.testing.assert_allclose(dKs[tok], dK[tok], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(dVs[tok], dV[tok], rtol=1e-13, atol=1e-15)
