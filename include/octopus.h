@@ -123,7 +123,11 @@ int octo_root(octo_pool_t pool, octo_cursor_t* out);
  * segment needs them; a segment's tokens fill its own pages in order.  pos_out (host,
  * n entries, may be NULL) receives each token's position: the cursor's next position,
  * which then advances by one.  k, v: device [n][n_kv_heads][head_dim] of the pool dtype,
- * copied into the pool arrays on `stream`; both NULL = metadata only.
+ * copied into the pool arrays on `stream`; both NULL = no rows copied.  Every page newly
+ * given to the segment is first zeroed in the pool's own arrays (when the pool has them):
+ * the attention kernels read whole pages and mask the slots a row does not see, so those
+ * slots must hold finite values.  Pool arrays passed directly to the attention calls must
+ * keep the same property (zero-initialise them).
  * ENOMEM if the free pages do not suffice (nothing changes), ESTATE if the cursor is
  * frozen, rewound away from or released. */
 int octo_append(octo_pool_t pool, octo_cursor_t cur, int32_t n, const void* k, const void* v,

@@ -182,8 +182,7 @@ class Pool:
 
     def append(self, cur, n, k=None, v=None, stream=None, check=True):
         pos = np.zeros(max(n, 1), dtype=np.int32)
-        st = self._L.octo_append(self.h, cur, n, _ptr(k), _ptr(v), _stream(stream) if k is not None else None,
-                                 _ip(pos))
+        st = self._L.octo_append(self.h, cur, n, _ptr(k), _ptr(v), _stream(stream), _ip(pos))
         if not check:
             return st
         _chk(st, "octo_append")

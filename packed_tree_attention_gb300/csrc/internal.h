@@ -104,6 +104,7 @@ inline int cuda_status(cudaError_t e) {
   } while (0)
 
 // kernels launched by the host pool code
+int launch_zero_pages(const octo_pool_desc& d, const int32_t* d_pages, int32_t n, cudaStream_t s);
 int launch_append_rows(const octo_pool_desc& d, const int32_t* d_dst_rows, int32_t n, const void* k,
                        const void* v, cudaStream_t s);
 

@@ -40,7 +40,28 @@ __global__ void append_rows_kernel(T* __restrict__ kp, T* __restrict__ vp, const
   }
 }
 
+// one block per (page, K or V): zero the page's slots for every kv head
+template <typename T>
+__global__ void zero_pages_kernel(T* __restrict__ kp, T* __restrict__ vp, const int32_t* __restrict__ pages,
+                                  int32_t n, size_t page_elems) {
+  const int32_t i = blockIdx.x >> 1;
+  if (i >= n) return;
+  T* base = ((blockIdx.x & 1) ? vp : kp) + (size_t)pages[i] * page_elems;
+  for (size_t e = threadIdx.x; e < page_elems; e += blockDim.x) base[e] = T(0);
+}
+
 }  // namespace
+
+int launch_zero_pages(const octo_pool_desc& d, const int32_t* d_pages, int32_t n, cudaStream_t s) {
+  if (n <= 0 || !d.k_pool || !d.v_pool) return OCTO_OK;
+  const size_t pe = (size_t)d.n_kv_heads * d.page_size * d.head_dim;
+  if (d.dtype == OCTO_DTYPE_F32)
+    zero_pages_kernel<float><<<2 * n, 256, 0, s>>>((float*)d.k_pool, (float*)d.v_pool, d_pages, n, pe);
+  else
+    zero_pages_kernel<uint16_t><<<2 * n, 256, 0, s>>>((uint16_t*)d.k_pool, (uint16_t*)d.v_pool, d_pages, n, pe);
+  count_launch();
+  return cuda_status(cudaGetLastError());
+}
 
 int launch_append_rows(const octo_pool_desc& d, const int32_t* d_dst, int32_t n, const void* k, const void* v,
                        cudaStream_t s) {
@@ -199,6 +220,7 @@ int octo_append(octo_pool_t p, octo_cursor_t c, int32_t n, const void* k, const 
     g.pages.push_back(*it);
     p->free_pages.erase(it);
   }
+  std::vector<int32_t> newp(g.pages.end() - need, g.pages.end());
   std::vector<int32_t> dst;
   if (k) dst.resize(n);
   for (int32_t i = 0; i < n; i++) {
@@ -209,13 +231,20 @@ int octo_append(octo_pool_t p, octo_cursor_t c, int32_t n, const void* k, const 
   }
   g.len += n;
   p->seq++;
-  if (k && n > 0) {
+  // Device work: pages new to the segment are zeroed in the pool arrays (the attention
+  // kernels read whole pages and mask, so slots past a segment's end must hold finite
+  // values), then the given K/V rows are copied into their slots.
+  const bool zero = !newp.empty() && p->desc.k_pool && p->desc.v_pool;
+  if (zero || (k && n > 0)) {
     cudaStream_t s = (cudaStream_t)stream;
-    int32_t* d_dst = nullptr;
-    OCTO_CUDA(cudaMallocAsync((void**)&d_dst, sizeof(int32_t) * n, s));
-    OCTO_CUDA(cudaMemcpyAsync(d_dst, dst.data(), sizeof(int32_t) * n, cudaMemcpyHostToDevice, s));
-    int st = octo::launch_append_rows(p->desc, d_dst, n, k, v, s);
-    OCTO_CUDA(cudaFreeAsync(d_dst, s));
+    std::vector<int32_t> host(newp);
+    host.insert(host.end(), dst.begin(), dst.end());
+    int32_t* d_buf = nullptr;
+    OCTO_CUDA(cudaMallocAsync((void**)&d_buf, sizeof(int32_t) * host.size(), s));
+    OCTO_CUDA(cudaMemcpyAsync(d_buf, host.data(), sizeof(int32_t) * host.size(), cudaMemcpyHostToDevice, s));
+    int st = zero ? octo::launch_zero_pages(p->desc, d_buf, (int32_t)newp.size(), s) : OCTO_OK;
+    if (st == OCTO_OK && k && n > 0) st = octo::launch_append_rows(p->desc, d_buf + newp.size(), n, k, v, s);
+    OCTO_CUDA(cudaFreeAsync(d_buf, s));
     // the host vector is pageable: make sure the copy has consumed it
     OCTO_CUDA(cudaStreamSynchronize(s));
     if (st != OCTO_OK) return st;

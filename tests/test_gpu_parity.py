@@ -26,7 +26,8 @@ def lib():
 class Run:
     """An episode replayed into both the oracle and the library, with its tensors."""
 
-    def __init__(self, lib, oracle_mod, ep, Hq, Hkv, d, dtype, seed, bm=None, npages=None, with_kv=True):
+    def __init__(self, lib, oracle_mod, ep, Hq, Hkv, d, dtype, seed, bm=None, npages=None, with_kv=True,
+                 pool_fill=0.0):
         self.ep, self.Hq, self.Hkv, self.d, self.dtype = ep, Hq, Hkv, d, dtype
         P = ep.page_size
         self.P = P
@@ -35,8 +36,10 @@ class Run:
         tdt = torch.float32 if dtype == "f32" else torch.bfloat16
         self.tdt = tdt
         dev = "cuda"
-        self.kpool = torch.zeros((self.npages, Hkv, P, d), dtype=tdt, device=dev)
-        self.vpool = torch.zeros_like(self.kpool)
+        # pool_fill: initial content of the pool arrays (NaN checks that pages a segment is
+        # given are cleared before slots past its end can reach a kernel)
+        self.kpool = torch.full((self.npages, Hkv, P, d), pool_fill, dtype=tdt, device=dev)
+        self.vpool = torch.full_like(self.kpool, pool_fill)
         self.pool = lib.Pool(self.npages, P, Hkv, d, lib.DTYPE_F32 if dtype == "f32" else lib.DTYPE_BF16,
                              self.kpool, self.vpool)
         K = torch.from_numpy(self.t.K).to(dev).to(tdt)
@@ -209,9 +212,10 @@ def test_random_fp32(lib, oracle_mod, seed):
 @pytest.mark.parametrize("seed", range(6))
 def test_random_bf16_gqa(lib, oracle_mod, seed):
     """bf16, 16 q heads over 4 kv heads, head_dim 128, page 64, q-tile 128: several tiles
-    per segment, ragged tails, partial pages, mounts, rewinds."""
+    per segment, ragged tails, partial pages, mounts, rewinds.  Odd seeds start from pool
+    arrays full of NaN."""
     ep = synth.random_dag(500 + seed, page_size=64, max_segments=10, max_len=400, n_roots=1 + seed % 2)
-    r = Run(lib, oracle_mod, ep, 16, 4, 128, "bf16", seed)
+    r = Run(lib, oracle_mod, ep, 16, 4, 128, "bf16", seed, pool_fill=float("nan") if seed % 2 else 0.0)
     r.pack(128)
     _check_fwd_bwd(r)
 
