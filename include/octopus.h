@@ -42,7 +42,8 @@ enum {
   OCTO_ESTATE = 3,   /* cursor is done, rewound away from, released, or freed */
   OCTO_ECUDA = 4,    /* a CUDA call failed; see octo_last_cuda_error() */
   OCTO_ETIMEOUT = 5, /* a bounded device wait expired; the kernel returned early */
-  OCTO_ENOTSUP = 6   /* shape or dtype this build has no kernel for */
+  OCTO_ENOTSUP = 6,  /* shape or dtype this build has no kernel for */
+  OCTO_ESCRATCH = 7  /* request needs more than the built-in scratch of octo_decode_noalloc */
 };
 
 enum { OCTO_DTYPE_F32 = 0, OCTO_DTYPE_BF16 = 1 };
@@ -237,6 +238,27 @@ size_t octo_decode_workspace_size(octo_plan_t plan, int32_t n_q_heads);
 int octo_decode(octo_plan_t plan, int32_t n_q_heads, const void* q, const void* k_pool,
                 const void* v_pool, void* out, float* lse, float scale, void* ws,
                 size_t ws_bytes, void* stream);
+
+/* Allocation-free variant of octo_decode, for callers that must not allocate device
+ * memory: engines whose device memory is all handed out by their own allocator at
+ * start-up, or code running where a cudaMalloc (or a torch allocation) is not allowed.
+ * Such callers still pass q, out and lse, but cannot provide octo_decode's workspace.
+ * The pages have no counterpart for this entry point; it is a deployment convenience.
+ *
+ * The split partials live in a file-scope device array of OCTO_NOALLOC_SCRATCH_BYTES
+ * bytes (32 MiB) that every GPU which loads the library holds until the process exits.
+ * A call needs octo_decode_workspace_size(plan, n_q_heads) bytes of it; larger requests
+ * return OCTO_ESCRATCH and launch nothing.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  The call itself allocates nothing.  Every call
+ * shares the one array and each call overwrites the part it reads before reading it, so
+ * nothing needs clearing between calls -- but calls that overlap on the GPU (on different
+ * streams, or on different host threads) race on it and must be serialised by the
+ * caller.  Arguments, layouts and results are those of octo_decode; bf16 pools with
+ * head_dim 128 and page size 64 only (OCTO_ENOTSUP otherwise). */
+#define OCTO_NOALLOC_SCRATCH_BYTES (32u << 20)
+int octo_decode_noalloc(octo_plan_t plan, int32_t n_q_heads, const void* q, const void* k_pool,
+                        const void* v_pool, void* out, float* lse, float scale, void* stream);
 
 /* ---- diagnostics ---- */
 const char* octo_strerror(int status);

@@ -21,7 +21,8 @@ from . import build as _build
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = _build.LIB
 
-OK, EINVAL, ENOMEM, ESTATE, ECUDA, ETIMEOUT, ENOTSUP = range(7)
+OK, EINVAL, ENOMEM, ESTATE, ECUDA, ETIMEOUT, ENOTSUP, ESCRATCH = range(8)
+NOALLOC_SCRATCH_BYTES = 32 << 20
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
 _lib = None
@@ -65,7 +66,7 @@ SYMBOLS = ("octo_pool_create", "octo_pool_destroy", "octo_root", "octo_append", 
            "octo_pack_tree", "octo_decode_plan", "octo_plan_info", "octo_plan_copy_out", "octo_plan_destroy",
            "octo_attn_fwd", "octo_attn_bwd_workspace_size", "octo_attn_bwd", "octo_decode_workspace_size",
            "octo_decode", "octo_strerror", "octo_last_cuda_error", "octo_sync", "octo_kernel_path",
-           "octo_launch_count")
+           "octo_launch_count", "octo_decode_noalloc")
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
@@ -109,6 +110,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "octo_sync": [P, P],
         "octo_kernel_path": [P, I32, I32],
         "octo_launch_count": [],
+        "octo_decode_noalloc": [P, I32, P, P, P, P, P, F, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -322,6 +324,12 @@ class Plan:
             ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
         _chk(self._L.octo_decode(self.h, n_q_heads, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(lse),
                                  float(scale), _ptr(ws), ws_bytes, _stream(stream)), "octo_decode")
+
+    def decode_noalloc(self, n_q_heads, q, out, lse, scale, k_pool=None, v_pool=None, stream=None):
+        """octo_decode_noalloc: the decode without a workspace argument, for callers that
+        cannot allocate device memory (its partials use the library's static scratch)."""
+        _chk(self._L.octo_decode_noalloc(self.h, n_q_heads, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(out),
+                                         _ptr(lse), float(scale), _stream(stream)), "octo_decode_noalloc")
 
     def sync(self, stream=None):
         _chk(self._L.octo_sync(self.h, _stream(stream)), "octo_sync")

@@ -22,6 +22,8 @@
 
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "internal.h"
 
 namespace octo {
@@ -258,3 +260,54 @@ int decode_split(const octo_plan_s* p, int32_t Hq, const void* q, const void* k,
 }
 
 }  // namespace octo
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free decode: the same split-KV kernels with their partials in a static device
+// array instead of a caller workspace.
+// ---------------------------------------------------------------------------------------
+namespace octo {
+namespace {
+
+// One per device that loads the library, alive until the process exits.
+static __device__ __align__(256) unsigned char g_decode_scratch[OCTO_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per device
+// (cudaGetSymbolAddress with that device current).
+int scratch_for_current_device(void** out) {
+  int dev = 0;
+  OCTO_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return OCTO_ENOTSUP;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    OCTO_CUDA(cudaGetSymbolAddress(&ptr, g_decode_scratch));
+    if (!ptr) return OCTO_ECUDA;
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return OCTO_OK;
+}
+
+}  // namespace
+}  // namespace octo
+
+extern "C" int octo_decode_noalloc(octo_plan_t plan, int32_t Hq, const void* q, const void* k_pool,
+                                   const void* v_pool, void* out, float* lse, float scale, void* stream) {
+  if (!plan || !plan->info.is_decode) return OCTO_EINVAL;
+  const int32_t Hkv = plan->pool->desc.n_kv_heads;
+  if (Hq <= 0 || Hq % Hkv != 0) return OCTO_EINVAL;
+  if (plan->info.n_rows > 0 && (!q || !out)) return OCTO_EINVAL;
+  if (!octo::decode_split_supported(plan, Hq)) return OCTO_ENOTSUP;
+  if (octo::decode_split_workspace(plan, Hq) > (size_t)OCTO_NOALLOC_SCRATCH_BYTES) return OCTO_ESCRATCH;
+  const void* k = k_pool ? k_pool : plan->pool->desc.k_pool;
+  const void* v = v_pool ? v_pool : plan->pool->desc.v_pool;
+  if (plan->info.n_entries > 0 && (!k || !v)) return OCTO_EINVAL;
+  void* scratch = nullptr;
+  if (int st = octo::scratch_for_current_device(&scratch)) return st;
+  plan->last_stream = (cudaStream_t)stream;
+  return octo::decode_split(plan, Hq, q, k, v, out, lse, scale, scratch, (cudaStream_t)stream);
+}

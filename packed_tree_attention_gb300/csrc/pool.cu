@@ -164,6 +164,7 @@ const char* octo_strerror(int st) {
     case OCTO_ECUDA: return "CUDA error";
     case OCTO_ETIMEOUT: return "bounded device wait expired";
     case OCTO_ENOTSUP: return "unsupported shape or dtype";
+    case OCTO_ESCRATCH: return "request exceeds the built-in scratch of the allocation-free decode";
   }
   return "unknown status";
 }
