@@ -73,9 +73,11 @@ __device__ __forceinline__ bool warp_wait_ab(uint64_t* bar, uint32_t parity, Ctl
 }
 
 // Loads this thread's row of S and dP (64 columns each, 32 at a time) from TMEM, applies
-// the entry mask, and returns packed bf16 P and dS (32 words each).
-__device__ __forceinline__ void make_p_ds(uint32_t tS, uint32_t tP, const octo_entry& e, int r, bool row_ok, float lse2,
-                                          float Dr, float scale_log2, uint32_t (&pk)[32], uint32_t (&dk)[32]) {
+// the entry mask, and writes the row of P (if p_row != 0) and of dS, as bf16, into the
+// 128-byte-swizzled row tiles at p_row / ds_row (byte addresses of this row).  Half a row
+// is live at a time.
+__device__ __forceinline__ void p_ds_to_smem(uint32_t tS, uint32_t tP, const octo_entry& e, int r, bool row_ok,
+                                             float lse2, float Dr, float scale_log2, uint32_t p_row, uint32_t ds_row) {
   int lo = (int)e.kv_lo, hi = (int)e.kv_hi;
   if (!row_ok || r < (int)e.q_lo) lo = 64;
   if (e.flags & 1) hi = min(hi, r + e.diag + 1);
@@ -85,27 +87,29 @@ __device__ __forceinline__ void make_p_ds(uint32_t tS, uint32_t tP, const octo_e
     tmem_ld32(tS + 32 * half, sv);
     tmem_ld32(tP + 32 * half, dv);
     tmem_wait_ld();
+    uint32_t pk[16], dk[16];
 #pragma unroll
     for (int i = 0; i < 16; i++) {
       const int j0 = 32 * half + 2 * i, j1 = j0 + 1;
       const float p0 = (j0 >= lo && j0 < hi) ? ex2(__uint_as_float(sv[2 * i]) * scale_log2 - lse2) : 0.f;
       const float p1 = (j1 >= lo && j1 < hi) ? ex2(__uint_as_float(sv[2 * i + 1]) * scale_log2 - lse2) : 0.f;
-      pk[16 * half + i] = pack_bf16(p0, p1);
-      dk[16 * half + i] = pack_bf16(p0 * (__uint_as_float(dv[2 * i]) - Dr), p1 * (__uint_as_float(dv[2 * i + 1]) - Dr));
+      pk[i] = pack_bf16(p0, p1);
+      dk[i] = pack_bf16(p0 * (__uint_as_float(dv[2 * i]) - Dr), p1 * (__uint_as_float(dv[2 * i + 1]) - Dr));
+    }
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      const int c = 4 * half + q;
+      const uint32_t off = (uint32_t)((c ^ (r & 7)) << 4);
+      if (p_row) st_shared_v4(p_row + off, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      st_shared_v4(ds_row + off, dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
     }
   }
-}
-
-__device__ __forceinline__ void store_rowtile(uint32_t base, int r, const uint32_t (&w)[32]) {
-#pragma unroll
-  for (int c = 0; c < 8; c++)
-    st_shared_v4(base + r * 128 + ((c ^ (r & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 }
 
 // =====================================================================================
 // dK / dV
 // =====================================================================================
-constexpr int kDkThreads = 384;
+constexpr int kDkThreads = 320;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 softmax
 // smem: K/V page 32KB | 2 stages x (Q 32KB + dO 32KB) | 2 stages x (P 16KB + dS 16KB)
 constexpr uint32_t kDkOffKV = 0;
 constexpr uint32_t kDkOffQD = 32768;
@@ -122,6 +126,7 @@ struct DkBars {
   uint64_t sd_free[2];
   uint64_t pd_full[2];
   uint64_t mm_done[2];
+  uint64_t acc_done;   // single use: every accumulation MMA of the CTA has completed
   uint64_t drain;
   Ctl ctl;
 };
@@ -150,11 +155,12 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       mbar_init(&B->pd_full[s], 128);
       mbar_init(&B->mm_done[s], 1);
     }
+    mbar_init(&B->acc_done, 1);
     mbar_init(&B->drain, 1);
     C->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tmem_alloc(&C->tmem_base, 512);
     tmem_relinquish();
   }
@@ -178,12 +184,14 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       tma_load_2d(smem + kDkOffKV + 16384, &tmV, &B->kv_full, 0, krow);
       tma_load_2d(smem + kDkOffKV + 24576, &tmV, &B->kv_full, 64, krow);
       int32_t issued = 0;
+      int32_t row0_next = p.tile_row0[p.entries[p.csc_perm[c0]].q_tile];
       for (int32_t w = 0; w < n; w++) {
         const int st = w & 1;
-        if (w >= 2 && !wait_ab(&B->mm_done[st], ((w >> 1) - 1) & 1, C, p.status)) break;
-        const octo_entry e = p.entries[p.csc_perm[c0 + w / G]];
         const int32_t h = g * G + (w % G);
-        const int32_t row0 = p.tile_row0[e.q_tile];
+        const int32_t row0 = row0_next;
+        // the next item's tile, looked up before this item's stage wait
+        if (w + 1 < n) row0_next = (w + 1) % G ? row0 : p.tile_row0[p.entries[p.csc_perm[c0 + (w + 1) / G]].q_tile];
+        if (w >= 2 && !wait_ab(&B->mm_done[st], ((w >> 1) - 1) & 1, C, p.status)) break;
         uint8_t* dst = smem + kDkOffQD + st * kDkStageQD;
         mbar_expect_tx(&B->qd_full[st], 65536);
         tma_load_3d(dst, &tmQ, &B->qd_full[st], 0, h, row0);
@@ -248,48 +256,60 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         tc_fence_after();
         issue_acc(w);
       }
+      if (ok) mma_commit(&B->acc_done);
       mma_commit(&B->drain);
       mbar_wait(&B->drain, 0, p.status, OCTO_ETIMEOUT);
     }
-  } else if (warp >= 4) {
-    // two warpgroups: warpgroup k takes the items w with w % 2 == k (stage k)
-    const int wg = (warp - 4) >> 2;
+  } else {
+    // warps 2-9: two warpgroups; warpgroup k takes the items w with w % 2 == k (stage k).
+    // A warp reaches the TMEM lanes of its quadrant warp % 4.
+    const int wg = (warp - 2) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     bool ok = true;
     int32_t w = wg;
+    // item metadata, loaded one item ahead (this warpgroup's next item is w + 2)
+    octo_entry e_n;
+    int32_t rows_n = 0;
+    float lse2_n = 0.f, Dr_n = 0.f;
+    auto load_item = [](const BwdParams& pp, int32_t c0_, int32_t G_, int32_t g_, int32_t wi, int r_, octo_entry& e,
+                        int32_t& rows, float& lse2, float& Dr) {
+      e = pp.entries[pp.csc_perm[c0_ + wi / G_]];
+      const int32_t h = g_ * G_ + (wi % G_);
+      rows = pp.tile_rows[e.q_tile];
+      const int64_t row = (int64_t)pp.tile_row0[e.q_tile] + r_;
+      const bool ok_ = r_ < rows;
+      lse2 = ok_ ? pp.lse[(int64_t)h * pp.n_rows + row] * 1.4426950408889634f : 0.f;
+      Dr = ok_ ? pp.Dv[(int64_t)h * pp.n_rows + row] : 0.f;
+    };
+    if (w < n) load_item(p, c0, G, g, w, r, e_n, rows_n, lse2_n, Dr_n);
     for (; w < n; w += 2) {
       const int st = w & 1;
-      const octo_entry e = p.entries[p.csc_perm[c0 + w / G]];
-      const int32_t h = g * G + (w % G);
-      const int32_t rows = p.tile_rows[e.q_tile];
-      const int64_t row = (int64_t)p.tile_row0[e.q_tile] + r;
-      const bool row_ok = r < rows;
-      const float lse2 = row_ok ? p.lse[(int64_t)h * p.n_rows + row] * 1.4426950408889634f : 0.f;
-      const float Dr = row_ok ? p.Dv[(int64_t)h * p.n_rows + row] : 0.f;
-      if (!(ok = warp_wait_ab(&B->sd_full[st], (w >> 1) & 1, C, p.status))) break;
-      tc_fence_after();
-      uint32_t pk[32], dk[32];
-      make_p_ds(tbase + lane_off + 128 + 128 * st, tbase + lane_off + 192 + 128 * st, e, r, row_ok, lse2, Dr,
-                p.scale_log2, pk, dk);
-      tc_fence_before();
-      mbar_arrive(&B->sd_free[st]);
+      const octo_entry e = e_n;
+      const bool row_ok = r < rows_n;
+      const float lse2 = lse2_n, Dr = Dr_n;
+      if (w + 2 < n) load_item(p, c0, G, g, w + 2, r, e_n, rows_n, lse2_n, Dr_n);
       // the accumulation MMAs of item w - 2 read this stage's P / dS buffers
       if (w >= 2) {
         if (!(ok = warp_wait_ab(&B->mm_done[st], ((w >> 1) - 1) & 1, C, p.status))) break;
       }
+      if (!(ok = warp_wait_ab(&B->sd_full[st], (w >> 1) & 1, C, p.status))) break;
+      tc_fence_after();
       const uint32_t pP = sPS + st * kDkStagePS;
-      store_rowtile(pP, r, pk);
-      store_rowtile(pP + 16384, r, dk);
+      p_ds_to_smem(tbase + lane_off + 128 + 128 * st, tbase + lane_off + 192 + 128 * st, e, r, row_ok, lse2, Dr,
+                   p.scale_log2, pP + r * 128, pP + 16384 + r * 128);
+      tc_fence_before();
+      mbar_arrive(&B->sd_free[st]);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&B->pd_full[st]);
     }
-    // epilogue (warpgroup 0): TMEM lane = d, 64 columns = page slots
+    // epilogue (warpgroup 0): TMEM lane = d, 64 columns = page slots.  It waits on a
+    // single-use barrier: a parity wait on mm_done of the other warpgroup's stage could be
+    // one completion short and still pass.
     if (wg == 0 && n > 0) {
-      const int32_t last = n - 1;
-      bool fin = ok && warp_wait_ab(&B->mm_done[last & 1], (last >> 1) & 1, C, p.status);
+      bool fin = ok && warp_wait_ab(&B->acc_done, 0, C, p.status);
       if (fin) {
         tc_fence_after();
         const int dd = r;
@@ -313,13 +333,13 @@ __global__ void __launch_bounds__(kDkThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tbase, 512);
+  if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
 // =====================================================================================
 // dQ
 // =====================================================================================
-constexpr int kDqThreads = 384;
+constexpr int kDqThreads = 320;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 softmax
 constexpr int kDqNS = 2;
 // smem: Q 64KB (2 heads) | dO 64KB | 2 stages x K/V 32KB | dS 2 heads x 16KB
 constexpr uint32_t kDqOffQ = 0;
@@ -375,7 +395,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     C->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tmem_alloc(&C->tmem_base, 512);
     tmem_relinquish();
   }
@@ -402,11 +422,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           tma_load_3d(smem + kDqOffDO + (hh * 2 + c) * 16384, &tmDO, &B->q_full, c * 64, h0 + hh, row0);
         }
       int32_t issued = 0;
+      uint32_t page_next = p.entries[e0].kv_page;
       for (int32_t j = 0; j < n; j++) {
         const int st = j % kDqNS;
+        const uint32_t page = page_next;
+        if (j + 1 < n) page_next = p.entries[e0 + j + 1].kv_page;   // off the critical path
         if (j >= kDqNS && !wait_ab(&B->kv_empty[st], ((j / kDqNS) - 1) & 1, C, p.status)) break;
-        const octo_entry e = p.entries[e0 + j];
-        const int32_t krow = (int32_t)((e.kv_page * (uint32_t)p.Hkv + (uint32_t)g) * 64u);
+        const int32_t krow = (int32_t)((page * (uint32_t)p.Hkv + (uint32_t)g) * 64u);
         uint8_t* kd = smem + kDqOffKV + st * 32768;
         mbar_expect_tx(&B->kv_full[st], 32768);
         tma_load_2d(kd, &tmK, &B->kv_full[st], 0, krow);
@@ -479,8 +501,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mma_commit(&B->drain);
       mbar_wait(&B->drain, 0, p.status, OCTO_ETIMEOUT);
     }
-  } else if (warp >= 4) {
-    const int hh = (warp - 4) >> 2;
+  } else {
+    // warps 2-9: warpgroup hh handles head h0 + hh; a warp reaches TMEM quadrant warp % 4
+    const int hh = (warp - 2) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -492,18 +515,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const uint32_t tS = tbase + lane_off + 256 + 128 * hh;
     const uint32_t dsrow = sDS + hh * 16384;
     bool ok = true;
+    octo_entry e_next = p.entries[e0];
     for (int32_t j = 0; j < n; j++) {
-      const octo_entry e = p.entries[e0 + j];
+      const octo_entry e = e_next;
+      if (j + 1 < n) e_next = p.entries[e0 + j + 1];   // prefetch
       if (!(ok = warp_wait_ab(&B->s_full[hh], j & 1, C, p.status))) break;
       tc_fence_after();
-      uint32_t pk[32], dk[32];
-      make_p_ds(tS, tS + 64, e, r, row_ok, lse2, Dr, p.scale_log2, pk, dk);
-      tc_fence_before();
-      mbar_arrive(&B->s_free[hh]);
       if (j > 0) {
         if (!(ok = warp_wait_ab(&B->o_done[hh], (j - 1) & 1, C, p.status))) break;
       }
-      store_rowtile(dsrow, r, dk);
+      p_ds_to_smem(tS, tS + 64, e, r, row_ok, lse2, Dr, p.scale_log2, 0u, dsrow + r * 128);
+      tc_fence_before();
+      mbar_arrive(&B->s_free[hh]);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&B->p_full[hh]);
@@ -530,7 +553,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tbase, 512);
+  if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
 }  // namespace
@@ -605,6 +628,12 @@ int bwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const
   if (!attr) {
     OCTO_CUDA(cudaFuncSetAttribute(k_dkdv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDkSmem));
     OCTO_CUDA(cudaFuncSetAttribute(k_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmem));
+    // the block sizes must fit the compiled register counts
+    cudaFuncAttributes fa;
+    OCTO_CUDA(cudaFuncGetAttributes(&fa, k_dkdv_tc));
+    if (fa.maxThreadsPerBlock < kDkThreads) return OCTO_ENOTSUP;
+    OCTO_CUDA(cudaFuncGetAttributes(&fa, k_dq_tc));
+    if (fa.maxThreadsPerBlock < kDqThreads) return OCTO_ENOTSUP;
     attr = true;
   }
   const int64_t g1 = (int64_t)p->info.n_touched_pages * d.n_kv_heads;

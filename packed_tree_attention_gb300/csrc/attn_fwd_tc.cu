@@ -11,15 +11,18 @@
 //               entry's page through a 3-stage ring
 //   warp 1      MMA issuer (one thread): S_h = Q_h K^T (M128 N64 K16 x8) and
 //               O_h += P_h V (M128 N128 K16 x4), accumulators in TMEM
-//   warp 2      TMEM allocator (512 columns: O_0, O_1, S_0, S_1)
+//   warp 2      TMEM allocator (512 columns: O_0, O_1, and two S buffers per head)
 //   warps 4-7   softmax of head 0, warps 8-11 softmax of head 1: one row per thread,
 //               S read with tcgen05.ld, mask from the entry rectangle, online softmax
 //               in the log2 domain with lazy rescaling (O is rescaled in TMEM only when
 //               the running max grows by more than 2^8), P written to shared memory in
 //               the 128-byte-swizzled K-major layout the MMA reads
-// The two heads' softmax warpgroups run half an entry apart, so the tensor core
-// alternates between them.  Every mbarrier wait is bounded; on expiry the kernel
-// records OCTO_ETIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+// S and P are double-buffered per head: the MMA issuer runs S two entries ahead, so a
+// softmax warpgroup starts entry j+1 while the tensor core still runs P V of entry j,
+// and the two heads' warpgroups keep the tensor core alternating between them.  Each
+// buffer has its own barriers, so no wait can see a barrier two phases ahead.  Every
+// mbarrier wait is bounded; on expiry the kernel records OCTO_ETIMEOUT, drains its own
+// copies and MMAs, frees TMEM and returns.
 
 #include <cuda_bf16.h>
 
@@ -35,7 +38,7 @@ constexpr int kNS = 3;
 constexpr int kThreads = 384;
 constexpr uint32_t kQBytes = 2 * 2 * 128 * 128;     // 2 heads x 2 chunks x 128 rows x 128 B
 constexpr uint32_t kKVStage = 2 * 2 * 64 * 128;     // K + V, 2 chunks x 64 rows x 128 B each
-constexpr uint32_t kPBytes = 2 * 128 * 128;         // 2 heads x 128 rows x 128 B
+constexpr uint32_t kPBytes = 2 * 2 * 128 * 128;     // 2 heads x 2 buffers x 128 rows x 128 B
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kQBytes;
 constexpr uint32_t kOffP = kOffKV + kNS * kKVStage;
@@ -63,10 +66,10 @@ struct Bars {
   uint64_t q_full;
   uint64_t kv_full[kNS];
   uint64_t kv_empty[kNS];
-  uint64_t s_full[2];
-  uint64_t s_free[2];
-  uint64_t p_full[2];
-  uint64_t o_done[2];
+  uint64_t s_full[2][2];   // [head][buffer]
+  uint64_t s_free[2][2];
+  uint64_t p_full[2][2];
+  uint64_t o_done[2][2];
   uint64_t drain;
   uint32_t tmem_base;
   volatile int32_t abort;
@@ -118,12 +121,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&B->kv_full[s], 1);
       mbar_init(&B->kv_empty[s], 1);
     }
-    for (int h = 0; h < 2; h++) {
-      mbar_init(&B->s_full[h], 1);
-      mbar_init(&B->s_free[h], 128);
-      mbar_init(&B->p_full[h], 128);
-      mbar_init(&B->o_done[h], 1);
-    }
+    for (int h = 0; h < 2; h++)
+      for (int b = 0; b < 2; b++) {
+        mbar_init(&B->s_full[h][b], 1);
+        mbar_init(&B->s_free[h][b], 128);
+        mbar_init(&B->p_full[h][b], 128);
+        mbar_init(&B->o_done[h][b], 1);
+      }
     mbar_init(&B->drain, 1);
     B->abort = 0;
     fence_mbar_init();
@@ -152,11 +156,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 2; c++)
           tma_load_3d(smem + kOffQ + (hh * 2 + c) * 16384, &tmQ, &B->q_full, c * 64, h0 + hh, row0);
       int32_t issued = 0;
+      uint32_t page_next = p.entries[e0].kv_page;
       for (int32_t j = 0; j < n; j++) {
         const int st = j % kNS;
+        const uint32_t page = page_next;
+        if (j + 1 < n) page_next = p.entries[e0 + j + 1].kv_page;   // off the critical path
         if (j >= kNS && !wait_or_abort(&B->kv_empty[st], ((j / kNS) - 1) & 1, B, p.status)) break;
-        const octo_entry e = p.entries[e0 + j];
-        const int32_t krow = (int32_t)((e.kv_page * (uint32_t)p.Hkv + (uint32_t)g) * 64u);
+        const int32_t krow = (int32_t)((page * (uint32_t)p.Hkv + (uint32_t)g) * 64u);
         uint8_t* kd = smem + kOffKV + st * kKVStage;
         mbar_expect_tx(&B->kv_full[st], kKVStage);
         tma_load_2d(kd, &tmK, &B->kv_full[st], 0, krow);
@@ -173,56 +179,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0 && n > 0) {
-      auto issue_S = [&](int hh, int st) {
-        const uint32_t d = tbase + 256 + hh * 64;
+      auto issue_S = [&](int hh, int st, int b) {
+        const uint32_t d = tbase + 256 + hh * 128 + b * 64;
         const uint32_t qa = sQ + hh * 32768;
         const uint32_t kb = sKV + st * kKVStage;
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
           uint64_t a = desc_sw128(qa + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-          uint64_t b = desc_sw128(kb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-          mma_f16_ss(d, a, b, kIdS, kk > 0);
+          uint64_t bb = desc_sw128(kb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+          mma_f16_ss(d, a, bb, kIdS, kk > 0);
         }
-        mma_commit(&B->s_full[hh]);
+        mma_commit(&B->s_full[hh][b]);
       };
-      auto issue_PV = [&](int hh, int st, bool first) {
+      auto issue_PV = [&](int hh, int st, int b, bool first) {
         const uint32_t d = tbase + hh * 128;
-        const uint32_t pa = sP + hh * 16384;
+        const uint32_t pa = sP + (hh * 2 + b) * 16384;
         const uint32_t vb = sKV + st * kKVStage + 16384;
 #pragma unroll
         for (int kk = 0; kk < 4; kk++) {
           uint64_t a = desc_sw128(pa + kk * 32, 16, 1024);
-          uint64_t b = desc_sw128(vb + kk * 2048, 8192, 1024);
-          mma_f16_ss(d, a, b, kIdO, (!first || kk > 0) ? 1u : 0u);
+          uint64_t bb = desc_sw128(vb + kk * 2048, 8192, 1024);
+          mma_f16_ss(d, a, bb, kIdO, (!first || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&B->o_done[hh]);
+        mma_commit(&B->o_done[hh][b]);
       };
-      bool ok = wait_or_abort(&B->q_full, 0, B, p.status) && wait_or_abort(&B->kv_full[0], 0, B, p.status);
-      if (ok) {
+      // S runs two entries ahead of P V
+      bool ok = wait_or_abort(&B->q_full, 0, B, p.status);
+      for (int32_t j = 0; ok && j < min(n, 2); j++) {
+        if (!(ok = wait_or_abort(&B->kv_full[j], 0, B, p.status))) break;
         tc_fence_after();
-        issue_S(0, 0);
-        issue_S(1, 0);
+        issue_S(0, j, j);
+        issue_S(1, j, j);
       }
       for (int32_t j = 0; ok && j < n; j++) {
         const int st = j % kNS;
-        const int st2 = (j + 1) % kNS;
-        if (!(ok = wait_or_abort(&B->p_full[0], j & 1, B, p.status))) break;
+        const int b = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        const int32_t j2 = j + 2;
+        const int st2 = j2 % kNS;
+        if (!(ok = wait_or_abort(&B->p_full[0][b], ph, B, p.status))) break;
         tc_fence_after();
-        issue_PV(0, st, j == 0);
-        if (j + 1 < n) {
-          if (!(ok = wait_or_abort(&B->kv_full[st2], ((j + 1) / kNS) & 1, B, p.status))) break;
-          if (!(ok = wait_or_abort(&B->s_free[0], j & 1, B, p.status))) break;
+        issue_PV(0, st, b, j == 0);
+        if (j2 < n) {
+          if (!(ok = wait_or_abort(&B->kv_full[st2], (j2 / kNS) & 1, B, p.status))) break;
+          if (!(ok = wait_or_abort(&B->s_free[0][b], ph, B, p.status))) break;
           tc_fence_after();
-          issue_S(0, st2);
+          issue_S(0, st2, b);
         }
-        if (!(ok = wait_or_abort(&B->p_full[1], j & 1, B, p.status))) break;
+        if (!(ok = wait_or_abort(&B->p_full[1][b], ph, B, p.status))) break;
         tc_fence_after();
-        issue_PV(1, st, j == 0);
+        issue_PV(1, st, b, j == 0);
         mma_commit(&B->kv_empty[st]);
-        if (j + 1 < n) {
-          if (!(ok = wait_or_abort(&B->s_free[1], j & 1, B, p.status))) break;
+        if (j2 < n) {
+          if (!(ok = wait_or_abort(&B->s_free[1][b], ph, B, p.status))) break;
           tc_fence_after();
-          issue_S(1, st2);
+          issue_S(1, st2, b);
         }
       }
       // drain: all MMAs this thread issued are complete before TMEM is released
@@ -235,21 +246,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tS = tbase + lane_off + 256 + hh * 64;
+    const uint32_t tS0 = tbase + lane_off + 256 + hh * 128;
     const uint32_t tO = tbase + lane_off + hh * 128;
-    const uint32_t prow = sP + hh * 16384 + r * 128;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    octo_entry e_next = p.entries[e0];
     for (int32_t j = 0; j < n; j++) {
-      const octo_entry e = p.entries[e0 + j];
-      if (!(ok = warp_wait(&B->s_full[hh], j & 1, B, p.status))) break;
+      const octo_entry e = e_next;
+      if (j + 1 < n) e_next = p.entries[e0 + j + 1];   // prefetch, off the critical path
+      const int b = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!(ok = warp_wait(&B->s_full[hh][b], ph, B, p.status))) break;
       tc_fence_after();
       uint32_t s0[32], s1[32];
-      tmem_ld32(tS, s0);
-      tmem_ld32(tS + 32, s1);
+      tmem_ld32(tS0 + b * 64, s0);
+      tmem_ld32(tS0 + b * 64 + 32, s1);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&B->s_free[hh]);
+      mbar_arrive(&B->s_free[hh][b]);
       float x[64];
 #pragma unroll
       for (int i = 0; i < 32; i++) {
@@ -283,17 +297,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       float ls = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; i++) {
-        float a = ex2(x[2 * i] - msub), b = ex2(x[2 * i + 1] - msub);
-        ls += a + b;
-        pk[i] = pack_bf16(a, b);
+        float a = ex2(x[2 * i] - msub), c = ex2(x[2 * i + 1] - msub);
+        ls += a + c;
+        pk[i] = pack_bf16(a, c);
       }
       l += ls;
-      // PV of the previous entry must be done before P or O is overwritten
-      if (j > 0) {
-        if (!(ok = warp_wait(&B->o_done[hh], (j - 1) & 1, B, p.status))) break;
+      // P buffer b was last read by P V of entry j - 2
+      if (j >= 2) {
+        if (!(ok = warp_wait(&B->o_done[hh][b], ((j - 2) >> 1) & 1, B, p.status))) break;
         tc_fence_after();
       }
       if (__any_sync(0xffffffffu, need)) {
+        // O must hold every P V so far before it is rescaled
+        if (!(ok = warp_wait(&B->o_done[hh][(j - 1) & 1], ((j - 1) >> 1) & 1, B, p.status))) break;
+        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 4; c++) {
           uint32_t ov[32];
@@ -305,15 +322,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
       }
+      const uint32_t prow = sP + (hh * 2 + b) * 16384 + r * 128;
 #pragma unroll
       for (int c = 0; c < 8; c++)
         st_shared_v4(prow + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&B->p_full[hh]);
+      mbar_arrive(&B->p_full[hh][b]);
     }
     // ---------------- epilogue ----------------
-    if (ok && n > 0 && warp_wait(&B->o_done[hh], (n - 1) & 1, B, p.status)) {
+    if (ok && n > 0 && warp_wait(&B->o_done[hh][(n - 1) & 1], ((n - 1) >> 1) & 1, B, p.status)) {
       tc_fence_after();
       const float inv = 1.f / l;
       const int h = h0 + hh;

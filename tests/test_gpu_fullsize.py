@@ -190,10 +190,14 @@ def _check_invariants(W, out):
     G = W.Hq // W.Hkv
     N = out["N"]
     sk = dk.sum(dim=(0, 2))                                  # [Hkv, d]
+    print("invariants: |sum dK| %.4g (scale %.4g)" % (float(sk.abs().max()), float(dk.abs().sum(dim=(0, 2)).max())))
     assert float(sk.abs().max()) <= 1e-2 * float(dk.abs().sum(dim=(0, 2)).max()) + 1e-3
     want = W.do.double().view(N, W.Hkv, G, W.d).sum(dim=(0, 2))  # [Hkv, d]
     sv = dv.sum(dim=(0, 2))
-    assert float((sv - want).abs().max()) <= 2e-2 * float(want.abs().max()) + 1e-2 * math.sqrt(N)
+    print("invariants: |sum dV - sum dO| %.4g (max |sum dO| %.4g)" % (float((sv - want).abs().max()),
+                                                                     float(want.abs().max())))
+    # measured ~1e-3 of max|want|; a lost or half-read reader contribution shows as percents
+    assert float((sv - want).abs().max()) <= 5e-3 * float(want.abs().max()) + 1e-2 * math.sqrt(N)
 
 
 def test_episode_fwd_bwd_full(lib, oracle_mod):
