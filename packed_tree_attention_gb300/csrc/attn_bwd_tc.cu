@@ -91,10 +91,23 @@ __device__ __forceinline__ void p_ds_to_smem(uint32_t tS, uint32_t tP, const oct
 #pragma unroll
     for (int i = 0; i < 16; i++) {
       const int j0 = 32 * half + 2 * i, j1 = j0 + 1;
-      const float p0 = (j0 >= lo && j0 < hi) ? ex2(__uint_as_float(sv[2 * i]) * scale_log2 - lse2) : 0.f;
-      const float p1 = (j1 >= lo && j1 < hi) ? ex2(__uint_as_float(sv[2 * i + 1]) * scale_log2 - lse2) : 0.f;
+      float a0, a1;
+      fma2(a0, a1, __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]), scale_log2, -lse2);
+      // MUFU for 3 of every 4 pairs, the FMA-pipe polynomial for the 4th
+      if ((i & 3) == 3) {
+        a0 = ex2_poly(a0);
+        a1 = ex2_poly(a1);
+      } else {
+        a0 = ex2(a0);
+        a1 = ex2(a1);
+      }
+      const float p0 = (j0 >= lo && j0 < hi) ? a0 : 0.f;
+      const float p1 = (j1 >= lo && j1 < hi) ? a1 : 0.f;
+      float d0, d1;
+      add2(d0, d1, __uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1]), -Dr, -Dr);
+      mul2(d0, d1, d0, d1, p0, p1);
       pk[i] = pack_bf16(p0, p1);
-      dk[i] = pack_bf16(p0 * (__uint_as_float(dv[2 * i]) - Dr), p1 * (__uint_as_float(dv[2 * i + 1]) - Dr));
+      dk[i] = pack_bf16(d0, d1);
     }
 #pragma unroll
     for (int q = 0; q < 4; q++) {

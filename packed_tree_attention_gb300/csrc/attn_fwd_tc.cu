@@ -8,19 +8,22 @@
 // One CTA = one q-tile x two query heads of one kv-head group (GQA: the pair shares each
 // K/V page it loads).  Warp roles (384 threads):
 //   warp 0      TMA producer: Q once (2 heads x 128 rows x 128 d), then K and V of each
-//               entry's page through a 3-stage ring
+//               entry's page through a 5-stage ring (a page load takes ~1.3 us, several
+//               entries' worth of tensor work, so it has to start well ahead)
 //   warp 1      MMA issuer (one thread): S_h = Q_h K^T (M128 N64 K16 x8) and
 //               O_h += P_h V (M128 N128 K16 x4), accumulators in TMEM
 //   warp 2      TMEM allocator (512 columns: O_0, O_1, and two S buffers per head)
 //   warps 4-7   softmax of head 0, warps 8-11 softmax of head 1: one row per thread,
 //               S read with tcgen05.ld, mask from the entry rectangle, online softmax
 //               in the log2 domain with lazy rescaling (O is rescaled in TMEM only when
-//               the running max grows by more than 2^8), P written to shared memory in
-//               the 128-byte-swizzled K-major layout the MMA reads
-// S and P are double-buffered per head: the MMA issuer runs S two entries ahead, so a
-// softmax warpgroup starts entry j+1 while the tensor core still runs P V of entry j,
-// and the two heads' warpgroups keep the tensor core alternating between them.  Each
-// buffer has its own barriers, so no wait can see a barrier two phases ahead.  Every
+//               the running max grows by more than 2^8), P written back to TMEM as bf16
+//               over the S it came from; P V takes its A operand from TMEM
+// S (and the P that replaces it) is double-buffered per head: the MMA issuer runs S two
+// entries ahead, so a softmax warpgroup starts entry j+1 while the tensor core still runs
+// P V of entry j, and the two heads' warpgroups keep the tensor core alternating between
+// them.  MMAs of one issuer execute in order, so S of entry j+2 overwrites a buffer only
+// after P V of entry j has read the P in it.  Each buffer has its own barriers, so no
+// wait can see a barrier two phases ahead.  Every
 // mbarrier wait is bounded; on expiry the kernel records OCTO_ETIMEOUT, drains its own
 // copies and MMAs, frees TMEM and returns.
 
@@ -34,15 +37,13 @@ namespace {
 
 using namespace tc;
 
-constexpr int kNS = 3;
+constexpr int kNS = 5;
 constexpr int kThreads = 384;
 constexpr uint32_t kQBytes = 2 * 2 * 128 * 128;     // 2 heads x 2 chunks x 128 rows x 128 B
 constexpr uint32_t kKVStage = 2 * 2 * 64 * 128;     // K + V, 2 chunks x 64 rows x 128 B each
-constexpr uint32_t kPBytes = 2 * 2 * 128 * 128;     // 2 heads x 2 buffers x 128 rows x 128 B
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kQBytes;
-constexpr uint32_t kOffP = kOffKV + kNS * kKVStage;
-constexpr uint32_t kOffBar = kOffP + kPBytes;
+constexpr uint32_t kOffBar = kOffKV + kNS * kKVStage;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 
 constexpr uint32_t kIdS = idesc_bf16(128, 64, 0, 0);
@@ -67,7 +68,6 @@ struct Bars {
   uint64_t kv_full[kNS];
   uint64_t kv_empty[kNS];
   uint64_t s_full[2][2];   // [head][buffer]
-  uint64_t s_free[2][2];
   uint64_t p_full[2][2];
   uint64_t o_done[2][2];
   uint64_t drain;
@@ -124,7 +124,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int h = 0; h < 2; h++)
       for (int b = 0; b < 2; b++) {
         mbar_init(&B->s_full[h][b], 1);
-        mbar_init(&B->s_free[h][b], 128);
         mbar_init(&B->p_full[h][b], 128);
         mbar_init(&B->o_done[h][b], 1);
       }
@@ -143,7 +142,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t sQ = smem_u32(smem + kOffQ);
   const uint32_t sKV = smem_u32(smem + kOffKV);
-  const uint32_t sP = smem_u32(smem + kOffP);
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -193,13 +191,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_PV = [&](int hh, int st, int b, bool first) {
         const uint32_t d = tbase + hh * 128;
-        const uint32_t pa = sP + (hh * 2 + b) * 16384;
+        const uint32_t pa = tbase + 256 + hh * 128 + b * 64;   // P (bf16 pairs) over S
         const uint32_t vb = sKV + st * kKVStage + 16384;
 #pragma unroll
         for (int kk = 0; kk < 4; kk++) {
-          uint64_t a = desc_sw128(pa + kk * 32, 16, 1024);
           uint64_t bb = desc_sw128(vb + kk * 2048, 8192, 1024);
-          mma_f16_ss(d, a, bb, kIdO, (!first || kk > 0) ? 1u : 0u);
+          mma_f16_ts(d, pa + kk * 8, bb, kIdO, (!first || kk > 0) ? 1u : 0u);
         }
         mma_commit(&B->o_done[hh][b]);
       };
@@ -221,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_PV(0, st, b, j == 0);
         if (j2 < n) {
+          // buffer b held P of entry j, which P V above has read (in-order MMAs)
           if (!(ok = wait_or_abort(&B->kv_full[st2], (j2 / kNS) & 1, B, p.status))) break;
-          if (!(ok = wait_or_abort(&B->s_free[0][b], ph, B, p.status))) break;
           tc_fence_after();
           issue_S(0, st2, b);
         }
@@ -231,8 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_PV(1, st, b, j == 0);
         mma_commit(&B->kv_empty[st]);
         if (j2 < n) {
-          if (!(ok = wait_or_abort(&B->s_free[1][b], ph, B, p.status))) break;
-          tc_fence_after();
           issue_S(1, st2, b);
         }
       }
@@ -262,13 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tS0 + b * 64, s0);
       tmem_ld32(tS0 + b * 64 + 32, s1);
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&B->s_free[hh][b]);
+      // raw scores; the scale is folded into the exponent below
       float x[64];
 #pragma unroll
       for (int i = 0; i < 32; i++) {
-        x[i] = __uint_as_float(s0[i]) * p.scale_log2;
-        x[32 + i] = __uint_as_float(s1[i]) * p.scale_log2;
+        x[i] = __uint_as_float(s0[i]);
+        x[32 + i] = __uint_as_float(s1[i]);
       }
       const bool full = e.q_lo == 0 && e.kv_lo == 0 && e.kv_hi == 64 && !(e.flags & 1);
       if (!full) {
@@ -279,9 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 64; i++)
           if (i < lo || i >= hi) x[i] = -INFINITY;
       }
-      float mc = x[0];
-#pragma unroll
-      for (int i = 1; i < 64; i++) mc = fmaxf(mc, x[i]);
+      const float mc = max64(x) * p.scale_log2;
       bool need = false;
       float factor = 1.f;
       if (j == 0) {
@@ -293,20 +285,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         need = true;
       }
       const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+      // p = 2^(s * scale_log2 - msub): MUFU for 3 of every 4 pairs, the FMA-pipe
+      // polynomial for the 4th; eight running partial sums
       uint32_t pk[32];
-      float ls = 0.f;
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < 32; i++) {
-        float a = ex2(x[2 * i] - msub), c = ex2(x[2 * i + 1] - msub);
-        ls += a + c;
+        float a, c;
+        fma2(a, c, x[2 * i], x[2 * i + 1], p.scale_log2, -msub);
+        if ((i & 3) == 3) {
+          a = ex2_poly(a);
+          c = ex2_poly(c);
+        } else {
+          a = ex2(a);
+          c = ex2(c);
+        }
+        add2(ps[2 * (i & 3)], ps[2 * (i & 3) + 1], ps[2 * (i & 3)], ps[2 * (i & 3) + 1], a, c);
         pk[i] = pack_bf16(a, c);
       }
-      l += ls;
-      // P buffer b was last read by P V of entry j - 2
-      if (j >= 2) {
-        if (!(ok = warp_wait(&B->o_done[hh][b], ((j - 2) >> 1) & 1, B, p.status))) break;
-        tc_fence_after();
-      }
+      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       if (__any_sync(0xffffffffu, need)) {
         // O must hold every P V so far before it is rescaled
         if (!(ok = warp_wait(&B->o_done[hh][(j - 1) & 1], ((j - 1) >> 1) & 1, B, p.status))) break;
@@ -322,11 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
       }
-      const uint32_t prow = sP + (hh * 2 + b) * 16384 + r * 128;
-#pragma unroll
-      for (int c = 0; c < 8; c++)
-        st_shared_v4(prow + ((c ^ (r & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_async_smem();
+      // P over the first 32 columns of this S buffer (its S is no longer needed)
+      tmem_st32(tS0 + b * 64, pk);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&B->p_full[hh][b]);
     }

@@ -107,6 +107,18 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T: A (M rows x K) read from TMEM, lane = row, two
+// bf16 values per 32-bit column in K order
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // arrive on the mbarrier once every tcgen05 op this thread issued so far has completed
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -163,6 +175,66 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x on the FMA and integer pipes, to take part of the exponentials off the MUFU pipe.
+// x = j + f with j = round(x) found by adding and subtracting 1.5 * 2^23, f in [-1/2, 1/2];
+// 2^f from a degree-3 polynomial whose coefficients were fitted for least maximum relative
+// error on [-1/2, 1/2] (7.6e-5, far below the 2^-8 of the bf16 probabilities it feeds);
+// j is added to the exponent field.  x is clamped below at -126 (the result is then ~1e-38,
+// i.e. zero for a probability); valid up to x = +127.
+__device__ __forceinline__ float ex2_poly(float x) {
+  x = fmaxf(x, -126.f);
+  const float t = x + 12582912.f;
+  const int j = __float_as_int(t) - 0x4B400000;
+  const float f = x - (t - 12582912.f);
+  float p = fmaf(f, 0.055170797f, 0.24260911f);
+  p = fmaf(f, p, 0.69326097f);
+  p = fmaf(f, p, 0.9999282f);
+  return __int_as_float(__float_as_int(p) + (j << 23));
+}
+
+// packed pairs of fp32 (sm_100 f32x2 instructions)
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+// (a0, a1) * b + c
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2pack(a0, a1)), "l"(f2pack(b, b)), "l"(f2pack(c, c)));
+  f2unpack(r, d0, d1);
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  uint64_t r;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2pack(a0, a1)), "l"(f2pack(b0, b1)));
+  f2unpack(r, d0, d1);
+}
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  uint64_t r;
+  asm("mul.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2pack(a0, a1)), "l"(f2pack(b0, b1)));
+  f2unpack(r, d0, d1);
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// maximum of 64 values as a shallow tree of 3-input maxima
+__device__ __forceinline__ float max64(const float (&x)[64]) {
+  float a[22];
+#pragma unroll
+  for (int i = 0; i < 21; i++) a[i] = max3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  a[21] = x[63];
+  float b[8];
+#pragma unroll
+  for (int i = 0; i < 7; i++) b[i] = max3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+  b[7] = a[21];
+  return max3(max3(b[0], b[1], b[2]), max3(b[3], b[4], b[5]), fmaxf(b[6], b[7]));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
