@@ -15,6 +15,11 @@
 // k_dq_tc    one CTA per (q-tile, kv head, query-head pair), like the forward: per entry
 //              S, dP, then dQ += dS K                         (M128 rows x N128 d, K = keys)
 //
+// Both kernels issue their small (N = 64) MMAs from two threads: issuing, not executing,
+// is what a single issuer is limited by at these tile sizes.  In k_dkdv_tc each issuer
+// owns one Q/dO stage and its own dV^T/dK^T accumulators; the epilogue adds the two in a
+// fixed order, so the sums stay deterministic.
+//
 // Shared-memory tiles are 128-byte swizzled; a [rows x 64 keys] tile of P or dS written by
 // the softmax warps is read as a K-major A operand (dQ) or an MN-major B operand (dK/dV),
 // and the TMA-loaded [rows x d] Q / dO tiles serve as K-major A (S, dP) and MN-major A
@@ -60,6 +65,7 @@ struct Ctl {
 };
 
 __device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, Ctl* C, int32_t* status) {
+  if (mbar_test(bar, parity)) return true;
   for (uint32_t i = 0; i < kSpinLimit; i++) {
     if (mbar_try(bar, parity)) return true;
     if ((i & 1023) == 1023 && C->abort) return false;
@@ -122,7 +128,7 @@ __device__ __forceinline__ void p_ds_to_smem(uint32_t tS, uint32_t tP, const oct
 // =====================================================================================
 // dK / dV
 // =====================================================================================
-constexpr int kDkThreads = 320;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 softmax
+constexpr int kDkThreads = 352;   // warp 0 TMA, warps 1-2 MMA (1 also TMEM), warps 3-10 softmax
 // smem: K/V page 32KB | 2 stages x (Q 32KB + dO 32KB) | 2 stages x (P 16KB + dS 16KB)
 constexpr uint32_t kDkOffKV = 0;
 constexpr uint32_t kDkOffQD = 32768;
@@ -139,7 +145,7 @@ struct DkBars {
   uint64_t sd_free[2];
   uint64_t pd_full[2];
   uint64_t mm_done[2];
-  uint64_t acc_done;   // single use: every accumulation MMA of the CTA has completed
+  uint64_t acc_done;   // single use, 2 arrivals: every accumulation MMA has completed
   uint64_t drain;
   Ctl ctl;
 };
@@ -168,8 +174,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       mbar_init(&B->pd_full[s], 128);
       mbar_init(&B->mm_done[s], 1);
     }
-    mbar_init(&B->acc_done, 1);
-    mbar_init(&B->drain, 1);
+    mbar_init(&B->acc_done, 2);
+    mbar_init(&B->drain, 2);
     C->abort = 0;
     fence_mbar_init();
   }
@@ -181,7 +187,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = C->tmem_base;
-  // TMEM columns: dV^T [0,64), dK^T [64,128), S_s [128 + 128 s, +64), dP_s [192 + 128 s, +64)
+  // TMEM columns: issuer k's dV^T [128 k, +64) and dK^T [128 k + 64, +64);
+  // stage s: S [256 + 128 s, +64), dP [320 + 128 s, +64)
   const uint32_t sKV = smem_u32(smem + kDkOffKV);
   const uint32_t sQD = smem_u32(smem + kDkOffQD);
   const uint32_t sPS = smem_u32(smem + kDkOffPS);
@@ -217,66 +224,63 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       for (int32_t w = max(0, issued - 2); w < issued; w++)
         mbar_wait(&B->qd_full[w & 1], (w >> 1) & 1, p.status, OCTO_ETIMEOUT);
     }
-  } else if (warp == 1) {
-    if (lane == 0 && n > 0) {
-      auto issue_sd = [&](int32_t w) {
-        const int st = w & 1;
-        const uint32_t q = sQD + st * kDkStageQD, dO = q + 32768;
-        const uint32_t tS = tbase + 128 + 128 * st, tP = tS + 64;
+  } else if (warp == 1 || warp == 2) {
+    // issuer k = warp - 1 takes the items w with w % 2 == k (Q/dO stage k)
+    const int k = warp - 1;
+    if (lane == 0 && n > k) {
+      const uint32_t q = sQD + k * kDkStageQD, dO = q + 32768;
+      const uint32_t pP = sPS + k * kDkStagePS, pS = pP + 16384;
+      const uint64_t dq_k = desc_sw128(q, 16, 1024), ddo_k = desc_sw128(dO, 16, 1024);
+      const uint64_t dk_b = desc_sw128(sKV, 16, 1024), dv_b = desc_sw128(sKV + 16384, 16, 1024);
+      const uint64_t dqT = desc_sw128(q, 16384, 1024), ddoT = desc_sw128(dO, 16384, 1024);
+      const uint64_t dpP = desc_sw128(pP, 16384, 1024), dpS = desc_sw128(pS, 16384, 1024);
+      const uint32_t tS = tbase + 256 + 128 * k, tP = tS + 64;
+      const uint32_t tdV = tbase + 128 * k, tdK = tdV + 64;
+      bool ok = wait_ab(&B->kv_full, 0, C, p.status);
+      for (int32_t w = k; ok && w < n; w += 2) {
+        const uint32_t ph = (w >> 1) & 1;
+        if (!(ok = wait_ab(&B->qd_full[k], ph, C, p.status))) break;
+        // S / dP buffer k: the softmax has read item w - 2's
+        if (w >= 2 && !(ok = wait_ab(&B->sd_free[k], ph ^ 1, C, p.status))) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_f16_ss(tS, desc_sw128(q + off, 16, 1024), desc_sw128(sKV + koff, 16, 1024), kIdRK, kk > 0);
+          const uint32_t qo = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          const uint32_t ko = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+          mma_f16_ss(tS, dq_k + qo, dk_b + ko, kIdRK, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint32_t voff = 16384 + (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_f16_ss(tP, desc_sw128(dO + off, 16, 1024), desc_sw128(sKV + voff, 16, 1024), kIdRK, kk > 0);
+          const uint32_t qo = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          const uint32_t vo = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+          mma_f16_ss(tP, ddo_k + qo, dv_b + vo, kIdRK, kk > 0);
         }
-        mma_commit(&B->sd_full[st]);
-      };
-      auto issue_acc = [&](int32_t w) {
-        const int st = w & 1;
-        const uint32_t q = sQD + st * kDkStageQD, dO = q + 32768;
-        const uint32_t pP = sPS + st * kDkStagePS, pS = pP + 16384;
+        mma_commit(&B->sd_full[k]);
+        if (!(ok = wait_ab(&B->pd_full[k], ph, C, p.status))) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
           // dV^T += dO^T P ; dK^T += Q^T dS  (K = 16 rows per step: 2 swizzle atoms)
-          const uint32_t acc = (w > 0 || kk > 0) ? 1u : 0u;
-          mma_f16_ss(tbase + 0, desc_sw128(dO + kk * 2048, 16384, 1024), desc_sw128(pP + kk * 2048, 16384, 1024),
-                     kIdDK, acc);
-          mma_f16_ss(tbase + 64, desc_sw128(q + kk * 2048, 16384, 1024), desc_sw128(pS + kk * 2048, 16384, 1024),
-                     kIdDK, acc);
+          const uint32_t acc = (w > k || kk > 0) ? 1u : 0u;
+          const uint64_t o = (uint64_t)(kk * (2048 >> 4));
+          mma_f16_ss(tdV, ddoT + o, dpP + o, kIdDK, acc);
+          mma_f16_ss(tdK, dqT + o, dpS + o, kIdDK, acc);
         }
-        mma_commit(&B->mm_done[st]);
-      };
-      bool ok = wait_ab(&B->kv_full, 0, C, p.status) && wait_ab(&B->qd_full[0], 0, C, p.status);
-      if (ok) {
-        tc_fence_after();
-        issue_sd(0);
-      }
-      for (int32_t w = 0; ok && w < n; w++) {
-        if (w + 1 < n) {
-          const int st1 = (w + 1) & 1;
-          if (!(ok = wait_ab(&B->qd_full[st1], ((w + 1) >> 1) & 1, C, p.status))) break;
-          if (w + 1 >= 2 && !(ok = wait_ab(&B->sd_free[st1], (((w + 1) >> 1) - 1) & 1, C, p.status))) break;
-          tc_fence_after();
-          issue_sd(w + 1);
-        }
-        if (!(ok = wait_ab(&B->pd_full[w & 1], (w >> 1) & 1, C, p.status))) break;
-        tc_fence_after();
-        issue_acc(w);
+        mma_commit(&B->mm_done[k]);
       }
       if (ok) mma_commit(&B->acc_done);
       mma_commit(&B->drain);
       mbar_wait(&B->drain, 0, p.status, OCTO_ETIMEOUT);
+    } else if (lane == 0 && n > 0) {
+      // no item for this issuer: its arrivals only
+      mma_commit(&B->acc_done);
+      mma_commit(&B->drain);
+      mbar_wait(&B->drain, 0, p.status, OCTO_ETIMEOUT);
     }
   } else {
-    // warps 2-9: two warpgroups; warpgroup k takes the items w with w % 2 == k (stage k).
+    // warps 3-10: two warpgroups; warpgroup k takes the items w with w % 2 == k (stage k).
     // A warp reaches the TMEM lanes of its quadrant warp % 4.
-    const int wg = (warp - 2) >> 2;
+    const int wg = (warp - 3) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       if (!(ok = warp_wait_ab(&B->sd_full[st], (w >> 1) & 1, C, p.status))) break;
       tc_fence_after();
       const uint32_t pP = sPS + st * kDkStagePS;
-      p_ds_to_smem(tbase + lane_off + 128 + 128 * st, tbase + lane_off + 192 + 128 * st, e, r, row_ok, lse2, Dr,
+      p_ds_to_smem(tbase + lane_off + 256 + 128 * st, tbase + lane_off + 320 + 128 * st, e, r, row_ok, lse2, Dr,
                    p.scale_log2, pP + r * 128, pP + 16384 + r * 128);
       tc_fence_before();
       mbar_arrive(&B->sd_free[st]);
@@ -328,17 +332,25 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         const int dd = r;
         float* dvp = p.dv + (size_t)krow * 128 + dd;
         float* dkp = p.dk + (size_t)krow * 128 + dd;
+        const bool two = n > 1;   // the second issuer accumulated something
 #pragma unroll 1
-        for (int c = 0; c < 2; c++) {
-          uint32_t v[32], k[32];
+        for (int c = 0; c < 4; c++) {
+          // c = 0, 1: dV^T columns; c = 2, 3: dK^T columns
+          uint32_t v[32];
           tmem_ld32(tbase + lane_off + c * 32, v);
-          tmem_ld32(tbase + lane_off + 64 + c * 32, k);
-          tmem_wait_ld();
+          if (two) {
+            uint32_t v1[32];
+            tmem_ld32(tbase + lane_off + 128 + c * 32, v1);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; j++) {
-            dvp[(size_t)(c * 32 + j) * 128] = __uint_as_float(v[j]);
-            dkp[(size_t)(c * 32 + j) * 128] = __uint_as_float(k[j]) * p.scale;
+            for (int j = 0; j < 32; j++) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
+          } else {
+            tmem_wait_ld();
           }
+          float* dst = c < 2 ? dvp : dkp;
+          const float sc = c < 2 ? 1.f : p.scale;
+#pragma unroll
+          for (int j = 0; j < 32; j++) dst[(size_t)((c & 1) * 32 + j) * 128] = __uint_as_float(v[j]) * sc;
         }
       }
     }
@@ -352,7 +364,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
 // =====================================================================================
 // dQ
 // =====================================================================================
-constexpr int kDqThreads = 320;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 softmax
+constexpr int kDqThreads = 352;   // warp 0 TMA, warps 1-2 MMA per head (1 also TMEM), warps 3-10 softmax
 constexpr int kDqNS = 2;
 // smem: Q 64KB (2 heads) | dO 64KB | 2 stages x K/V 32KB | dS 2 heads x 16KB
 constexpr uint32_t kDqOffQ = 0;
@@ -396,7 +408,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&B->q_full, 1);
     for (int s = 0; s < kDqNS; s++) {
       mbar_init(&B->kv_full[s], 1);
-      mbar_init(&B->kv_empty[s], 1);
+      mbar_init(&B->kv_empty[s], 2);   // released by both heads' dQ MMAs
     }
     for (int h = 0; h < 2; h++) {
       mbar_init(&B->s_full[h], 1);
@@ -404,7 +416,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mbar_init(&B->p_full[h], 128);
       mbar_init(&B->o_done[h], 1);
     }
-    mbar_init(&B->drain, 1);
+    mbar_init(&B->drain, 2);
     C->abort = 0;
     fence_mbar_init();
   }
@@ -454,69 +466,62 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       for (int32_t j = max(0, issued - kDqNS); j < issued; j++)
         mbar_wait(&B->kv_full[j % kDqNS], (j / kDqNS) & 1, p.status, OCTO_ETIMEOUT);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
+    // MMA issuer for head hh = warp - 1
+    const int hh = warp - 1;
     if (lane == 0 && n > 0) {
-      auto issue_sd = [&](int hh, int st) {
-        const uint32_t tS = tbase + 256 + 128 * hh, tP = tS + 64;
-        const uint32_t q = sQ + hh * 32768, dO = sDO + hh * 32768;
-        const uint32_t kv = sKV + st * 32768;
+      const uint32_t tS = tbase + 256 + 128 * hh, tP = tS + 64, tQ = tbase + 128 * hh;
+      const uint64_t dq_h = desc_sw128(sQ + hh * 32768, 16, 1024), ddo_h = desc_sw128(sDO + hh * 32768, 16, 1024);
+      const uint64_t dk0 = desc_sw128(sKV, 16, 1024), dv0 = desc_sw128(sKV + 16384, 16, 1024);
+      const uint64_t dkmn = desc_sw128(sKV, 8192, 1024);   // K page as the MN-major B operand [keys x d]
+      const uint64_t dds = desc_sw128(sDS + hh * 16384, 16, 1024);
+      auto issue_sd = [&](int st) {
+        const uint64_t ko_st = (uint64_t)(st * (32768 >> 4));
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_f16_ss(tS, desc_sw128(q + off, 16, 1024), desc_sw128(kv + koff, 16, 1024), kIdRK, kk > 0);
+          const uint32_t qo = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          const uint32_t ko = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+          mma_f16_ss(tS, dq_h + qo, dk0 + ko_st + ko, kIdRK, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint32_t voff = 16384 + (kk >> 2) * 8192 + (kk & 3) * 32;
-          mma_f16_ss(tP, desc_sw128(dO + off, 16, 1024), desc_sw128(kv + voff, 16, 1024), kIdRK, kk > 0);
+          const uint32_t qo = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          const uint32_t vo = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+          mma_f16_ss(tP, ddo_h + qo, dv0 + ko_st + vo, kIdRK, kk > 0);
         }
         mma_commit(&B->s_full[hh]);
       };
-      auto issue_dq = [&](int hh, int st, bool first) {
-        const uint32_t d = tbase + 128 * hh;
-        const uint32_t a0 = sDS + hh * 16384;
-        const uint32_t kb = sKV + st * 32768;  // K page as the MN-major B operand [keys x d]
+      auto issue_dq = [&](int st, bool first) {
+        const uint64_t kb = dkmn + (uint64_t)(st * (32768 >> 4));
 #pragma unroll
         for (int kk = 0; kk < 4; kk++)
-          mma_f16_ss(d, desc_sw128(a0 + kk * 32, 16, 1024), desc_sw128(kb + kk * 2048, 8192, 1024), kIdDQ,
-                     (!first || kk > 0) ? 1u : 0u);
+          mma_f16_ss(tQ, dds + (uint64_t)(kk * 2), kb + (uint64_t)(kk * (2048 >> 4)), kIdDQ, (!first || kk > 0) ? 1u : 0u);
         mma_commit(&B->o_done[hh]);
       };
       bool ok = wait_ab(&B->q_full, 0, C, p.status) && wait_ab(&B->kv_full[0], 0, C, p.status);
       if (ok) {
         tc_fence_after();
-        issue_sd(0, 0);
-        issue_sd(1, 0);
+        issue_sd(0);
       }
       for (int32_t j = 0; ok && j < n; j++) {
         const int st = j % kDqNS, st2 = (j + 1) % kDqNS;
-        if (!(ok = wait_ab(&B->p_full[0], j & 1, C, p.status))) break;
+        if (!(ok = wait_ab(&B->p_full[hh], j & 1, C, p.status))) break;
         tc_fence_after();
-        issue_dq(0, st, j == 0);
-        if (j + 1 < n) {
-          if (!(ok = wait_ab(&B->kv_full[st2], ((j + 1) / kDqNS) & 1, C, p.status))) break;
-          if (!(ok = wait_ab(&B->s_free[0], j & 1, C, p.status))) break;
-          tc_fence_after();
-          issue_sd(0, st2);
-        }
-        if (!(ok = wait_ab(&B->p_full[1], j & 1, C, p.status))) break;
-        tc_fence_after();
-        issue_dq(1, st, j == 0);
+        issue_dq(st, j == 0);
         mma_commit(&B->kv_empty[st]);
         if (j + 1 < n) {
-          if (!(ok = wait_ab(&B->s_free[1], j & 1, C, p.status))) break;
+          if (!(ok = wait_ab(&B->kv_full[st2], ((j + 1) / kDqNS) & 1, C, p.status))) break;
+          if (!(ok = wait_ab(&B->s_free[hh], j & 1, C, p.status))) break;
           tc_fence_after();
-          issue_sd(1, st2);
+          issue_sd(st2);
         }
       }
       mma_commit(&B->drain);
       mbar_wait(&B->drain, 0, p.status, OCTO_ETIMEOUT);
     }
   } else {
-    // warps 2-9: warpgroup hh handles head h0 + hh; a warp reaches TMEM quadrant warp % 4
-    const int hh = (warp - 2) >> 2;
+    // warps 3-10: warpgroup hh handles head h0 + hh; a warp reaches TMEM quadrant warp % 4
+    const int hh = (warp - 3) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;

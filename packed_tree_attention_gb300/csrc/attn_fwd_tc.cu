@@ -10,8 +10,10 @@
 //   warp 0      TMA producer: Q once (2 heads x 128 rows x 128 d), then K and V of each
 //               entry's page through a 5-stage ring (a page load takes ~1.3 us, several
 //               entries' worth of tensor work, so it has to start well ahead)
-//   warp 1      MMA issuer (one thread): S_h = Q_h K^T (M128 N64 K16 x8) and
-//               O_h += P_h V (M128 N128 K16 x4), accumulators in TMEM
+//   warps 1, 3  MMA issuers, one thread each, one per head: S_h = Q_h K^T (M128 N64
+//               K16 x8) and O_h += P_h V (M128 N128 K16 x4), accumulators in TMEM.  With
+//               64-key pages the MMAs are small, and issuing them (not executing them)
+//               is what a single issuer is limited by; two issue streams double that rate
 //   warp 2      TMEM allocator (512 columns: O_0, O_1, and two S buffers per head)
 //   warps 4-7   softmax of head 0, warps 8-11 softmax of head 1: one row per thread,
 //               S read with tcgen05.ld, mask from the entry rectangle, online softmax
@@ -76,6 +78,7 @@ struct Bars {
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* B, int32_t* status) {
+  if (mbar_test(bar, parity)) return true;
   for (uint32_t i = 0; i < kSpinLimit; i++) {
     if (mbar_try(bar, parity)) return true;
     if ((i & 1023) == 1023 && B->abort) return false;
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&B->q_full, 1);
     for (int s = 0; s < kNS; s++) {
       mbar_init(&B->kv_full[s], 1);
-      mbar_init(&B->kv_empty[s], 1);
+      mbar_init(&B->kv_empty[s], 2);   // released by both heads' P V
     }
     for (int h = 0; h < 2; h++)
       for (int b = 0; b < 2; b++) {
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&B->p_full[h][b], 128);
         mbar_init(&B->o_done[h][b], 1);
       }
-    mbar_init(&B->drain, 1);
+    mbar_init(&B->drain, 2);
     B->abort = 0;
     fence_mbar_init();
   }
@@ -174,30 +177,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int32_t j = max(0, issued - kNS); j < issued; j++)
         mbar_wait(&B->kv_full[j % kNS], (j / kNS) & 1, p.status, OCTO_ETIMEOUT);
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 1 || warp == 3) {
+    // ---------------- MMA issuers: warp 1 for head 0, warp 3 for head 1 ----------------
+    const int hh = warp == 1 ? 0 : 1;
     if (lane == 0 && n > 0) {
-      auto issue_S = [&](int hh, int st, int b) {
-        const uint32_t d = tbase + 256 + hh * 128 + b * 64;
-        const uint32_t qa = sQ + hh * 32768;
-        const uint32_t kb = sKV + st * kKVStage;
+      // Descriptors are built once; per MMA only the start-address field moves (all smem
+      // offsets here stay inside the 14-bit field), so each issue is an add and the MMA.
+      const uint64_t dq0 = desc_sw128(sQ + hh * 32768, 16, 1024);
+      const uint64_t dk0 = desc_sw128(sKV, 16, 1024);
+      const uint64_t dv0 = desc_sw128(sKV + 16384, 8192, 1024);
+      const uint32_t dO_ = tbase + hh * 128;
+      const uint32_t dS_ = tbase + 256 + hh * 128;
+      auto issue_S = [&](int st, int b) {
+        const uint64_t kb = dk0 + (uint64_t)(st * (kKVStage >> 4));
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
-          uint64_t a = desc_sw128(qa + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-          uint64_t bb = desc_sw128(kb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-          mma_f16_ss(d, a, bb, kIdS, kk > 0);
+          const uint32_t qo = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          const uint32_t ko = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+          mma_f16_ss(dS_ + b * 64, dq0 + qo, kb + ko, kIdS, kk > 0);
         }
         mma_commit(&B->s_full[hh][b]);
       };
-      auto issue_PV = [&](int hh, int st, int b, bool first) {
-        const uint32_t d = tbase + hh * 128;
-        const uint32_t pa = tbase + 256 + hh * 128 + b * 64;   // P (bf16 pairs) over S
-        const uint32_t vb = sKV + st * kKVStage + 16384;
+      auto issue_PV = [&](int st, int b, bool first) {
+        const uint32_t pa = dS_ + b * 64;   // P (bf16 pairs) over S
+        const uint64_t vb = dv0 + (uint64_t)(st * (kKVStage >> 4));
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++) {
-          uint64_t bb = desc_sw128(vb + kk * 2048, 8192, 1024);
-          mma_f16_ts(d, pa + kk * 8, bb, kIdO, (!first || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 4; kk++)
+          mma_f16_ts(dO_, pa + kk * 8, vb + (uint64_t)(kk * (2048 >> 4)), kIdO, (!first || kk > 0) ? 1u : 0u);
         mma_commit(&B->o_done[hh][b]);
       };
       // S runs two entries ahead of P V
@@ -205,30 +211,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int32_t j = 0; ok && j < min(n, 2); j++) {
         if (!(ok = wait_or_abort(&B->kv_full[j], 0, B, p.status))) break;
         tc_fence_after();
-        issue_S(0, j, j);
-        issue_S(1, j, j);
+        issue_S(j, j);
       }
       for (int32_t j = 0; ok && j < n; j++) {
         const int st = j % kNS;
         const int b = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
         const int32_t j2 = j + 2;
-        const int st2 = j2 % kNS;
-        if (!(ok = wait_or_abort(&B->p_full[0][b], ph, B, p.status))) break;
+        if (!(ok = wait_or_abort(&B->p_full[hh][b], (j >> 1) & 1, B, p.status))) break;
         tc_fence_after();
-        issue_PV(0, st, b, j == 0);
-        if (j2 < n) {
-          // buffer b held P of entry j, which P V above has read (in-order MMAs)
-          if (!(ok = wait_or_abort(&B->kv_full[st2], (j2 / kNS) & 1, B, p.status))) break;
-          tc_fence_after();
-          issue_S(0, st2, b);
-        }
-        if (!(ok = wait_or_abort(&B->p_full[1][b], ph, B, p.status))) break;
-        tc_fence_after();
-        issue_PV(1, st, b, j == 0);
+        issue_PV(st, b, j == 0);
         mma_commit(&B->kv_empty[st]);
         if (j2 < n) {
-          issue_S(1, st2, b);
+          // buffer b held P of entry j, which P V above has read (in-order MMAs)
+          if (!(ok = wait_or_abort(&B->kv_full[j2 % kNS], (j2 / kNS) & 1, B, p.status))) break;
+          tc_fence_after();
+          issue_S(j2 % kNS, b);
         }
       }
       // drain: all MMAs this thread issued are complete before TMEM is released
