@@ -4,28 +4,34 @@
 // reader's gradient into the producer's KV; shared prefix tokens are owned once, so their
 // dK/dV are sums over every reader row.  Two kernels, no atomics:
 //
-// k_dkdv_tc  one CTA per (kv page, kv head), pages launched heaviest first.  It walks the
-//            page's reader entries (the plan's kv-page-major list, in list order) and, for
-//            each reader entry and each of the G query heads of the group:
-//              S  = Q K^T,  dP = dO V^T                       (M128 rows x N64 keys, K = d)
-//              P  = exp(S - LSE),  dS = P (dP - D)            (softmax warps, entry mask)
-//              dV^T += dO^T P,  dK^T += Q^T dS                (M128 d x N64 keys, K = rows)
-//            The transposed accumulators keep the MMA at M = 128 with 64-key pages.  The
-//            page's dK/dV are written once at the end (dK scaled).
-// k_dq_tc    one CTA per (q-tile, kv head, query-head pair), like the forward: per entry
-//              S, dP, then dQ += dS K                         (M128 rows x N128 d, K = keys)
+// k_dkdv_tc  one CTA per (page pair, kv head): two consecutive own pages of a segment give
+//            128 keys (a lone page fills keys 0-63).  It walks the pair's work items (a
+//            query tile against one or both pages, each half with its own entry mask) and,
+//            for each item and each of the G query heads of the group, computes in the
+//            transposed orientation, keys on the TMEM lanes:
+//              S^T = K Q^T,  dP^T = V dO^T                    (M128 keys x N128 rows, K = d)
+//              P^T = exp(S^T - LSE),  dS^T = P^T (dP^T - D)   (softmax warps, written back to
+//                                                              TMEM as bf16 over S^T / dP^T)
+//              dV += P^T dO,  dK += dS^T Q                    (M128 keys x N128 d, K = rows,
+//                                                              A operand read from TMEM)
+//            Every MMA is 128 x 128 and each Q/dO tile load serves 128 keys.  The pair's
+//            dK/dV are written once at the end (dK scaled).
+// k_dq_tc    one CTA per (q-tile, query head), tiles heaviest first: the tile's entries two
+//            at a time (128 keys), per step
+//              S = Q K^T,  dP = dO V^T                        (M128 rows x N128 keys, K = d)
+//              P = exp(S - LSE),  dS = P (dP - D)             (softmax warps, dS written back
+//                                                              to TMEM as bf16 over dP)
+//              dQ += dS K                                     (M128 rows x N128 d, K = keys,
+//                                                              A operand read from TMEM)
 //
-// Both kernels issue their small (N = 64) MMAs from two threads: issuing, not executing,
-// is what a single issuer is limited by at these tile sizes.  In k_dkdv_tc each issuer
-// owns one Q/dO stage and its own dV^T/dK^T accumulators; the epilogue adds the two in a
-// fixed order, so the sums stay deterministic.
-//
-// Shared-memory tiles are 128-byte swizzled; a [rows x 64 keys] tile of P or dS written by
-// the softmax warps is read as a K-major A operand (dQ) or an MN-major B operand (dK/dV),
-// and the TMA-loaded [rows x d] Q / dO tiles serve as K-major A (S, dP) and MN-major A
-// (dK^T, dV^T).  Waits are bounded as in the forward.
+// Shared-memory tiles are 128-byte swizzled.  A 128-key K or V operand is two TMA boxes of
+// 64 rows per 64-column d-half, so the two pages need not be adjacent in the pool.  The
+// [rows x d] Q / dO tiles and the K tiles serve both as K-major operands and as MN-major B
+// operands; P and dS never touch shared memory.  Waits are bounded as in the forward.
 
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "internal.h"
 #include "tc_common.cuh"
@@ -35,9 +41,7 @@ namespace {
 
 using namespace tc;
 
-constexpr uint32_t kIdRK = idesc_bf16(128, 64, 0, 0);    // rows x keys, both K-major
-constexpr uint32_t kIdDK = idesc_bf16(128, 64, 1, 1);    // d x keys, both MN-major
-constexpr uint32_t kIdDQ = idesc_bf16(128, 128, 0, 1);   // rows x d, B MN-major
+constexpr uint32_t kIdDQ = idesc_bf16(128, 128, 0, 1);   // rows x d, A from TMEM, B MN-major
 
 struct BwdParams {
   const int32_t* tile_off;
@@ -48,6 +52,11 @@ struct BwdParams {
   const int32_t* csc_perm;
   const int32_t* page_off;
   const int32_t* page_order;
+  const int32_t* pair_pages;
+  const int32_t* pair_item_off;
+  const int32_t* pair_n_items;
+  const int32_t* pair_order;
+  const PairItem* pair_items;
   const float* lse;
   const float* Dv;
   float* dq;
@@ -78,78 +87,38 @@ __device__ __forceinline__ bool warp_wait_ab(uint64_t* bar, uint32_t parity, Ctl
   return __all_sync(0xffffffffu, wait_ab(bar, parity, C, status));
 }
 
-// Loads this thread's row of S and dP (64 columns each, 32 at a time) from TMEM, applies
-// the entry mask, and writes the row of P (if p_row != 0) and of dS, as bf16, into the
-// 128-byte-swizzled row tiles at p_row / ds_row (byte addresses of this row).  Half a row
-// is live at a time.
-__device__ __forceinline__ void p_ds_to_smem(uint32_t tS, uint32_t tP, const octo_entry& e, int r, bool row_ok,
-                                             float lse2, float Dr, float scale_log2, uint32_t p_row, uint32_t ds_row) {
-  int lo = (int)e.kv_lo, hi = (int)e.kv_hi;
-  if (!row_ok || r < (int)e.q_lo) lo = 64;
-  if (e.flags & 1) hi = min(hi, r + e.diag + 1);
-#pragma unroll
-  for (int half = 0; half < 2; half++) {
-    uint32_t sv[32], dv[32];
-    tmem_ld32(tS + 32 * half, sv);
-    tmem_ld32(tP + 32 * half, dv);
-    tmem_wait_ld();
-    uint32_t pk[16], dk[16];
-#pragma unroll
-    for (int i = 0; i < 16; i++) {
-      const int j0 = 32 * half + 2 * i, j1 = j0 + 1;
-      float a0, a1;
-      fma2(a0, a1, __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]), scale_log2, -lse2);
-      // MUFU for 3 of every 4 pairs, the FMA-pipe polynomial for the 4th
-      if ((i & 3) == 3) {
-        a0 = ex2_poly(a0);
-        a1 = ex2_poly(a1);
-      } else {
-        a0 = ex2(a0);
-        a1 = ex2(a1);
-      }
-      const float p0 = (j0 >= lo && j0 < hi) ? a0 : 0.f;
-      const float p1 = (j1 >= lo && j1 < hi) ? a1 : 0.f;
-      float d0, d1;
-      add2(d0, d1, __uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1]), -Dr, -Dr);
-      mul2(d0, d1, d0, d1, p0, p1);
-      pk[i] = pack_bf16(p0, p1);
-      dk[i] = pack_bf16(d0, d1);
-    }
-#pragma unroll
-    for (int q = 0; q < 4; q++) {
-      const int c = 4 * half + q;
-      const uint32_t off = (uint32_t)((c ^ (r & 7)) << 4);
-      if (p_row) st_shared_v4(p_row + off, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-      st_shared_v4(ds_row + off, dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
-    }
-  }
-}
-
 // =====================================================================================
 // dK / dV
 // =====================================================================================
-constexpr int kDkThreads = 352;   // warp 0 TMA, warps 1-2 MMA (1 also TMEM), warps 3-10 softmax
-// smem: K/V page 32KB | 2 stages x (Q 32KB + dO 32KB) | 2 stages x (P 16KB + dS 16KB)
-constexpr uint32_t kDkOffKV = 0;
-constexpr uint32_t kDkOffQD = 32768;
+constexpr int kDkThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, warp 2 row statistics, warps 4-11 softmax
+// smem: K pair 32KB | V pair 32KB | 2 stages x (Q 32KB + dO 32KB) | 2 stages x row statistics
+constexpr uint32_t kDkOffK = 0;
+constexpr uint32_t kDkOffV = 32768;
+constexpr uint32_t kDkOffQD = 65536;
 constexpr uint32_t kDkStageQD = 65536;
-constexpr uint32_t kDkOffPS = kDkOffQD + 2 * kDkStageQD;
-constexpr uint32_t kDkStagePS = 32768;
-constexpr uint32_t kDkOffBar = kDkOffPS + 2 * kDkStagePS;
+constexpr uint32_t kDkOffSt = kDkOffQD + 2 * kDkStageQD;
+constexpr uint32_t kDkStageSt = 1152;   // log2-domain LSE [128], D [128], the PairItem
+constexpr uint32_t kDkOffBar = kDkOffSt + 2 * kDkStageSt;
 constexpr uint32_t kDkSmem = kDkOffBar + 256 + 1024;
+constexpr uint32_t kIdKR = idesc_bf16(128, 128, 0, 0);   // keys x rows, both K-major
+constexpr uint32_t kIdKD = idesc_bf16(128, 128, 0, 1);   // keys x d, A from TMEM, B MN-major
 
 struct DkBars {
   uint64_t kv_full;
   uint64_t qd_full[2];
-  uint64_t sd_full[2];
-  uint64_t sd_free[2];
-  uint64_t pd_full[2];
-  uint64_t mm_done[2];
-  uint64_t acc_done;   // single use, 2 arrivals: every accumulation MMA has completed
+  uint64_t qd_free[2];
+  uint64_t st_full[2];
+  uint64_t st_free[2];
+  uint64_t s_full, dp_full;   // S^T / dP^T of the current step in TMEM
+  uint64_t s_read, dp_read;   // softmax warpgroup 0 has read its S^T / dP^T columns
+  uint64_t p_full, ds_full;   // P^T / dS^T written back to TMEM
+  uint64_t acc_done;          // single use: every accumulation MMA has completed
   uint64_t drain;
   Ctl ctl;
 };
 
+// One CTA per (page pair, kv head).  TMEM: S^T [0,128) (P^T as bf16 over its first 64
+// columns), dP^T [128,256) (dS^T likewise), dV [256,384), dK [384,512); lane = key.
 __global__ void __launch_bounds__(kDkThreads, 1)
     k_dkdv_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, BwdParams p) {
@@ -159,23 +128,29 @@ __global__ void __launch_bounds__(kDkThreads, 1)
   Ctl* C = &B->ctl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t g = blockIdx.x % p.Hkv;
-  const int32_t page = p.page_order[blockIdx.x / p.Hkv];
-  const int32_t c0 = p.page_off[page];
-  const int32_t n_ent = p.page_off[page + 1] - c0;
+  const int32_t pr = p.pair_order[blockIdx.x / p.Hkv];
+  const int32_t pa = p.pair_pages[2 * pr], pb = p.pair_pages[2 * pr + 1];
+  const PairItem* items = p.pair_items + p.pair_item_off[pr];
+  const int32_t n_items = p.pair_n_items[pr];
   const int32_t G = p.G;
-  const int32_t n = n_ent * G;  // work items: (reader entry, head)
+  const int32_t n = n_items * G;   // steps: (item, query head of the group)
 
   if (threadIdx.x == 0) {
     mbar_init(&B->kv_full, 1);
     for (int s = 0; s < 2; s++) {
       mbar_init(&B->qd_full[s], 1);
-      mbar_init(&B->sd_full[s], 1);
-      mbar_init(&B->sd_free[s], 128);
-      mbar_init(&B->pd_full[s], 128);
-      mbar_init(&B->mm_done[s], 1);
+      mbar_init(&B->qd_free[s], 1);
+      mbar_init(&B->st_full[s], 32);
+      mbar_init(&B->st_free[s], 256);
     }
-    mbar_init(&B->acc_done, 2);
-    mbar_init(&B->drain, 2);
+    mbar_init(&B->s_full, 1);
+    mbar_init(&B->dp_full, 1);
+    mbar_init(&B->s_read, 128);
+    mbar_init(&B->dp_read, 128);
+    mbar_init(&B->p_full, 256);
+    mbar_init(&B->ds_full, 256);
+    mbar_init(&B->acc_done, 1);
+    mbar_init(&B->drain, 1);
     C->abort = 0;
     fence_mbar_init();
   }
@@ -187,31 +162,33 @@ __global__ void __launch_bounds__(kDkThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = C->tmem_base;
-  // TMEM columns: issuer k's dV^T [128 k, +64) and dK^T [128 k + 64, +64);
-  // stage s: S [256 + 128 s, +64), dP [320 + 128 s, +64)
-  const uint32_t sKV = smem_u32(smem + kDkOffKV);
+  const uint32_t sK = smem_u32(smem + kDkOffK);
+  const uint32_t sV = smem_u32(smem + kDkOffV);
   const uint32_t sQD = smem_u32(smem + kDkOffQD);
-  const uint32_t sPS = smem_u32(smem + kDkOffPS);
-  const int32_t krow = (page * p.Hkv + g) * 64;
 
   if (warp == 0) {
     if (lane == 0 && n > 0) {
       prefetch_map(&tmQ);
       prefetch_map(&tmDO);
-      mbar_expect_tx(&B->kv_full, 32768);
-      tma_load_2d(smem + kDkOffKV, &tmK, &B->kv_full, 0, krow);
-      tma_load_2d(smem + kDkOffKV + 8192, &tmK, &B->kv_full, 64, krow);
-      tma_load_2d(smem + kDkOffKV + 16384, &tmV, &B->kv_full, 0, krow);
-      tma_load_2d(smem + kDkOffKV + 24576, &tmV, &B->kv_full, 64, krow);
+      mbar_expect_tx(&B->kv_full, pb >= 0 ? 65536 : 32768);
+      for (int hp = 0; hp < 2; hp++) {
+        const int32_t pg = hp ? pb : pa;
+        if (pg < 0) continue;
+        const int32_t krow = (pg * p.Hkv + g) * 64;
+        // keys 64 hp .. 64 hp + 63 of each 128-row d-half
+        tma_load_2d(smem + kDkOffK + hp * 8192, &tmK, &B->kv_full, 0, krow);
+        tma_load_2d(smem + kDkOffK + 16384 + hp * 8192, &tmK, &B->kv_full, 64, krow);
+        tma_load_2d(smem + kDkOffV + hp * 8192, &tmV, &B->kv_full, 0, krow);
+        tma_load_2d(smem + kDkOffV + 16384 + hp * 8192, &tmV, &B->kv_full, 64, krow);
+      }
       int32_t issued = 0;
-      int32_t row0_next = p.tile_row0[p.entries[p.csc_perm[c0]].q_tile];
+      int32_t row0_next = items[0].row0;
       for (int32_t w = 0; w < n; w++) {
         const int st = w & 1;
         const int32_t h = g * G + (w % G);
         const int32_t row0 = row0_next;
-        // the next item's tile, looked up before this item's stage wait
-        if (w + 1 < n) row0_next = (w + 1) % G ? row0 : p.tile_row0[p.entries[p.csc_perm[c0 + (w + 1) / G]].q_tile];
-        if (w >= 2 && !wait_ab(&B->mm_done[st], ((w >> 1) - 1) & 1, C, p.status)) break;
+        if (w + 1 < n) row0_next = (w + 1) % G ? row0 : items[(w + 1) / G].row0;
+        if (w >= 2 && !wait_ab(&B->qd_free[st], ((w >> 1) - 1) & 1, C, p.status)) break;
         uint8_t* dst = smem + kDkOffQD + st * kDkStageQD;
         mbar_expect_tx(&B->qd_full[st], 65536);
         tma_load_3d(dst, &tmQ, &B->qd_full[st], 0, h, row0);
@@ -224,133 +201,247 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       for (int32_t w = max(0, issued - 2); w < issued; w++)
         mbar_wait(&B->qd_full[w & 1], (w >> 1) & 1, p.status, OCTO_ETIMEOUT);
     }
-  } else if (warp == 1 || warp == 2) {
-    // issuer k = warp - 1 takes the items w with w % 2 == k (Q/dO stage k)
-    const int k = warp - 1;
-    if (lane == 0 && n > k) {
-      const uint32_t q = sQD + k * kDkStageQD, dO = q + 32768;
-      const uint32_t pP = sPS + k * kDkStagePS, pS = pP + 16384;
-      const uint64_t dq_k = desc_sw128(q, 16, 1024), ddo_k = desc_sw128(dO, 16, 1024);
-      const uint64_t dk_b = desc_sw128(sKV, 16, 1024), dv_b = desc_sw128(sKV + 16384, 16, 1024);
-      const uint64_t dqT = desc_sw128(q, 16384, 1024), ddoT = desc_sw128(dO, 16384, 1024);
-      const uint64_t dpP = desc_sw128(pP, 16384, 1024), dpS = desc_sw128(pS, 16384, 1024);
-      const uint32_t tS = tbase + 256 + 128 * k, tP = tS + 64;
-      const uint32_t tdV = tbase + 128 * k, tdK = tdV + 64;
-      bool ok = wait_ab(&B->kv_full, 0, C, p.status);
-      for (int32_t w = k; ok && w < n; w += 2) {
-        const uint32_t ph = (w >> 1) & 1;
-        if (!(ok = wait_ab(&B->qd_full[k], ph, C, p.status))) break;
-        // S / dP buffer k: the softmax has read item w - 2's
-        if (w >= 2 && !(ok = wait_ab(&B->sd_free[k], ph ^ 1, C, p.status))) break;
+  } else if (warp == 1) {
+    if (lane == 0 && n > 0) {
+      const uint64_t aK = desc_sw128(sK, 16, 1024), aV = desc_sw128(sV, 16, 1024);
+      const uint64_t bQ0 = desc_sw128(sQD, 16, 1024), bDO0 = desc_sw128(sQD + 32768, 16, 1024);
+      const uint64_t bQm0 = desc_sw128(sQD, 16384, 1024), bDOm0 = desc_sw128(sQD + 32768, 16384, 1024);
+      const uint32_t tS = tbase, tDP = tbase + 128, tDV = tbase + 256, tDK = tbase + 384;
+      auto issue_s = [&](int st) {
+        const uint64_t so = (uint64_t)(st * (kDkStageQD >> 4));
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) {
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_f16_ss(tS, aK + o, bQ0 + so + o, kIdKR, kk > 0);
+        }
+        mma_commit(&B->s_full);
+      };
+      auto issue_dp = [&](int st) {
+        const uint64_t so = (uint64_t)(st * (kDkStageQD >> 4));
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) {
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_f16_ss(tDP, aV + o, bDO0 + so + o, kIdKR, kk > 0);
+        }
+        mma_commit(&B->dp_full);
+      };
+      bool ok = wait_ab(&B->kv_full, 0, C, p.status) && wait_ab(&B->qd_full[0], 0, C, p.status);
+      if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++) {
-          const uint32_t qo = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          const uint32_t ko = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-          mma_f16_ss(tS, dq_k + qo, dk_b + ko, kIdRK, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++) {
-          const uint32_t qo = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          const uint32_t vo = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-          mma_f16_ss(tP, ddo_k + qo, dv_b + vo, kIdRK, kk > 0);
-        }
-        mma_commit(&B->sd_full[k]);
-        if (!(ok = wait_ab(&B->pd_full[k], ph, C, p.status))) break;
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int32_t w = 0; ok && w < n; w++) {
+        const int st = w & 1;
+        const uint64_t so = (uint64_t)(st * (kDkStageQD >> 4));
+        if (!(ok = wait_ab(&B->p_full, w & 1, C, p.status))) break;
         tc_fence_after();
+        // dV += P^T dO   (K = 16 query rows per MMA: 8 TMEM columns of P^T, 2 swizzle atoms of dO)
 #pragma unroll
-        for (int kk = 0; kk < 8; kk++) {
-          // dV^T += dO^T P ; dK^T += Q^T dS  (K = 16 rows per step: 2 swizzle atoms)
-          const uint32_t acc = (w > k || kk > 0) ? 1u : 0u;
-          const uint64_t o = (uint64_t)(kk * (2048 >> 4));
-          mma_f16_ss(tdV, ddoT + o, dpP + o, kIdDK, acc);
-          mma_f16_ss(tdK, dqT + o, dpS + o, kIdDK, acc);
+        for (int kk = 0; kk < 8; kk++)
+          mma_f16_ts(tDV, tS + kk * 8, bDOm0 + so + (uint64_t)(kk * (2048 >> 4)), kIdKD, (w > 0 || kk > 0) ? 1u : 0u);
+        if (w + 1 < n) {
+          // S^T of the next step overwrites P^T only after the MMAs above have read it
+          if (!(ok = wait_ab(&B->qd_full[st ^ 1], ((w + 1) >> 1) & 1, C, p.status))) break;
+          tc_fence_after();
+          issue_s(st ^ 1);
         }
-        mma_commit(&B->mm_done[k]);
+        if (!(ok = wait_ab(&B->ds_full, w & 1, C, p.status))) break;
+        tc_fence_after();
+        // dK += dS^T Q
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++)
+          mma_f16_ts(tDK, tDP + kk * 8, bQm0 + so + (uint64_t)(kk * (2048 >> 4)), kIdKD, (w > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&B->qd_free[st]);
+        if (w + 1 < n) issue_dp(st ^ 1);
       }
       if (ok) mma_commit(&B->acc_done);
       mma_commit(&B->drain);
       mbar_wait(&B->drain, 0, p.status, OCTO_ETIMEOUT);
-    } else if (lane == 0 && n > 0) {
-      // no item for this issuer: its arrivals only
-      mma_commit(&B->acc_done);
-      mma_commit(&B->drain);
-      mbar_wait(&B->drain, 0, p.status, OCTO_ETIMEOUT);
     }
-  } else {
-    // warps 3-10: two warpgroups; warpgroup k takes the items w with w % 2 == k (stage k).
-    // A warp reaches the TMEM lanes of its quadrant warp % 4.
-    const int wg = (warp - 3) >> 2;
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    bool ok = true;
-    int32_t w = wg;
-    // item metadata, loaded one item ahead (this warpgroup's next item is w + 2)
-    octo_entry e_n;
-    int32_t rows_n = 0;
-    float lse2_n = 0.f, Dr_n = 0.f;
-    auto load_item = [](const BwdParams& pp, int32_t c0_, int32_t G_, int32_t g_, int32_t wi, int r_, octo_entry& e,
-                        int32_t& rows, float& lse2, float& Dr) {
-      e = pp.entries[pp.csc_perm[c0_ + wi / G_]];
-      const int32_t h = g_ * G_ + (wi % G_);
-      rows = pp.tile_rows[e.q_tile];
-      const int64_t row = (int64_t)pp.tile_row0[e.q_tile] + r_;
-      const bool ok_ = r_ < rows;
-      lse2 = ok_ ? pp.lse[(int64_t)h * pp.n_rows + row] * 1.4426950408889634f : 0.f;
-      Dr = ok_ ? pp.Dv[(int64_t)h * pp.n_rows + row] : 0.f;
-    };
-    if (w < n) load_item(p, c0, G, g, w, r, e_n, rows_n, lse2_n, Dr_n);
-    for (; w < n; w += 2) {
-      const int st = w & 1;
-      const octo_entry e = e_n;
-      const bool row_ok = r < rows_n;
-      const float lse2 = lse2_n, Dr = Dr_n;
-      if (w + 2 < n) load_item(p, c0, G, g, w + 2, r, e_n, rows_n, lse2_n, Dr_n);
-      // the accumulation MMAs of item w - 2 read this stage's P / dS buffers
-      if (w >= 2) {
-        if (!(ok = warp_wait_ab(&B->mm_done[st], ((w >> 1) - 1) & 1, C, p.status))) break;
+  } else if (warp == 2) {
+    // row statistics of each step's (query tile, head), and the item, into the stage ring
+    if (n > 0) {
+      PairItem it = items[0];
+      PairItem it_next = it;
+      if (n_items > 1) it_next = items[1];
+      for (int32_t w = 0; w < n; w++) {
+        const int st = w & 1;
+        if (w > 0 && w % G == 0) {
+          it = it_next;
+          if (w / G + 1 < n_items) it_next = items[w / G + 1];
+        }
+        const int32_t h = g * G + (w % G);
+        const int r0 = lane * 4;
+        float l[4], d[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          const int r = r0 + q;
+          const int64_t idx = (int64_t)h * p.n_rows + it.row0 + r;
+          l[q] = r < it.rows ? p.lse[idx] * 1.4426950408889634f : 0.f;
+          d[q] = r < it.rows ? p.Dv[idx] : 0.f;
+        }
+        if (w >= 2 && !warp_wait_ab(&B->st_free[st], ((w >> 1) - 1) & 1, C, p.status)) break;
+        float* S = reinterpret_cast<float*>(smem + kDkOffSt + st * kDkStageSt);
+        *reinterpret_cast<float4*>(S + r0) = make_float4(l[0], l[1], l[2], l[3]);
+        *reinterpret_cast<float4*>(S + 128 + r0) = make_float4(d[0], d[1], d[2], d[3]);
+        if (lane == 0) *reinterpret_cast<PairItem*>(S + 256) = it;
+        mbar_arrive(&B->st_full[st]);
       }
-      if (!(ok = warp_wait_ab(&B->sd_full[st], (w >> 1) & 1, C, p.status))) break;
-      tc_fence_after();
-      const uint32_t pP = sPS + st * kDkStagePS;
-      p_ds_to_smem(tbase + lane_off + 256 + 128 * st, tbase + lane_off + 320 + 128 * st, e, r, row_ok, lse2, Dr,
-                   p.scale_log2, pP + r * 128, pP + 16384 + r * 128);
-      tc_fence_before();
-      mbar_arrive(&B->sd_free[st]);
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&B->pd_full[st]);
     }
-    // epilogue (warpgroup 0): TMEM lane = d, 64 columns = page slots.  It waits on a
-    // single-use barrier: a parity wait on mm_done of the other warpgroup's stage could be
-    // one completion short and still pass.
-    if (wg == 0 && n > 0) {
-      bool fin = ok && warp_wait_ab(&B->acc_done, 0, C, p.status);
+  } else if (warp >= 4) {
+    // softmax warps: warpgroup c takes query rows [64 c, 64 c + 64) of every step; a warp
+    // reaches the TMEM lanes (keys) of its quadrant warp % 4
+    const int c = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int k = wq * 32 + lane;
+    const int hk = k >> 6, j = k & 63;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tbase + lane_off, tDP = tS + 128;
+    bool ok = true;
+    for (int32_t w = 0; ok && w < n; w++) {
+      const int st = w & 1;
+      if (!(ok = warp_wait_ab(&B->st_full[st], (w >> 1) & 1, C, p.status))) break;
+      const float* S = reinterpret_cast<const float*>(smem + kDkOffSt + st * kDkStageSt);
+      const PairItem* it = reinterpret_cast<const PairItem*>(S + 256);
+      // visible rows of this key: rmin <= r < rmax
+      const int lo = it->lo[hk], hi = it->hi[hk];
+      int rmin = it->qlo[hk];
+      if (it->cz[hk]) rmin = max(rmin, j - it->diag[hk]);
+      const int rmax = (j >= lo && j < hi) ? it->rows : 0;
+      const float* L = S + 64 * c;
+      const float* Dr = S + 128 + 64 * c;
+      if (!(ok = warp_wait_ab(&B->s_full, w & 1, C, p.status))) break;
+      tc_fence_after();
+      uint32_t x0[32], x1[32];
+      tmem_ld32(tS + 64 * c, x0);
+      tmem_ld32(tS + 64 * c + 32, x1);
+      tmem_wait_ld();
+      if (c == 0) {
+        tc_fence_before();
+        mbar_arrive(&B->s_read);
+      }
+      // most steps see all 64 rows of this warpgroup for every key: no per-element mask
+      const bool all_vis = __all_sync(0xffffffffu, rmin <= 64 * c && rmax >= 64 * c + 64);
+      float P[64];
+      auto p_phase = [&](auto masked) {
+#pragma unroll
+        for (int i = 0; i < 64; i += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(L + i);
+          const uint32_t* xs = i < 32 ? x0 : x1;
+          const int ii = i & 31;
+          float a0, a1, a2, a3;
+          fma2v(a0, a1, __uint_as_float(xs[ii]), __uint_as_float(xs[ii + 1]), p.scale_log2, -l4.x, -l4.y);
+          fma2v(a2, a3, __uint_as_float(xs[ii + 2]), __uint_as_float(xs[ii + 3]), p.scale_log2, -l4.z, -l4.w);
+          // MUFU for 3 of every 4 pairs, the FMA-pipe polynomial for the 4th
+          if ((i & 7) == 4) {
+            a2 = ex2_poly(a2);
+            a3 = ex2_poly(a3);
+          } else {
+            a2 = ex2(a2);
+            a3 = ex2(a3);
+          }
+          a0 = ex2(a0);
+          a1 = ex2(a1);
+          if constexpr (decltype(masked)::value) {
+            const int r = 64 * c + i;
+            a0 = (r >= rmin && r < rmax) ? a0 : 0.f;
+            a1 = (r + 1 >= rmin && r + 1 < rmax) ? a1 : 0.f;
+            a2 = (r + 2 >= rmin && r + 2 < rmax) ? a2 : 0.f;
+            a3 = (r + 3 >= rmin && r + 3 < rmax) ? a3 : 0.f;
+          }
+          P[i] = a0;
+          P[i + 1] = a1;
+          P[i + 2] = a2;
+          P[i + 3] = a3;
+        }
+      };
+      if (all_vis)
+        p_phase(std::false_type{});
+      else
+        p_phase(std::true_type{});
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; i++) pk[i] = pack_bf16(P[2 * i], P[2 * i + 1]);
+      if (c == 1) {
+        // P^T of rows 64-127 lands on S^T columns that warpgroup 0 reads
+        if (!(ok = warp_wait_ab(&B->s_read, w & 1, C, p.status))) break;
+        tc_fence_after();
+      }
+      tmem_st32(tS + 32 * c, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&B->p_full);
+      if (!(ok = warp_wait_ab(&B->dp_full, w & 1, C, p.status))) break;
+      tc_fence_after();
+      auto ds_phase = [&](auto masked) {
+#pragma unroll
+        for (int half = 0; half < 2; half++) {
+          uint32_t x[32];
+          tmem_ld32(tDP + 64 * c + 32 * half, x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(Dr + 32 * half + i);
+            const int q = 32 * half + i;
+            float d0, d1, d2, d3;
+            add2(d0, d1, __uint_as_float(x[i]), __uint_as_float(x[i + 1]), -d4.x, -d4.y);
+            add2(d2, d3, __uint_as_float(x[i + 2]), __uint_as_float(x[i + 3]), -d4.z, -d4.w);
+            mul2(d0, d1, d0, d1, P[q], P[q + 1]);
+            mul2(d2, d3, d2, d3, P[q + 2], P[q + 3]);
+            if constexpr (decltype(masked)::value) {
+              // masked entries: exactly zero even where dP is not finite
+              const int r = 64 * c + q;
+              d0 = (r >= rmin && r < rmax) ? d0 : 0.f;
+              d1 = (r + 1 >= rmin && r + 1 < rmax) ? d1 : 0.f;
+              d2 = (r + 2 >= rmin && r + 2 < rmax) ? d2 : 0.f;
+              d3 = (r + 3 >= rmin && r + 3 < rmax) ? d3 : 0.f;
+            }
+            pk[q / 2] = pack_bf16(d0, d1);
+            pk[q / 2 + 1] = pack_bf16(d2, d3);
+          }
+        }
+      };
+      if (all_vis)
+        ds_phase(std::false_type{});
+      else
+        ds_phase(std::true_type{});
+      if (c == 0) {
+        tc_fence_before();
+        mbar_arrive(&B->dp_read);
+      } else {
+        if (!(ok = warp_wait_ab(&B->dp_read, w & 1, C, p.status))) break;
+        tc_fence_after();
+      }
+      tmem_st32(tDP + 32 * c, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&B->ds_full);
+      mbar_arrive(&B->st_free[st]);
+    }
+    // epilogue: warpgroup c writes d columns [64 c, 64 c + 64) of this key's dV and dK rows
+    if (n > 0) {
+      const bool fin = ok && warp_wait_ab(&B->acc_done, 0, C, p.status);
       if (fin) {
         tc_fence_after();
-        const int dd = r;
-        float* dvp = p.dv + (size_t)krow * 128 + dd;
-        float* dkp = p.dk + (size_t)krow * 128 + dd;
-        const bool two = n > 1;   // the second issuer accumulated something
+        const int32_t pg = hk ? pb : pa;
+        const size_t row = (size_t)(max(pg, 0) * p.Hkv + g) * 64 + j;
 #pragma unroll 1
-        for (int c = 0; c < 4; c++) {
-          // c = 0, 1: dV^T columns; c = 2, 3: dK^T columns
+        for (int part = 0; part < 4; part++) {
+          // part 0, 1: dV columns; 2, 3: dK columns
           uint32_t v[32];
-          tmem_ld32(tbase + lane_off + c * 32, v);
-          if (two) {
-            uint32_t v1[32];
-            tmem_ld32(tbase + lane_off + 128 + c * 32, v1);
-            tmem_wait_ld();
+          tmem_ld32(tbase + lane_off + (part < 2 ? 256 : 384) + 64 * c + 32 * (part & 1), v);
+          tmem_wait_ld();
+          if (pg >= 0) {
+            float* out = (part < 2 ? p.dv : p.dk) + row * 128 + 64 * c + 32 * (part & 1);
+            const float sc = part < 2 ? 1.f : p.scale;
 #pragma unroll
-            for (int j = 0; j < 32; j++) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
-          } else {
-            tmem_wait_ld();
+            for (int q4 = 0; q4 < 8; q4++)
+              st_global_v4(out + 4 * q4, __float_as_uint(__uint_as_float(v[4 * q4]) * sc),
+                           __float_as_uint(__uint_as_float(v[4 * q4 + 1]) * sc),
+                           __float_as_uint(__uint_as_float(v[4 * q4 + 2]) * sc),
+                           __float_as_uint(__uint_as_float(v[4 * q4 + 3]) * sc));
           }
-          float* dst = c < 2 ? dvp : dkp;
-          const float sc = c < 2 ? 1.f : p.scale;
-#pragma unroll
-          for (int j = 0; j < 32; j++) dst[(size_t)((c & 1) * 32 + j) * 128] = __uint_as_float(v[j]) * sc;
         }
       }
     }
@@ -364,28 +455,34 @@ __global__ void __launch_bounds__(kDkThreads, 1)
 // =====================================================================================
 // dQ
 // =====================================================================================
-constexpr int kDqThreads = 352;   // warp 0 TMA, warps 1-2 MMA per head (1 also TMEM), warps 3-10 softmax
+constexpr int kDqThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, warps 4-11 softmax
 constexpr int kDqNS = 2;
-// smem: Q 64KB (2 heads) | dO 64KB | 2 stages x K/V 32KB | dS 2 heads x 16KB
+// smem: Q 32KB | dO 32KB | 2 stages x (K pair 32KB + V pair 32KB)
 constexpr uint32_t kDqOffQ = 0;
-constexpr uint32_t kDqOffDO = 65536;
-constexpr uint32_t kDqOffKV = 131072;
-constexpr uint32_t kDqOffDS = kDqOffKV + kDqNS * 32768;
-constexpr uint32_t kDqOffBar = kDqOffDS + 32768;
+constexpr uint32_t kDqOffDO = 32768;
+constexpr uint32_t kDqOffKV = 65536;
+constexpr uint32_t kDqStageKV = 65536;
+constexpr uint32_t kDqOffBar = kDqOffKV + kDqNS * kDqStageKV;
 constexpr uint32_t kDqSmem = kDqOffBar + 256 + 1024;
+constexpr uint32_t kIdRP = idesc_bf16(128, 128, 0, 0);   // rows x keys of an entry pair, both K-major
 
 struct DqBars {
   uint64_t q_full;
   uint64_t kv_full[kDqNS];
   uint64_t kv_empty[kDqNS];
   uint64_t s_full[2];
-  uint64_t s_free[2];
-  uint64_t p_full[2];
-  uint64_t o_done[2];
+  uint64_t dp_full;
+  uint64_t dp_read;   // softmax warpgroup 0 has read its dP columns
+  uint64_t ds_full;
+  uint64_t acc_done;  // single use: every dQ MMA has completed
   uint64_t drain;
   Ctl ctl;
 };
 
+// One CTA per (query tile, query head), tiles heaviest first.  The tile's entries go two at
+// a time: keys 0-63 of a step from the first entry, 64-127 from the second (an odd last
+// entry runs alone; its dQ MMAs stop at key 64).  TMEM: S of step j in [128 (j % 2), +128),
+// dP [256, 384) with dS as bf16 over its first 64 columns, dQ [384, 512); lane = row.
 __global__ void __launch_bounds__(kDqThreads, 1)
     k_dq_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
             const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, BwdParams p) {
@@ -394,13 +491,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   DqBars* B = reinterpret_cast<DqBars*>(smem + kDqOffBar);
   Ctl* C = &B->ctl;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int32_t HP = p.G >> 1;
-  const int32_t hp = blockIdx.x % HP;
-  const int32_t g = (blockIdx.x / HP) % p.Hkv;
-  const int32_t tile = p.tile_order[blockIdx.x / (HP * p.Hkv)];
-  const int32_t h0 = g * p.G + 2 * hp;
+  const int32_t h = blockIdx.x % p.Hq;
+  const int32_t g = h / p.G;
+  const int32_t tile = p.tile_order[blockIdx.x / p.Hq];
   const int32_t e0 = p.tile_off[tile];
-  const int32_t n = p.tile_off[tile + 1] - e0;
+  const int32_t ne = p.tile_off[tile + 1] - e0;
+  const int32_t n = (ne + 1) >> 1;   // steps (entry pairs)
   const int32_t rows = p.tile_rows[tile];
   const int32_t row0 = p.tile_row0[tile];
 
@@ -408,15 +504,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&B->q_full, 1);
     for (int s = 0; s < kDqNS; s++) {
       mbar_init(&B->kv_full[s], 1);
-      mbar_init(&B->kv_empty[s], 2);   // released by both heads' dQ MMAs
+      mbar_init(&B->kv_empty[s], 1);
     }
-    for (int h = 0; h < 2; h++) {
-      mbar_init(&B->s_full[h], 1);
-      mbar_init(&B->s_free[h], 128);
-      mbar_init(&B->p_full[h], 128);
-      mbar_init(&B->o_done[h], 1);
-    }
-    mbar_init(&B->drain, 2);
+    mbar_init(&B->s_full[0], 1);
+    mbar_init(&B->s_full[1], 1);
+    mbar_init(&B->dp_full, 1);
+    mbar_init(&B->dp_read, 128);
+    mbar_init(&B->ds_full, 256);
+    mbar_init(&B->acc_done, 1);
+    mbar_init(&B->drain, 1);
     C->abort = 0;
     fence_mbar_init();
   }
@@ -428,11 +524,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = C->tmem_base;
-  // TMEM: dQ_h [128 h, +128), S_h [256 + 128 h, +64), dP_h [320 + 128 h, +64)
   const uint32_t sQ = smem_u32(smem + kDqOffQ);
   const uint32_t sDO = smem_u32(smem + kDqOffDO);
   const uint32_t sKV = smem_u32(smem + kDqOffKV);
-  const uint32_t sDS = smem_u32(smem + kDqOffDS);
 
   if (warp == 0) {
     if (lane == 0 && n > 0) {
@@ -440,130 +534,223 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       prefetch_map(&tmDO);
       prefetch_map(&tmK);
       prefetch_map(&tmV);
-      mbar_expect_tx(&B->q_full, 131072);
-      for (int hh = 0; hh < 2; hh++)
-        for (int c = 0; c < 2; c++) {
-          tma_load_3d(smem + kDqOffQ + (hh * 2 + c) * 16384, &tmQ, &B->q_full, c * 64, h0 + hh, row0);
-          tma_load_3d(smem + kDqOffDO + (hh * 2 + c) * 16384, &tmDO, &B->q_full, c * 64, h0 + hh, row0);
-        }
+      mbar_expect_tx(&B->q_full, 65536);
+      for (int c = 0; c < 2; c++) {
+        tma_load_3d(smem + kDqOffQ + c * 16384, &tmQ, &B->q_full, c * 64, h, row0);
+        tma_load_3d(smem + kDqOffDO + c * 16384, &tmDO, &B->q_full, c * 64, h, row0);
+      }
       int32_t issued = 0;
-      uint32_t page_next = p.entries[e0].kv_page;
       for (int32_t j = 0; j < n; j++) {
-        const int st = j % kDqNS;
-        const uint32_t page = page_next;
-        if (j + 1 < n) page_next = p.entries[e0 + j + 1].kv_page;   // off the critical path
-        if (j >= kDqNS && !wait_ab(&B->kv_empty[st], ((j / kDqNS) - 1) & 1, C, p.status)) break;
-        const int32_t krow = (int32_t)((page * (uint32_t)p.Hkv + (uint32_t)g) * 64u);
-        uint8_t* kd = smem + kDqOffKV + st * 32768;
-        mbar_expect_tx(&B->kv_full[st], 32768);
-        tma_load_2d(kd, &tmK, &B->kv_full[st], 0, krow);
-        tma_load_2d(kd + 8192, &tmK, &B->kv_full[st], 64, krow);
-        tma_load_2d(kd + 16384, &tmV, &B->kv_full[st], 0, krow);
-        tma_load_2d(kd + 24576, &tmV, &B->kv_full[st], 64, krow);
+        const int st = j & 1;
+        const int32_t ea = e0 + 2 * j;
+        const int32_t pa = (int32_t)p.entries[ea].kv_page;
+        const int32_t pb = 2 * j + 1 < ne ? (int32_t)p.entries[ea + 1].kv_page : -1;
+        if (j >= kDqNS && !wait_ab(&B->kv_empty[st], ((j >> 1) - 1) & 1, C, p.status)) break;
+        uint8_t* kd = smem + kDqOffKV + st * kDqStageKV;
+        mbar_expect_tx(&B->kv_full[st], pb >= 0 ? 65536 : 32768);
+        for (int hp = 0; hp < 2; hp++) {
+          const int32_t pg = hp ? pb : pa;
+          if (pg < 0) continue;
+          const int32_t krow = (pg * p.Hkv + g) * 64;
+          tma_load_2d(kd + hp * 8192, &tmK, &B->kv_full[st], 0, krow);
+          tma_load_2d(kd + 16384 + hp * 8192, &tmK, &B->kv_full[st], 64, krow);
+          tma_load_2d(kd + 32768 + hp * 8192, &tmV, &B->kv_full[st], 0, krow);
+          tma_load_2d(kd + 49152 + hp * 8192, &tmV, &B->kv_full[st], 64, krow);
+        }
         issued = j + 1;
       }
       mbar_wait(&B->q_full, 0, p.status, OCTO_ETIMEOUT);
       for (int32_t j = max(0, issued - kDqNS); j < issued; j++)
-        mbar_wait(&B->kv_full[j % kDqNS], (j / kDqNS) & 1, p.status, OCTO_ETIMEOUT);
+        mbar_wait(&B->kv_full[j & 1], (j >> 1) & 1, p.status, OCTO_ETIMEOUT);
     }
-  } else if (warp == 1 || warp == 2) {
-    // MMA issuer for head hh = warp - 1
-    const int hh = warp - 1;
+  } else if (warp == 1) {
     if (lane == 0 && n > 0) {
-      const uint32_t tS = tbase + 256 + 128 * hh, tP = tS + 64, tQ = tbase + 128 * hh;
-      const uint64_t dq_h = desc_sw128(sQ + hh * 32768, 16, 1024), ddo_h = desc_sw128(sDO + hh * 32768, 16, 1024);
-      const uint64_t dk0 = desc_sw128(sKV, 16, 1024), dv0 = desc_sw128(sKV + 16384, 16, 1024);
-      const uint64_t dkmn = desc_sw128(sKV, 8192, 1024);   // K page as the MN-major B operand [keys x d]
-      const uint64_t dds = desc_sw128(sDS + hh * 16384, 16, 1024);
-      auto issue_sd = [&](int st) {
-        const uint64_t ko_st = (uint64_t)(st * (32768 >> 4));
+      const uint64_t aQ = desc_sw128(sQ, 16, 1024), aDO = desc_sw128(sDO, 16, 1024);
+      const uint64_t bK0 = desc_sw128(sKV, 16, 1024), bV0 = desc_sw128(sKV + 32768, 16, 1024);
+      const uint64_t bKm0 = desc_sw128(sKV, 16384, 1024);   // K pair as the MN-major B operand [keys x d]
+      const uint32_t tDP = tbase + 256, tDQ = tbase + 384;
+      auto issue_s = [&](int32_t j) {
+        const int st = j & 1;
+        const uint64_t so = (uint64_t)(st * (kDqStageKV >> 4));
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
-          const uint32_t qo = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          const uint32_t ko = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-          mma_f16_ss(tS, dq_h + qo, dk0 + ko_st + ko, kIdRK, kk > 0);
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_f16_ss(tbase + 128 * st, aQ + o, bK0 + so + o, kIdRP, kk > 0);
         }
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++) {
-          const uint32_t qo = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          const uint32_t vo = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-          mma_f16_ss(tP, ddo_h + qo, dv0 + ko_st + vo, kIdRK, kk > 0);
-        }
-        mma_commit(&B->s_full[hh]);
+        mma_commit(&B->s_full[st]);
       };
-      auto issue_dq = [&](int st, bool first) {
-        const uint64_t kb = dkmn + (uint64_t)(st * (32768 >> 4));
+      auto issue_dp = [&](int32_t j) {
+        const uint64_t so = (uint64_t)((j & 1) * (kDqStageKV >> 4));
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++)
-          mma_f16_ss(tQ, dds + (uint64_t)(kk * 2), kb + (uint64_t)(kk * (2048 >> 4)), kIdDQ, (!first || kk > 0) ? 1u : 0u);
-        mma_commit(&B->o_done[hh]);
+        for (int kk = 0; kk < 8; kk++) {
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_f16_ss(tDP, aDO + o, bV0 + so + o, kIdRP, kk > 0);
+        }
+        mma_commit(&B->dp_full);
       };
       bool ok = wait_ab(&B->q_full, 0, C, p.status) && wait_ab(&B->kv_full[0], 0, C, p.status);
       if (ok) {
         tc_fence_after();
-        issue_sd(0);
+        issue_s(0);
       }
-      for (int32_t j = 0; ok && j < n; j++) {
-        const int st = j % kDqNS, st2 = (j + 1) % kDqNS;
-        if (!(ok = wait_ab(&B->p_full[hh], j & 1, C, p.status))) break;
+      if (ok && n > 1 && (ok = wait_ab(&B->kv_full[1], 0, C, p.status))) {
         tc_fence_after();
-        issue_dq(st, j == 0);
+        issue_s(1);
+      }
+      if (ok) issue_dp(0);
+      for (int32_t j = 0; ok && j < n; j++) {
+        const int st = j & 1;
+        const uint64_t so = (uint64_t)(st * (kDqStageKV >> 4));
+        if (!(ok = wait_ab(&B->ds_full, j & 1, C, p.status))) break;
+        tc_fence_after();
+        // dQ += dS K  (K = 16 keys per MMA: 8 TMEM columns of dS, 2 swizzle atoms of K)
+        const int nk = 2 * j + 1 < ne ? 8 : 4;
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++)
+          if (kk < nk)
+            mma_f16_ts(tDQ, tDP + kk * 8, bKm0 + so + (uint64_t)(kk * (2048 >> 4)), kIdDQ, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&B->kv_empty[st]);
-        if (j + 1 < n) {
-          if (!(ok = wait_ab(&B->kv_full[st2], ((j + 1) / kDqNS) & 1, C, p.status))) break;
-          if (!(ok = wait_ab(&B->s_free[hh], j & 1, C, p.status))) break;
+        // dP of the next step overwrites dS only after the MMAs above have read it
+        if (j + 1 < n) issue_dp(j + 1);
+        if (j + 2 < n) {
+          if (!(ok = wait_ab(&B->kv_full[st], ((j + 2) >> 1) & 1, C, p.status))) break;
           tc_fence_after();
-          issue_sd(st2);
+          issue_s(j + 2);
         }
       }
+      if (ok) mma_commit(&B->acc_done);
       mma_commit(&B->drain);
       mbar_wait(&B->drain, 0, p.status, OCTO_ETIMEOUT);
     }
-  } else {
-    // warps 3-10: warpgroup hh handles head h0 + hh; a warp reaches TMEM quadrant warp % 4
-    const int hh = (warp - 3) >> 2;
+  } else if (warp >= 4) {
+    // softmax warps: warpgroup c takes keys [64 c, 64 c + 64) of every step, i.e. the
+    // step's entry c; a warp reaches the TMEM lanes (rows) of its quadrant warp % 4
+    const int c = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const int h = h0 + hh;
     const bool row_ok = r < rows;
     const int64_t row = (int64_t)row0 + r;
     const float lse2 = row_ok ? p.lse[(int64_t)h * p.n_rows + row] * 1.4426950408889634f : 0.f;
     const float Dr = row_ok ? p.Dv[(int64_t)h * p.n_rows + row] : 0.f;
-    const uint32_t tS = tbase + lane_off + 256 + 128 * hh;
-    const uint32_t dsrow = sDS + hh * 16384;
+    const uint32_t tDP = tbase + lane_off + 256;
     bool ok = true;
-    octo_entry e_next = p.entries[e0];
+    octo_entry e_next{};
+    if (n > 0 && c < ne) e_next = p.entries[e0 + c];
     for (int32_t j = 0; j < n; j++) {
+      const bool has = 2 * j + c < ne;
       const octo_entry e = e_next;
-      if (j + 1 < n) e_next = p.entries[e0 + j + 1];   // prefetch
-      if (!(ok = warp_wait_ab(&B->s_full[hh], j & 1, C, p.status))) break;
-      tc_fence_after();
-      if (j > 0) {
-        if (!(ok = warp_wait_ab(&B->o_done[hh], (j - 1) & 1, C, p.status))) break;
+      if (2 * (j + 1) + c < ne) e_next = p.entries[e0 + 2 * (j + 1) + c];   // prefetch
+      // visible slots [lo, hi) of this row in this entry
+      int lo = 64, hi = 0;
+      if (has && row_ok && r >= (int)e.q_lo) {
+        lo = e.kv_lo;
+        hi = e.kv_hi;
+        if (e.flags & 1) hi = min(hi, r + e.diag + 1);
       }
-      p_ds_to_smem(tS, tS + 64, e, r, row_ok, lse2, Dr, p.scale_log2, 0u, dsrow + r * 128);
-      tc_fence_before();
-      mbar_arrive(&B->s_free[hh]);
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&B->p_full[hh]);
-    }
-    if (ok && n > 0 && warp_wait_ab(&B->o_done[hh], (n - 1) & 1, C, p.status)) {
+      const bool all_vis = __all_sync(0xffffffffu, lo == 0 && hi == 64);
+      const int b = j & 1;
+      if (!(ok = warp_wait_ab(&B->s_full[b], (j >> 1) & 1, C, p.status))) break;
       tc_fence_after();
-      float* out = p.dq + (row * p.Hq + h) * 128;
-#pragma unroll 1
-      for (int c = 0; c < 4; c++) {
-        uint32_t v[32];
-        tmem_ld32(tbase + lane_off + 128 * hh + c * 32, v);
-        tmem_wait_ld();
-        if (row_ok) {
+      uint32_t x0[32], x1[32];
+      tmem_ld32(tbase + lane_off + 128 * b + 64 * c, x0);
+      tmem_ld32(tbase + lane_off + 128 * b + 64 * c + 32, x1);
+      tmem_wait_ld();
+      float P[64];
+      auto p_phase = [&](auto masked) {
 #pragma unroll
-          for (int q4 = 0; q4 < 8; q4++)
-            st_global_v4(out + c * 32 + q4 * 4, __float_as_uint(__uint_as_float(v[4 * q4]) * p.scale),
-                         __float_as_uint(__uint_as_float(v[4 * q4 + 1]) * p.scale),
-                         __float_as_uint(__uint_as_float(v[4 * q4 + 2]) * p.scale),
-                         __float_as_uint(__uint_as_float(v[4 * q4 + 3]) * p.scale));
+        for (int i = 0; i < 64; i += 4) {
+          const uint32_t* xs = i < 32 ? x0 : x1;
+          const int ii = i & 31;
+          float a0, a1, a2, a3;
+          fma2(a0, a1, __uint_as_float(xs[ii]), __uint_as_float(xs[ii + 1]), p.scale_log2, -lse2);
+          fma2(a2, a3, __uint_as_float(xs[ii + 2]), __uint_as_float(xs[ii + 3]), p.scale_log2, -lse2);
+          // MUFU for 3 of every 4 pairs, the FMA-pipe polynomial for the 4th
+          if ((i & 7) == 4) {
+            a2 = ex2_poly(a2);
+            a3 = ex2_poly(a3);
+          } else {
+            a2 = ex2(a2);
+            a3 = ex2(a3);
+          }
+          a0 = ex2(a0);
+          a1 = ex2(a1);
+          if constexpr (decltype(masked)::value) {
+            a0 = (i >= lo && i < hi) ? a0 : 0.f;
+            a1 = (i + 1 >= lo && i + 1 < hi) ? a1 : 0.f;
+            a2 = (i + 2 >= lo && i + 2 < hi) ? a2 : 0.f;
+            a3 = (i + 3 >= lo && i + 3 < hi) ? a3 : 0.f;
+          }
+          P[i] = a0;
+          P[i + 1] = a1;
+          P[i + 2] = a2;
+          P[i + 3] = a3;
+        }
+      };
+      if (all_vis)
+        p_phase(std::false_type{});
+      else
+        p_phase(std::true_type{});
+      if (!(ok = warp_wait_ab(&B->dp_full, j & 1, C, p.status))) break;
+      tc_fence_after();
+      uint32_t pk[32];
+      auto ds_phase = [&](auto masked) {
+#pragma unroll
+        for (int half = 0; half < 2; half++) {
+          uint32_t x[32];
+          tmem_ld32(tDP + 64 * c + 32 * half, x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int q = 32 * half + i;
+            float d0, d1;
+            add2(d0, d1, __uint_as_float(x[i]), __uint_as_float(x[i + 1]), -Dr, -Dr);
+            mul2(d0, d1, d0, d1, P[q], P[q + 1]);
+            if constexpr (decltype(masked)::value) {
+              // masked entries: exactly zero even where dP is not finite
+              d0 = (q >= lo && q < hi) ? d0 : 0.f;
+              d1 = (q + 1 >= lo && q + 1 < hi) ? d1 : 0.f;
+            }
+            pk[q / 2] = pack_bf16(d0, d1);
+          }
+        }
+      };
+      if (all_vis)
+        ds_phase(std::false_type{});
+      else
+        ds_phase(std::true_type{});
+      if (c == 0) {
+        tc_fence_before();
+        mbar_arrive(&B->dp_read);
+      } else {
+        // dS of keys 64-127 lands on dP columns that warpgroup 0 reads
+        if (!(ok = warp_wait_ab(&B->dp_read, j & 1, C, p.status))) break;
+        tc_fence_after();
+      }
+      tmem_st32(tDP + 32 * c, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&B->ds_full);
+    }
+    // epilogue: warpgroup c writes d columns [64 c, 64 c + 64) of this row's dQ
+    if (n > 0) {
+      const bool fin = ok && warp_wait_ab(&B->acc_done, 0, C, p.status);
+      if (fin) {
+        tc_fence_after();
+        float* out = p.dq + (row * p.Hq + h) * 128 + 64 * c;
+#pragma unroll 1
+        for (int part = 0; part < 2; part++) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_off + 384 + 64 * c + 32 * part, v);
+          tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; q4++)
+              st_global_v4(out + 32 * part + 4 * q4, __float_as_uint(__uint_as_float(v[4 * q4]) * p.scale),
+                           __float_as_uint(__uint_as_float(v[4 * q4 + 1]) * p.scale),
+                           __float_as_uint(__uint_as_float(v[4 * q4 + 2]) * p.scale),
+                           __float_as_uint(__uint_as_float(v[4 * q4 + 3]) * p.scale));
+          }
         }
       }
     }
@@ -582,7 +769,7 @@ bool bwd_tc_supported(const octo_plan_s* p, int32_t Hq) {
   const octo_pool_desc& d = p->pool->desc;
   const int32_t G = Hq / d.n_kv_heads;
   return d.dtype == OCTO_DTYPE_BF16 && d.head_dim == 128 && d.page_size == 64 && p->info.bm == 128 &&
-         !p->info.is_decode && (G % 2) == 0 && p->tile_order && p->page_order;
+         !p->info.is_decode && (G % 2) == 0 && p->tile_order && (p->n_pairs == 0 || p->pair_order);
 }
 
 size_t bwd_tc_workspace(const octo_plan_s* p, int32_t Hq) {
@@ -630,6 +817,11 @@ int bwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const
   prm.csc_perm = p->csc_perm;
   prm.page_off = p->page_off;
   prm.page_order = p->page_order;
+  prm.pair_pages = p->pair_pages;
+  prm.pair_item_off = p->pair_item_off;
+  prm.pair_n_items = p->pair_n_items;
+  prm.pair_order = p->pair_order;
+  prm.pair_items = p->pair_items;
   prm.lse = lse;
   prm.Dv = Dv;
   prm.dq = dq;
@@ -654,12 +846,12 @@ int bwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const
     if (fa.maxThreadsPerBlock < kDqThreads) return OCTO_ENOTSUP;
     attr = true;
   }
-  const int64_t g1 = (int64_t)p->info.n_touched_pages * d.n_kv_heads;
+  const int64_t g1 = (int64_t)p->n_pairs * d.n_kv_heads;
   if (g1 > 0) {
     k_dkdv_tc<<<(unsigned)g1, kDkThreads, kDkSmem, s>>>(mq, mdo, mk, mv, prm);
     count_launch();
   }
-  const int64_t g2 = p->info.n_tiles * d.n_kv_heads * (prm.G / 2);
+  const int64_t g2 = p->info.n_tiles * Hq;
   k_dq_tc<<<(unsigned)g2, kDqThreads, kDqSmem, s>>>(mq, mdo, mk, mv, prm);
   count_launch();
   return cuda_status(cudaGetLastError());

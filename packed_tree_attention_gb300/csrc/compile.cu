@@ -404,6 +404,91 @@ __global__ void k_touched(const int32_t* __restrict__ page_off, int32_t num_page
   if (threadIdx.x == 0) *n_out = carry;
 }
 
+// One block per page pair (pa, pb): the pair's work items.  Every entry of pa's reader
+// list gives an item; when the next entry of the tile list is pb's, for the same query
+// tile, it joins that item as its second half.  pb's remaining entries follow as items
+// of their own, in list order (a block-wide compaction).  Items of one pair are thus in
+// a fixed order, and every entry of pa and pb is in exactly one of them.
+__device__ __forceinline__ void pair_half(PairItem& it, int h, const octo_entry* e) {
+  if (e) {
+    it.lo[h] = (int16_t)e->kv_lo;
+    it.hi[h] = (int16_t)e->kv_hi;
+    it.qlo[h] = (int16_t)e->q_lo;
+    it.cz[h] = (int16_t)(e->flags & 1);
+    it.diag[h] = e->diag;
+  } else {
+    it.lo[h] = it.hi[h] = it.qlo[h] = it.cz[h] = 0;
+    it.diag[h] = 0;
+  }
+}
+
+__global__ void k_pair_items(const int32_t* __restrict__ pair_pages, const int32_t* __restrict__ pair_off,
+                             const int32_t* __restrict__ page_off, const int32_t* __restrict__ csc,
+                             const octo_entry* __restrict__ entries, int32_t n_entries,
+                             const int32_t* __restrict__ tile_row0, const int32_t* __restrict__ tile_rows,
+                             PairItem* __restrict__ items, int32_t* __restrict__ pair_n) {
+  __shared__ int32_t warp_s[32];
+  __shared__ int32_t carry;
+  const int32_t b = blockIdx.x;
+  const int32_t pa = pair_pages[2 * b], pb = pair_pages[2 * b + 1];
+  const int32_t base = pair_off[b];
+  const int32_t oa = page_off[pa], la = page_off[pa + 1] - oa;
+  for (int32_t i = threadIdx.x; i < la; i += blockDim.x) {
+    const int32_t e = csc[oa + i];
+    const octo_entry E = entries[e];
+    PairItem it;
+    it.row0 = tile_row0[E.q_tile];
+    it.rows = tile_rows[E.q_tile];
+    pair_half(it, 0, &E);
+    bool joined = false;
+    if (pb >= 0 && e + 1 < n_entries) {
+      const octo_entry F = entries[e + 1];
+      if ((int32_t)F.kv_page == pb && F.q_tile == E.q_tile) {
+        pair_half(it, 1, &F);
+        joined = true;
+      }
+    }
+    if (!joined) pair_half(it, 1, nullptr);
+    items[base + i] = it;
+  }
+  int32_t n = la;
+  if (pb >= 0) {
+    const int32_t ob = page_off[pb], lb = page_off[pb + 1] - ob;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int32_t s0 = 0; s0 < lb; s0 += blockDim.x) {
+      const int32_t i = s0 + threadIdx.x;
+      int32_t e = -1;
+      bool keep = false;
+      if (i < lb) {
+        e = csc[ob + i];
+        keep = !(e >= 1 && (int32_t)entries[e - 1].kv_page == pa && entries[e - 1].q_tile == entries[e].q_tile);
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+      if (lane == 0) warp_s[wid] = __popc(bal);
+      __syncthreads();
+      int32_t before = carry;
+      for (int w2 = 0; w2 < wid; w2++) before += warp_s[w2];
+      if (keep) {
+        const octo_entry F = entries[e];
+        PairItem it;
+        it.row0 = tile_row0[F.q_tile];
+        it.rows = tile_rows[F.q_tile];
+        pair_half(it, 0, nullptr);
+        pair_half(it, 1, &F);
+        items[base + la + before + __popc(bal & ((1u << lane) - 1))] = it;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0)
+        for (int w2 = 0; w2 < nw; w2++) carry += warp_s[w2];
+      __syncthreads();
+    }
+    n = la + carry;
+  }
+  if (threadIdx.x == 0) pair_n[b] = n;
+}
+
 template <typename T>
 int dalloc(octo_plan_s* pl, T** ptr, size_t n, cudaStream_t s) {
   void* p = nullptr;
@@ -611,6 +696,57 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
       if (poff[pg + 1] > poff[pg]) pord.push_back(pg);
     std::stable_sort(pord.begin(), pord.end(),
                      [&](int32_t a, int32_t b) { return poff[a + 1] - poff[a] > poff[b + 1] - poff[b]; });
+    // dK/dV work units: consecutive own pages of each segment, two at a time, among the
+    // touched pages; a touched page without a touched partner runs alone
+    if (!is_decode && !pord.empty()) {
+      std::vector<int32_t> pp, pub;
+      std::vector<char> seen((size_t)pl->num_pages, 0);
+      auto cnt = [&](int32_t pg) { return pg < 0 ? 0 : poff[pg + 1] - poff[pg]; };
+      for (const Segment& g : pool->segs) {
+        if (g.freed) continue;
+        int32_t pend = -1;
+        for (int32_t pg : g.pages) {
+          if (pg < 0 || pg >= pl->num_pages || cnt(pg) == 0 || seen[pg]) {
+            if (pend >= 0) { pp.push_back(pend); pp.push_back(-1); pend = -1; }
+            continue;
+          }
+          seen[pg] = 1;
+          if (pend < 0) {
+            pend = pg;
+          } else {
+            pp.push_back(pend);
+            pp.push_back(pg);
+            pend = -1;
+          }
+        }
+        if (pend >= 0) { pp.push_back(pend); pp.push_back(-1); }
+      }
+      for (int32_t pg = 0; pg < pl->num_pages; pg++)
+        if (cnt(pg) > 0 && !seen[pg]) { pp.push_back(pg); pp.push_back(-1); }
+      const int32_t np = (int32_t)(pp.size() / 2);
+      std::vector<int32_t> poff2(np + 1, 0), pord2(np);
+      for (int32_t i = 0; i < np; i++) {
+        poff2[i + 1] = poff2[i] + cnt(pp[2 * i]) + cnt(pp[2 * i + 1]);
+        pord2[i] = i;
+      }
+      std::stable_sort(pord2.begin(), pord2.end(), [&](int32_t a, int32_t b) {
+        return poff2[a + 1] - poff2[a] > poff2[b + 1] - poff2[b];
+      });
+      pl->n_pairs = np;
+      OCTO_TRY(dalloc(pl, &pl->pair_pages, pp.size(), s));
+      OCTO_TRY(dalloc(pl, &pl->pair_item_off, poff2.size(), s));
+      OCTO_TRY(dalloc(pl, &pl->pair_n_items, np, s));
+      OCTO_TRY(dalloc(pl, &pl->pair_order, np, s));
+      OCTO_TRY(dalloc(pl, &pl->pair_items, (size_t)n_entries, s));
+      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->pair_pages, pp.data(), pp.size() * 4, cudaMemcpyHostToDevice, s)));
+      OCTO_TRY(cuda_status(
+          cudaMemcpyAsync(pl->pair_item_off, poff2.data(), poff2.size() * 4, cudaMemcpyHostToDevice, s)));
+      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->pair_order, pord2.data(), np * 4, cudaMemcpyHostToDevice, s)));
+      k_pair_items<<<np, 256, 0, s>>>(pl->pair_pages, pl->pair_item_off, pl->page_off, pl->csc_perm, pl->entries,
+                                      n_entries, pl->tile_row0, pl->tile_rows, pl->pair_items, pl->pair_n_items);
+      count_launch();
+      OCTO_TRY(cuda_status(cudaGetLastError()));
+    }
     OCTO_TRY(dalloc(pl, &pl->tile_order, n_tiles, s));
     OCTO_TRY(dalloc(pl, &pl->page_order, pord.size(), s));
     if (n_tiles > 0)

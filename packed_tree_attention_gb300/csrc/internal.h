@@ -43,6 +43,16 @@ struct DevMount {
   int32_t m, created, producer, a, b, id, jump, pad;
 };
 
+// One work item of the dK/dV kernel: a query tile against a pair of pages (keys 0-63 from
+// the first page, 64-127 from the second), with each half's visibility rectangle copied
+// from its tile-list entry (lo = hi = 0: no entry for that half).  32 bytes.
+struct PairItem {
+  int32_t row0, rows;     // first packed row of the query tile, rows in it
+  int16_t lo[2], hi[2];   // visible slots [lo, hi) of each page
+  int16_t qlo[2], cz[2];  // first visible tile row; causal flag
+  int32_t diag[2];        // causal: row r sees slot j iff j <= r + diag
+};
+
 }  // namespace octo
 
 struct octo_pool_s {
@@ -73,6 +83,13 @@ struct octo_plan_s {
   int32_t* touched = nullptr;        // [n_touched_pages] pages with >= 1 entry, ascending
   int32_t* tile_order = nullptr;     // [n_tiles] tiles by descending entry count (scheduling)
   int32_t* page_order = nullptr;     // [n_touched] touched pages by descending entry count
+  // dK/dV work units: pairs of consecutive own pages of a segment (second -1: one page)
+  int32_t n_pairs = 0;
+  int32_t* pair_pages = nullptr;     // [2 n_pairs]
+  int32_t* pair_item_off = nullptr;  // [n_pairs+1] item slice of each pair (upper bound)
+  int32_t* pair_n_items = nullptr;   // [n_pairs] items actually written
+  int32_t* pair_order = nullptr;     // [n_pairs] launch order, heaviest first
+  octo::PairItem* pair_items = nullptr;  // [n_entries]
   // decode plans: runs of up to kSplitEntries entries of one cursor (split-KV)
   int32_t n_splits = 0;
   int32_t* split_tile = nullptr;     // [n_splits] cursor (tile) of the split
