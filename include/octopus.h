@@ -267,7 +267,8 @@ int octo_last_cuda_error(void);   /* last cudaError_t seen by the library */
  * (OCTO_ETIMEOUT if a bounded wait expired) and clears it. */
 int octo_sync(octo_plan_t plan, void* stream);
 /* Which kernel family octo_attn_fwd / bwd / decode will use for this plan:
- * 0 = CUDA-core (SIMT) kernels, 1 = tcgen05 tensor-core kernels.  which: 0 fwd, 1 bwd,
+ * 0 = CUDA-core (SIMT) kernels, 1 = tcgen05 tensor-core kernels (the backward takes them
+ * only with a nonzero scale), 2 = split-KV decode kernels.  which: 0 fwd, 1 bwd,
  * 2 decode. */
 int octo_kernel_path(octo_plan_t plan, int32_t n_q_heads, int32_t which);
 /* Number of kernels the library has enqueued in this process so far (all pools, all

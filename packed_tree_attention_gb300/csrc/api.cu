@@ -1,6 +1,8 @@
 // Attention entry points: argument checks and dispatch between the tensor-core kernels
 // (bf16, head_dim 128, page 64, q-tile 128) and the CUDA-core kernels (everything else).
 
+#include <algorithm>
+#include <cmath>
 #include <cstdlib>
 
 #include "internal.h"
@@ -13,6 +15,7 @@ int bwd_simt(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, con
              cudaStream_t s);
 bool fwd_tc_supported(const octo_plan_s* p, int32_t Hq);
 bool bwd_tc_supported(const octo_plan_s* p, int32_t Hq);
+size_t bwd_tc_workspace(const octo_plan_s* p, int32_t Hq);
 bool decode_split_supported(const octo_plan_s* p, int32_t Hq);
 size_t decode_split_workspace(const octo_plan_s* p, int32_t Hq);
 int decode_split(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const void* v, void* out, float* lse,
@@ -73,7 +76,9 @@ int octo_attn_fwd(octo_plan_t plan, int32_t Hq, const void* q, const void* k_poo
 
 size_t octo_attn_bwd_workspace_size(octo_plan_t plan, int32_t Hq) {
   if (!plan || Hq <= 0) return 0;
-  return octo::align_up((size_t)plan->info.n_rows * Hq * sizeof(float), 256);
+  const size_t simt = octo::align_up((size_t)plan->info.n_rows * Hq * sizeof(float), 256);
+  if (plan->info.is_decode || check_heads(plan, Hq) != OCTO_OK || !octo::bwd_tc_supported(plan, Hq)) return simt;
+  return std::max(simt, octo::bwd_tc_workspace(plan, Hq));
 }
 
 int octo_attn_bwd(octo_plan_t plan, int32_t Hq, const void* q, const void* k_pool, const void* v_pool, const void* o,
@@ -89,7 +94,8 @@ int octo_attn_bwd(octo_plan_t plan, int32_t Hq, const void* q, const void* k_poo
   const void* v = v_pool ? v_pool : plan->pool->desc.v_pool;
   if (plan->info.n_entries > 0 && (!k || !v)) return OCTO_EINVAL;
   plan->last_stream = (cudaStream_t)stream;
-  if (!tc_disabled() && octo::bwd_tc_supported(plan, Hq))
+  // the tensor-core backward folds LSE / scale into its MMAs: it needs a finite 1 / scale
+  if (!tc_disabled() && octo::bwd_tc_supported(plan, Hq) && scale != 0.f && std::isfinite(1.f / scale))
     return octo::bwd_tc(plan, Hq, q, k, v, o, lse, dout, dq, dk_pool, dv_pool, scale, ws, (cudaStream_t)stream);
   return octo::bwd_simt(plan, Hq, q, k, v, o, lse, dout, dq, dk_pool, dv_pool, scale, ws, (cudaStream_t)stream);
 }

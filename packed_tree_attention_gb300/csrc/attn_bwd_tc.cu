@@ -57,8 +57,9 @@ struct BwdParams {
   const int32_t* pair_n_items;
   const int32_t* pair_order;
   const PairItem* pair_items;
-  const float* lse;
-  const float* Dv;
+  const float* lse2t;   // [n_tiles][Hq][128] LSE * log2(e) per tile row (0 past the tile)
+  const float* Dt;      // [n_tiles][Hq][128] D = rowsum(dO * O) per tile row
+  const uint4* aug;     // [n_tiles][Hq][128 rows] bf16 (-LSE/scale hi, lo, -D hi, lo, 0 x 4)
   float* dq;
   float* dk;
   float* dv;
@@ -87,18 +88,76 @@ __device__ __forceinline__ bool warp_wait_ab(uint64_t* bar, uint32_t parity, Ctl
   return __all_sync(0xffffffffu, wait_ab(bar, parity, C, status));
 }
 
+// Row statistics in a tile-padded layout, one CTA per (tile, head): the log2-domain LSE and
+// D = rowsum(dO * O) of each tile row at [tile][head][0, 128), zero past the tile, read by
+// the dQ softmax; and for the dK/dV MMAs a [128 rows x 8] bf16 block per (tile, head)
+// holding -LSE/scale and -D, each as a bf16 pair hi + lo (about 16 significant bits):
+// multiplied by a block of ones in one extra K = 16 MMA step, it subtracts them from S^T
+// and dP^T inside the accumulator.
+__global__ void __launch_bounds__(128) k_pre_tiles(const __nv_bfloat16* __restrict__ o,
+                                                   const __nv_bfloat16* __restrict__ dout,
+                                                   const float* __restrict__ lse, const int32_t* __restrict__ tile_row0,
+                                                   const int32_t* __restrict__ tile_rows, int64_t n_rows, int32_t Hq,
+                                                   float inv_scale, float* __restrict__ lse2t, float* __restrict__ Dt,
+                                                   uint4* __restrict__ aug) {
+  const int32_t tile = blockIdx.x / Hq, h = blockIdx.x % Hq;
+  const int32_t row0 = tile_row0[tile], rows = tile_rows[tile];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* lo = lse2t + (size_t)blockIdx.x * 128;
+  float* dd = Dt + (size_t)blockIdx.x * 128;
+  uint4* ag = aug + (size_t)blockIdx.x * 128;
+  for (int r = warp; r < 128; r += 4) {
+    float part = 0.f;
+    if (r < rows) {
+      const size_t base = ((size_t)(row0 + r) * Hq + h) * 128 + lane * 4;
+      const uint2 a = *reinterpret_cast<const uint2*>(o + base);
+      const uint2 b = *reinterpret_cast<const uint2*>(dout + base);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int i = 0; i < 2; i++) {
+        const float2 x = __bfloat1622float2(a2[i]), y = __bfloat1622float2(b2[i]);
+        part = fmaf(x.x, y.x, part);
+        part = fmaf(x.y, y.y, part);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    if (lane == 0) {
+      const float L = r < rows ? lse[(int64_t)h * n_rows + row0 + r] : 0.f;
+      dd[r] = part;
+      lo[r] = L * 1.4426950408889634f;
+      const float av = -L * inv_scale, bv = -part;
+      const __nv_bfloat16 ah = __float2bfloat16_rn(av), bh = __float2bfloat16_rn(bv);
+      const __nv_bfloat16 al = __float2bfloat16_rn(av - __bfloat162float(ah));
+      const __nv_bfloat16 bl = __float2bfloat16_rn(bv - __bfloat162float(bh));
+      uint4 v;
+      v.x = (uint32_t)__bfloat16_as_ushort(ah) | ((uint32_t)__bfloat16_as_ushort(al) << 16);
+      v.y = (uint32_t)__bfloat16_as_ushort(bh) | ((uint32_t)__bfloat16_as_ushort(bl) << 16);
+      v.z = 0;
+      v.w = 0;
+      ag[r] = v;
+    }
+  }
+}
+
 // =====================================================================================
 // dK / dV
 // =====================================================================================
-constexpr int kDkThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, warp 2 row statistics, warps 4-11 softmax
-// smem: K pair 32KB | V pair 32KB | 2 stages x (Q 32KB + dO 32KB) | 2 stages x row statistics
-constexpr uint32_t kDkOffK = 0;
-constexpr uint32_t kDkOffV = 32768;
-constexpr uint32_t kDkOffQD = 65536;
+constexpr int kDkThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, warps 4-11 softmax
+// smem: ones blocks 2 x 4KB | 2 stages x row-statistics block 4KB | K pair 32KB | V pair 32KB |
+// 2 stages x (Q 32KB + dO 32KB).  The softmax warps read no memory per element: LSE and D
+// enter through one more K = 16 MMA step (ones x statistics block) of S^T and dP^T.
+// The 4KB blocks are K-major without swizzle: 128 rows x 8 bf16 (16 B per row; K = 0..7),
+// then 2KB of zeros for K = 8..15.
+constexpr uint32_t kDkOffOnesS = 0;      // rows: 1, 1, 0 ...  (picks -LSE/scale hi + lo)
+constexpr uint32_t kDkOffOnesD = 4096;   // rows: 0, 0, 1, 1, 0 ...  (picks -D hi + lo)
+constexpr uint32_t kDkOffAug = 8192;     // per stage: the (tile, head) statistics block
+constexpr uint32_t kDkOffK = 16384;
+constexpr uint32_t kDkOffV = kDkOffK + 32768;
+constexpr uint32_t kDkOffQD = kDkOffV + 32768;
 constexpr uint32_t kDkStageQD = 65536;
-constexpr uint32_t kDkOffSt = kDkOffQD + 2 * kDkStageQD;
-constexpr uint32_t kDkStageSt = 1152;   // log2-domain LSE [128], D [128], the PairItem
-constexpr uint32_t kDkOffBar = kDkOffSt + 2 * kDkStageSt;
+constexpr uint32_t kDkOffBar = kDkOffQD + 2 * kDkStageQD;
 constexpr uint32_t kDkSmem = kDkOffBar + 256 + 1024;
 constexpr uint32_t kIdKR = idesc_bf16(128, 128, 0, 0);   // keys x rows, both K-major
 constexpr uint32_t kIdKD = idesc_bf16(128, 128, 0, 1);   // keys x d, A from TMEM, B MN-major
@@ -107,8 +166,6 @@ struct DkBars {
   uint64_t kv_full;
   uint64_t qd_full[2];
   uint64_t qd_free[2];
-  uint64_t st_full[2];
-  uint64_t st_free[2];
   uint64_t s_full, dp_full;   // S^T / dP^T of the current step in TMEM
   uint64_t s_read, dp_read;   // softmax warpgroup 0 has read its S^T / dP^T columns
   uint64_t p_full, ds_full;   // P^T / dS^T written back to TMEM
@@ -140,8 +197,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     for (int s = 0; s < 2; s++) {
       mbar_init(&B->qd_full[s], 1);
       mbar_init(&B->qd_free[s], 1);
-      mbar_init(&B->st_full[s], 32);
-      mbar_init(&B->st_free[s], 256);
     }
     mbar_init(&B->s_full, 1);
     mbar_init(&B->dp_full, 1);
@@ -157,6 +212,20 @@ __global__ void __launch_bounds__(kDkThreads, 1)
   if (warp == 1) {
     tmem_alloc(&C->tmem_base, 512);
     tmem_relinquish();
+  }
+  {
+    // ones blocks (rows 0-127, then the zero K = 8..15 half) and the zero halves of the
+    // statistics stages; 16 KB, 1024 x 16 B
+    const uint32_t one2 = 0x3F803F80u;   // two bf16 ones
+    for (int i = threadIdx.x; i < 1024; i += kDkThreads) {
+      const int blk = i >> 8, row = i & 255;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (row < 128 && blk == 0) v.x = one2;
+      if (row < 128 && blk == 1) v.y = one2;
+      if (row < 128 && blk >= 2) continue;   // statistics rows: written by the TMA
+      reinterpret_cast<uint4*>(smem + blk * 4096)[row] = v;
+    }
+    fence_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -182,15 +251,19 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         tma_load_2d(smem + kDkOffV + 16384 + hp * 8192, &tmV, &B->kv_full, 64, krow);
       }
       int32_t issued = 0;
-      int32_t row0_next = items[0].row0;
+      int32_t row0_next = items[0].row0, tile_next = items[0].tile;
       for (int32_t w = 0; w < n; w++) {
         const int st = w & 1;
         const int32_t h = g * G + (w % G);
-        const int32_t row0 = row0_next;
-        if (w + 1 < n) row0_next = (w + 1) % G ? row0 : items[(w + 1) / G].row0;
+        const int32_t row0 = row0_next, tile_n = tile_next;
+        if (w + 1 < n && (w + 1) % G == 0) {
+          row0_next = items[(w + 1) / G].row0;
+          tile_next = items[(w + 1) / G].tile;
+        }
         if (w >= 2 && !wait_ab(&B->qd_free[st], ((w >> 1) - 1) & 1, C, p.status)) break;
         uint8_t* dst = smem + kDkOffQD + st * kDkStageQD;
-        mbar_expect_tx(&B->qd_full[st], 65536);
+        mbar_expect_tx(&B->qd_full[st], 65536 + 2048);
+        bulk_load(smem + kDkOffAug + st * 4096, p.aug + ((size_t)tile_n * p.Hq + h) * 128, 2048, &B->qd_full[st]);
         tma_load_3d(dst, &tmQ, &B->qd_full[st], 0, h, row0);
         tma_load_3d(dst + 16384, &tmQ, &B->qd_full[st], 64, h, row0);
         tma_load_3d(dst + 32768, &tmDO, &B->qd_full[st], 0, h, row0);
@@ -207,6 +280,10 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       const uint64_t bQ0 = desc_sw128(sQD, 16, 1024), bDO0 = desc_sw128(sQD + 32768, 16, 1024);
       const uint64_t bQm0 = desc_sw128(sQD, 16384, 1024), bDOm0 = desc_sw128(sQD + 32768, 16384, 1024);
       const uint32_t tS = tbase, tDP = tbase + 128, tDV = tbase + 256, tDK = tbase + 384;
+      const uint64_t aOnesS = desc_noswz(smem_u32(smem + kDkOffOnesS), 2048, 128);
+      const uint64_t aOnesD = desc_noswz(smem_u32(smem + kDkOffOnesD), 2048, 128);
+      const uint64_t bAug0 = desc_noswz(smem_u32(smem + kDkOffAug), 2048, 128);
+      // S'^T = K Q^T - LSE/scale  and  dP'^T = V dO^T - D
       auto issue_s = [&](int st) {
         const uint64_t so = (uint64_t)(st * (kDkStageQD >> 4));
 #pragma unroll
@@ -214,6 +291,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
           mma_f16_ss(tS, aK + o, bQ0 + so + o, kIdKR, kk > 0);
         }
+        mma_f16_ss(tS, aOnesS, bAug0 + (uint64_t)(st * (4096 >> 4)), kIdKR, 1);
         mma_commit(&B->s_full);
       };
       auto issue_dp = [&](int st) {
@@ -223,6 +301,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
           mma_f16_ss(tDP, aV + o, bDO0 + so + o, kIdKR, kk > 0);
         }
+        mma_f16_ss(tDP, aOnesD, bAug0 + (uint64_t)(st * (4096 >> 4)), kIdKR, 1);
         mma_commit(&B->dp_full);
       };
       bool ok = wait_ab(&B->kv_full, 0, C, p.status) && wait_ab(&B->qd_full[0], 0, C, p.status);
@@ -259,36 +338,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       mma_commit(&B->drain);
       mbar_wait(&B->drain, 0, p.status, OCTO_ETIMEOUT);
     }
-  } else if (warp == 2) {
-    // row statistics of each step's (query tile, head), and the item, into the stage ring
-    if (n > 0) {
-      PairItem it = items[0];
-      PairItem it_next = it;
-      if (n_items > 1) it_next = items[1];
-      for (int32_t w = 0; w < n; w++) {
-        const int st = w & 1;
-        if (w > 0 && w % G == 0) {
-          it = it_next;
-          if (w / G + 1 < n_items) it_next = items[w / G + 1];
-        }
-        const int32_t h = g * G + (w % G);
-        const int r0 = lane * 4;
-        float l[4], d[4];
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-          const int r = r0 + q;
-          const int64_t idx = (int64_t)h * p.n_rows + it.row0 + r;
-          l[q] = r < it.rows ? p.lse[idx] * 1.4426950408889634f : 0.f;
-          d[q] = r < it.rows ? p.Dv[idx] : 0.f;
-        }
-        if (w >= 2 && !warp_wait_ab(&B->st_free[st], ((w >> 1) - 1) & 1, C, p.status)) break;
-        float* S = reinterpret_cast<float*>(smem + kDkOffSt + st * kDkStageSt);
-        *reinterpret_cast<float4*>(S + r0) = make_float4(l[0], l[1], l[2], l[3]);
-        *reinterpret_cast<float4*>(S + 128 + r0) = make_float4(d[0], d[1], d[2], d[3]);
-        if (lane == 0) *reinterpret_cast<PairItem*>(S + 256) = it;
-        mbar_arrive(&B->st_full[st]);
-      }
-    }
   } else if (warp >= 4) {
     // softmax warps: warpgroup c takes query rows [64 c, 64 c + 64) of every step; a warp
     // reaches the TMEM lanes (keys) of its quadrant warp % 4
@@ -299,18 +348,19 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tbase + lane_off, tDP = tS + 128;
     bool ok = true;
+    PairItem it{}, it_n{};
+    if (n > 0) it_n = items[0];
     for (int32_t w = 0; ok && w < n; w++) {
-      const int st = w & 1;
-      if (!(ok = warp_wait_ab(&B->st_full[st], (w >> 1) & 1, C, p.status))) break;
-      const float* S = reinterpret_cast<const float*>(smem + kDkOffSt + st * kDkStageSt);
-      const PairItem* it = reinterpret_cast<const PairItem*>(S + 256);
+      if (w % G == 0) {
+        it = it_n;
+        if (w / G + 1 < n_items) it_n = items[w / G + 1];   // prefetch
+      }
       // visible rows of this key: rmin <= r < rmax
-      const int lo = it->lo[hk], hi = it->hi[hk];
-      int rmin = it->qlo[hk];
-      if (it->cz[hk]) rmin = max(rmin, j - it->diag[hk]);
-      const int rmax = (j >= lo && j < hi) ? it->rows : 0;
-      const float* L = S + 64 * c;
-      const float* Dr = S + 128 + 64 * c;
+      // (selects, not indexing by hk: a dynamic index would put the item in local memory)
+      const int lo = hk ? it.lo[1] : it.lo[0], hi = hk ? it.hi[1] : it.hi[0];
+      int rmin = hk ? it.qlo[1] : it.qlo[0];
+      if ((it.causal >> hk) & 1) rmin = max(rmin, j - (hk ? it.diag[1] : it.diag[0]));
+      const int rmax = (j >= lo && j < hi) ? it.rows : 0;
       if (!(ok = warp_wait_ab(&B->s_full, w & 1, C, p.status))) break;
       tc_fence_after();
       uint32_t x0[32], x1[32];
@@ -327,12 +377,12 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       auto p_phase = [&](auto masked) {
 #pragma unroll
         for (int i = 0; i < 64; i += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(L + i);
           const uint32_t* xs = i < 32 ? x0 : x1;
           const int ii = i & 31;
           float a0, a1, a2, a3;
-          fma2v(a0, a1, __uint_as_float(xs[ii]), __uint_as_float(xs[ii + 1]), p.scale_log2, -l4.x, -l4.y);
-          fma2v(a2, a3, __uint_as_float(xs[ii + 2]), __uint_as_float(xs[ii + 3]), p.scale_log2, -l4.z, -l4.w);
+          // S'^T already holds S - LSE / scale
+          mul2(a0, a1, __uint_as_float(xs[ii]), __uint_as_float(xs[ii + 1]), p.scale_log2, p.scale_log2);
+          mul2(a2, a3, __uint_as_float(xs[ii + 2]), __uint_as_float(xs[ii + 3]), p.scale_log2, p.scale_log2);
           // MUFU for 3 of every 4 pairs, the FMA-pipe polynomial for the 4th
           if ((i & 7) == 4) {
             a2 = ex2_poly(a2);
@@ -382,13 +432,11 @@ __global__ void __launch_bounds__(kDkThreads, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(Dr + 32 * half + i);
             const int q = 32 * half + i;
             float d0, d1, d2, d3;
-            add2(d0, d1, __uint_as_float(x[i]), __uint_as_float(x[i + 1]), -d4.x, -d4.y);
-            add2(d2, d3, __uint_as_float(x[i + 2]), __uint_as_float(x[i + 3]), -d4.z, -d4.w);
-            mul2(d0, d1, d0, d1, P[q], P[q + 1]);
-            mul2(d2, d3, d2, d3, P[q + 2], P[q + 3]);
+            // dP'^T already holds dP - D
+            mul2(d0, d1, __uint_as_float(x[i]), __uint_as_float(x[i + 1]), P[q], P[q + 1]);
+            mul2(d2, d3, __uint_as_float(x[i + 2]), __uint_as_float(x[i + 3]), P[q + 2], P[q + 3]);
             if constexpr (decltype(masked)::value) {
               // masked entries: exactly zero even where dP is not finite
               const int r = 64 * c + q;
@@ -417,7 +465,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&B->ds_full);
-      mbar_arrive(&B->st_free[st]);
     }
     // epilogue: warpgroup c writes d columns [64 c, 64 c + 64) of this key's dV and dK rows
     if (n > 0) {
@@ -456,20 +503,21 @@ __global__ void __launch_bounds__(kDkThreads, 1)
 // dQ
 // =====================================================================================
 constexpr int kDqThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, warps 4-11 softmax
-constexpr int kDqNS = 2;
-// smem: Q 32KB | dO 32KB | 2 stages x (K pair 32KB + V pair 32KB)
+constexpr int kDqNK = 3;          // K pairs in flight: step j's K lands while step j - 1 runs
+constexpr int kDqNV = 2;
+// smem: Q 32KB | dO 32KB | 3 stages x K pair 32KB | 2 stages x V pair 32KB
 constexpr uint32_t kDqOffQ = 0;
 constexpr uint32_t kDqOffDO = 32768;
-constexpr uint32_t kDqOffKV = 65536;
-constexpr uint32_t kDqStageKV = 65536;
-constexpr uint32_t kDqOffBar = kDqOffKV + kDqNS * kDqStageKV;
+constexpr uint32_t kDqOffK = 65536;
+constexpr uint32_t kDqOffV = kDqOffK + kDqNK * 32768;
+constexpr uint32_t kDqOffBar = kDqOffV + kDqNV * 32768;
 constexpr uint32_t kDqSmem = kDqOffBar + 256 + 1024;
 constexpr uint32_t kIdRP = idesc_bf16(128, 128, 0, 0);   // rows x keys of an entry pair, both K-major
 
 struct DqBars {
   uint64_t q_full;
-  uint64_t kv_full[kDqNS];
-  uint64_t kv_empty[kDqNS];
+  uint64_t k_full[kDqNK], k_empty[kDqNK];
+  uint64_t v_full[kDqNV], v_empty[kDqNV];
   uint64_t s_full[2];
   uint64_t dp_full;
   uint64_t dp_read;   // softmax warpgroup 0 has read its dP columns
@@ -483,6 +531,8 @@ struct DqBars {
 // a time: keys 0-63 of a step from the first entry, 64-127 from the second (an odd last
 // entry runs alone; its dQ MMAs stop at key 64).  TMEM: S of step j in [128 (j % 2), +128),
 // dP [256, 384) with dS as bf16 over its first 64 columns, dQ [384, 512); lane = row.
+// MMA order per step j: dQ(j), dP(j + 1), S(j + 2); K and V have rings of their own, as V
+// is free once dP has run while K is read again by dQ.
 __global__ void __launch_bounds__(kDqThreads, 1)
     k_dq_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
             const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, BwdParams p) {
@@ -502,9 +552,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&B->q_full, 1);
-    for (int s = 0; s < kDqNS; s++) {
-      mbar_init(&B->kv_full[s], 1);
-      mbar_init(&B->kv_empty[s], 1);
+    for (int s = 0; s < kDqNK; s++) {
+      mbar_init(&B->k_full[s], 1);
+      mbar_init(&B->k_empty[s], 1);
+    }
+    for (int s = 0; s < kDqNV; s++) {
+      mbar_init(&B->v_full[s], 1);
+      mbar_init(&B->v_empty[s], 1);
     }
     mbar_init(&B->s_full[0], 1);
     mbar_init(&B->s_full[1], 1);
@@ -526,7 +580,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const uint32_t tbase = C->tmem_base;
   const uint32_t sQ = smem_u32(smem + kDqOffQ);
   const uint32_t sDO = smem_u32(smem + kDqOffDO);
-  const uint32_t sKV = smem_u32(smem + kDqOffKV);
+  const uint32_t sK = smem_u32(smem + kDqOffK);
+  const uint32_t sV = smem_u32(smem + kDqOffV);
 
   if (warp == 0) {
     if (lane == 0 && n > 0) {
@@ -541,66 +596,81 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       int32_t issued = 0;
       for (int32_t j = 0; j < n; j++) {
-        const int st = j & 1;
+        const int sk = j % kDqNK, sv = j % kDqNV;
         const int32_t ea = e0 + 2 * j;
         const int32_t pa = (int32_t)p.entries[ea].kv_page;
         const int32_t pb = 2 * j + 1 < ne ? (int32_t)p.entries[ea + 1].kv_page : -1;
-        if (j >= kDqNS && !wait_ab(&B->kv_empty[st], ((j >> 1) - 1) & 1, C, p.status)) break;
-        uint8_t* kd = smem + kDqOffKV + st * kDqStageKV;
-        mbar_expect_tx(&B->kv_full[st], pb >= 0 ? 65536 : 32768);
+        const uint32_t bytes = pb >= 0 ? 32768 : 16384;
+        if (j >= kDqNK && !wait_ab(&B->k_empty[sk], ((j / kDqNK) - 1) & 1, C, p.status)) break;
+        uint8_t* kd = smem + kDqOffK + sk * 32768;
+        mbar_expect_tx(&B->k_full[sk], bytes);
         for (int hp = 0; hp < 2; hp++) {
           const int32_t pg = hp ? pb : pa;
           if (pg < 0) continue;
           const int32_t krow = (pg * p.Hkv + g) * 64;
-          tma_load_2d(kd + hp * 8192, &tmK, &B->kv_full[st], 0, krow);
-          tma_load_2d(kd + 16384 + hp * 8192, &tmK, &B->kv_full[st], 64, krow);
-          tma_load_2d(kd + 32768 + hp * 8192, &tmV, &B->kv_full[st], 0, krow);
-          tma_load_2d(kd + 49152 + hp * 8192, &tmV, &B->kv_full[st], 64, krow);
+          tma_load_2d(kd + hp * 8192, &tmK, &B->k_full[sk], 0, krow);
+          tma_load_2d(kd + 16384 + hp * 8192, &tmK, &B->k_full[sk], 64, krow);
+        }
+        if (j >= kDqNV && !wait_ab(&B->v_empty[sv], ((j / kDqNV) - 1) & 1, C, p.status)) break;
+        uint8_t* vd = smem + kDqOffV + sv * 32768;
+        mbar_expect_tx(&B->v_full[sv], bytes);
+        for (int hp = 0; hp < 2; hp++) {
+          const int32_t pg = hp ? pb : pa;
+          if (pg < 0) continue;
+          const int32_t krow = (pg * p.Hkv + g) * 64;
+          tma_load_2d(vd + hp * 8192, &tmV, &B->v_full[sv], 0, krow);
+          tma_load_2d(vd + 16384 + hp * 8192, &tmV, &B->v_full[sv], 64, krow);
         }
         issued = j + 1;
       }
       mbar_wait(&B->q_full, 0, p.status, OCTO_ETIMEOUT);
-      for (int32_t j = max(0, issued - kDqNS); j < issued; j++)
-        mbar_wait(&B->kv_full[j & 1], (j >> 1) & 1, p.status, OCTO_ETIMEOUT);
+      // copies still in flight land before the CTA can exit
+      for (int32_t j = max(0, issued - kDqNK); j < issued; j++)
+        mbar_wait(&B->k_full[j % kDqNK], (j / kDqNK) & 1, p.status, OCTO_ETIMEOUT);
+      for (int32_t j = max(0, issued - kDqNV); j < issued; j++)
+        mbar_wait(&B->v_full[j % kDqNV], (j / kDqNV) & 1, p.status, OCTO_ETIMEOUT);
     }
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
       const uint64_t aQ = desc_sw128(sQ, 16, 1024), aDO = desc_sw128(sDO, 16, 1024);
-      const uint64_t bK0 = desc_sw128(sKV, 16, 1024), bV0 = desc_sw128(sKV + 32768, 16, 1024);
-      const uint64_t bKm0 = desc_sw128(sKV, 16384, 1024);   // K pair as the MN-major B operand [keys x d]
+      const uint64_t bK0 = desc_sw128(sK, 16, 1024), bV0 = desc_sw128(sV, 16, 1024);
+      const uint64_t bKm0 = desc_sw128(sK, 16384, 1024);   // K pair as the MN-major B operand [keys x d]
       const uint32_t tDP = tbase + 256, tDQ = tbase + 384;
-      auto issue_s = [&](int32_t j) {
-        const int st = j & 1;
-        const uint64_t so = (uint64_t)(st * (kDqStageKV >> 4));
+      // S of step j: needs its K pair
+      auto issue_s = [&](int32_t j) -> bool {
+        const int sk = j % kDqNK;
+        if (!wait_ab(&B->k_full[sk], (j / kDqNK) & 1, C, p.status)) return false;
+        tc_fence_after();
+        const uint64_t so = (uint64_t)(sk * (32768 >> 4));
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          mma_f16_ss(tbase + 128 * st, aQ + o, bK0 + so + o, kIdRP, kk > 0);
+          mma_f16_ss(tbase + 128 * (j & 1), aQ + o, bK0 + so + o, kIdRP, kk > 0);
         }
-        mma_commit(&B->s_full[st]);
+        mma_commit(&B->s_full[j & 1]);
+        return true;
       };
-      auto issue_dp = [&](int32_t j) {
-        const uint64_t so = (uint64_t)((j & 1) * (kDqStageKV >> 4));
+      // dP of step j: needs its V pair, which it alone reads
+      auto issue_dp = [&](int32_t j) -> bool {
+        const int sv = j % kDqNV;
+        if (!wait_ab(&B->v_full[sv], (j / kDqNV) & 1, C, p.status)) return false;
+        tc_fence_after();
+        const uint64_t so = (uint64_t)(sv * (32768 >> 4));
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
           mma_f16_ss(tDP, aDO + o, bV0 + so + o, kIdRP, kk > 0);
         }
         mma_commit(&B->dp_full);
+        mma_commit(&B->v_empty[sv]);
+        return true;
       };
-      bool ok = wait_ab(&B->q_full, 0, C, p.status) && wait_ab(&B->kv_full[0], 0, C, p.status);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-      }
-      if (ok && n > 1 && (ok = wait_ab(&B->kv_full[1], 0, C, p.status))) {
-        tc_fence_after();
-        issue_s(1);
-      }
-      if (ok) issue_dp(0);
+      bool ok = wait_ab(&B->q_full, 0, C, p.status) && issue_s(0);
+      if (ok && n > 1) ok = issue_s(1);
+      if (ok) ok = issue_dp(0);
       for (int32_t j = 0; ok && j < n; j++) {
-        const int st = j & 1;
-        const uint64_t so = (uint64_t)(st * (kDqStageKV >> 4));
+        const int sk = j % kDqNK;
+        const uint64_t so = (uint64_t)(sk * (32768 >> 4));
         if (!(ok = wait_ab(&B->ds_full, j & 1, C, p.status))) break;
         tc_fence_after();
         // dQ += dS K  (K = 16 keys per MMA: 8 TMEM columns of dS, 2 swizzle atoms of K)
@@ -609,14 +679,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         for (int kk = 0; kk < 8; kk++)
           if (kk < nk)
             mma_f16_ts(tDQ, tDP + kk * 8, bKm0 + so + (uint64_t)(kk * (2048 >> 4)), kIdDQ, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&B->kv_empty[st]);
+        mma_commit(&B->k_empty[sk]);
         // dP of the next step overwrites dS only after the MMAs above have read it
-        if (j + 1 < n) issue_dp(j + 1);
-        if (j + 2 < n) {
-          if (!(ok = wait_ab(&B->kv_full[st], ((j + 2) >> 1) & 1, C, p.status))) break;
-          tc_fence_after();
-          issue_s(j + 2);
-        }
+        if (j + 1 < n && !(ok = issue_dp(j + 1))) break;
+        if (j + 2 < n && !(ok = issue_s(j + 2))) break;
       }
       if (ok) mma_commit(&B->acc_done);
       mma_commit(&B->drain);
@@ -631,8 +697,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const bool row_ok = r < rows;
     const int64_t row = (int64_t)row0 + r;
-    const float lse2 = row_ok ? p.lse[(int64_t)h * p.n_rows + row] * 1.4426950408889634f : 0.f;
-    const float Dr = row_ok ? p.Dv[(int64_t)h * p.n_rows + row] : 0.f;
+    const float lse2 = p.lse2t[((size_t)tile * p.Hq + h) * 128 + r];
+    const float Dr = p.Dt[((size_t)tile * p.Hq + h) * 128 + r];
     const uint32_t tDP = tbase + lane_off + 256;
     bool ok = true;
     octo_entry e_next{};
@@ -763,7 +829,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
 }  // namespace
 
-int bwd_pre_launch(const octo_plan_s* p, int32_t Hq, const void* o, const void* dout, float* Dv, cudaStream_t s);
 
 bool bwd_tc_supported(const octo_plan_s* p, int32_t Hq) {
   const octo_pool_desc& d = p->pool->desc;
@@ -773,7 +838,8 @@ bool bwd_tc_supported(const octo_plan_s* p, int32_t Hq) {
 }
 
 size_t bwd_tc_workspace(const octo_plan_s* p, int32_t Hq) {
-  return align_up((size_t)p->info.n_rows * Hq * sizeof(float), 256);
+  // LSE and D per tile row (fp32) and the 2 KB statistics block per (tile, head)
+  return 2 * align_up((size_t)p->info.n_tiles * Hq * 128 * sizeof(float), 256) + (size_t)p->info.n_tiles * Hq * 2048;
 }
 
 int bwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const void* v, const void* o,
@@ -782,9 +848,16 @@ int bwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const
   const octo_pool_desc& d = p->pool->desc;
   const int64_t N = p->info.n_rows;
   if (N == 0 || p->info.n_tiles == 0) return OCTO_OK;
-  if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)dout | (uintptr_t)dq) & 15) return OCTO_EINVAL;
-  float* Dv = (float*)ws;
-  if (int st = bwd_pre_launch(p, Hq, o, dout, Dv, s)) return st;
+  if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)o | (uintptr_t)dout | (uintptr_t)dq | (uintptr_t)ws) & 15)
+    return OCTO_EINVAL;
+  const size_t st_bytes = align_up((size_t)p->info.n_tiles * Hq * 128 * sizeof(float), 256);
+  float* lse2t = (float*)ws;
+  float* Dt = (float*)((char*)ws + st_bytes);
+  uint4* aug = (uint4*)((char*)ws + 2 * st_bytes);
+  k_pre_tiles<<<(unsigned)(p->info.n_tiles * Hq), 128, 0, s>>>((const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, lse,
+                                                                 p->tile_row0, p->tile_rows, N, Hq, 1.f / scale, lse2t,
+                                                                 Dt, aug);
+  count_launch();
   CUtensorMap mq, mdo, mk, mv;
   {
     uint64_t dims[3] = {128, (uint64_t)Hq, (uint64_t)N};
@@ -822,8 +895,9 @@ int bwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const
   prm.pair_n_items = p->pair_n_items;
   prm.pair_order = p->pair_order;
   prm.pair_items = p->pair_items;
-  prm.lse = lse;
-  prm.Dv = Dv;
+  prm.lse2t = lse2t;
+  prm.Dt = Dt;
+  prm.aug = aug;
   prm.dq = dq;
   prm.dk = dk;
   prm.dv = dv;

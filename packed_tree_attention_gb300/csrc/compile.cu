@@ -414,10 +414,10 @@ __device__ __forceinline__ void pair_half(PairItem& it, int h, const octo_entry*
     it.lo[h] = (int16_t)e->kv_lo;
     it.hi[h] = (int16_t)e->kv_hi;
     it.qlo[h] = (int16_t)e->q_lo;
-    it.cz[h] = (int16_t)(e->flags & 1);
+    if (e->flags & 1) it.causal |= (int16_t)(1 << h);
     it.diag[h] = e->diag;
   } else {
-    it.lo[h] = it.hi[h] = it.qlo[h] = it.cz[h] = 0;
+    it.lo[h] = it.hi[h] = it.qlo[h] = 0;
     it.diag[h] = 0;
   }
 }
@@ -437,8 +437,10 @@ __global__ void k_pair_items(const int32_t* __restrict__ pair_pages, const int32
     const int32_t e = csc[oa + i];
     const octo_entry E = entries[e];
     PairItem it;
+    it.tile = (int32_t)E.q_tile;
     it.row0 = tile_row0[E.q_tile];
-    it.rows = tile_rows[E.q_tile];
+    it.rows = (int16_t)tile_rows[E.q_tile];
+    it.causal = 0;
     pair_half(it, 0, &E);
     bool joined = false;
     if (pb >= 0 && e + 1 < n_entries) {
@@ -473,8 +475,10 @@ __global__ void k_pair_items(const int32_t* __restrict__ pair_pages, const int32
       if (keep) {
         const octo_entry F = entries[e];
         PairItem it;
+        it.tile = (int32_t)F.q_tile;
         it.row0 = tile_row0[F.q_tile];
-        it.rows = tile_rows[F.q_tile];
+        it.rows = (int16_t)tile_rows[F.q_tile];
+        it.causal = 0;
         pair_half(it, 0, nullptr);
         pair_half(it, 1, &F);
         items[base + la + before + __popc(bal & ((1u << lane) - 1))] = it;

@@ -47,9 +47,11 @@ struct DevMount {
 // the first page, 64-127 from the second), with each half's visibility rectangle copied
 // from its tile-list entry (lo = hi = 0: no entry for that half).  32 bytes.
 struct PairItem {
-  int32_t row0, rows;     // first packed row of the query tile, rows in it
+  int32_t tile, row0;     // query tile, its first packed row
   int16_t lo[2], hi[2];   // visible slots [lo, hi) of each page
-  int16_t qlo[2], cz[2];  // first visible tile row; causal flag
+  int16_t qlo[2];         // first visible tile row
+  int16_t rows;           // rows in the tile
+  int16_t causal;         // bit h: half h is causal
   int32_t diag[2];        // causal: row r sees slot j iff j <= r + diag
 };
 
