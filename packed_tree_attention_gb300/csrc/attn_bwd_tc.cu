@@ -518,10 +518,14 @@ struct DqBars {
   uint64_t q_full;
   uint64_t k_full[kDqNK], k_empty[kDqNK];
   uint64_t v_full[kDqNV], v_empty[kDqNV];
-  uint64_t s_full[2];
-  uint64_t dp_full;
-  uint64_t dp_read;   // softmax warpgroup 0 has read its dP columns
-  uint64_t ds_full;
+  uint64_t s_full, s_free;   // S of the current step in TMEM / read by every softmax thread
+  uint64_t dp_full[2];
+  uint64_t dp_read[2];       // softmax warpgroup 0 has read its columns of that dP buffer
+  // dS of that buffer written back by all 256 softmax threads.  One barrier per buffer:
+  // warpgroup 0 may finish step j + 1 before warpgroup 1 finishes step j, and its
+  // arrivals must not complete step j's phase.
+  uint64_t ds_full[2];
+  uint64_t dq_done;   // the dQ MMAs of a step have completed (their dS buffer may be rewritten)
   uint64_t acc_done;  // single use: every dQ MMA has completed
   uint64_t drain;
   Ctl ctl;
@@ -529,10 +533,12 @@ struct DqBars {
 
 // One CTA per (query tile, query head), tiles heaviest first.  The tile's entries go two at
 // a time: keys 0-63 of a step from the first entry, 64-127 from the second (an odd last
-// entry runs alone; its dQ MMAs stop at key 64).  TMEM: S of step j in [128 (j % 2), +128),
-// dP [256, 384) with dS as bf16 over its first 64 columns, dQ [384, 512); lane = row.
-// MMA order per step j: dQ(j), dP(j + 1), S(j + 2); K and V have rings of their own, as V
-// is free once dP has run while K is read again by dQ.
+// entry runs alone; its dQ MMAs stop at key 64).  TMEM: S [0, 128), dP of step j in
+// [128 + 128 (j % 2), +128) with dS as bf16 over its first 64 columns, dQ [384, 512);
+// lane = row.  MMA order per step j: S(j + 1) once the softmax has read S(j), dP(j + 1)
+// once dQ(j - 1) has completed (it read dS(j - 1) from that buffer), dQ(j) once dS(j) is
+// written; the softmax finds S(j + 1) and dP(j + 1) ready when it finishes step j.  K and
+// V have rings of their own, as V is free once dP has run while K is read again by dQ.
 __global__ void __launch_bounds__(kDqThreads, 1)
     k_dq_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
             const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, BwdParams p) {
@@ -560,11 +566,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mbar_init(&B->v_full[s], 1);
       mbar_init(&B->v_empty[s], 1);
     }
-    mbar_init(&B->s_full[0], 1);
-    mbar_init(&B->s_full[1], 1);
-    mbar_init(&B->dp_full, 1);
-    mbar_init(&B->dp_read, 128);
-    mbar_init(&B->ds_full, 256);
+    mbar_init(&B->s_full, 1);
+    mbar_init(&B->s_free, 256);
+    for (int b = 0; b < 2; b++) {
+      mbar_init(&B->dp_full[b], 1);
+      mbar_init(&B->dp_read[b], 128);
+    }
+    mbar_init(&B->ds_full[0], 256);
+    mbar_init(&B->ds_full[1], 256);
+    mbar_init(&B->dq_done, 1);
     mbar_init(&B->acc_done, 1);
     mbar_init(&B->drain, 1);
     C->abort = 0;
@@ -635,7 +645,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const uint64_t aQ = desc_sw128(sQ, 16, 1024), aDO = desc_sw128(sDO, 16, 1024);
       const uint64_t bK0 = desc_sw128(sK, 16, 1024), bV0 = desc_sw128(sV, 16, 1024);
       const uint64_t bKm0 = desc_sw128(sK, 16384, 1024);   // K pair as the MN-major B operand [keys x d]
-      const uint32_t tDP = tbase + 256, tDQ = tbase + 384;
+      const uint32_t tDQ = tbase + 384;
       // S of step j: needs its K pair
       auto issue_s = [&](int32_t j) -> bool {
         const int sk = j % kDqNK;
@@ -645,9 +655,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          mma_f16_ss(tbase + 128 * (j & 1), aQ + o, bK0 + so + o, kIdRP, kk > 0);
+          mma_f16_ss(tbase, aQ + o, bK0 + so + o, kIdRP, kk > 0);
         }
-        mma_commit(&B->s_full[j & 1]);
+        mma_commit(&B->s_full);
         return true;
       };
       // dP of step j: needs its V pair, which it alone reads
@@ -659,30 +669,38 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          mma_f16_ss(tDP, aDO + o, bV0 + so + o, kIdRP, kk > 0);
+          mma_f16_ss(tbase + 128 + 128 * (j & 1), aDO + o, bV0 + so + o, kIdRP, kk > 0);
         }
-        mma_commit(&B->dp_full);
+        mma_commit(&B->dp_full[j & 1]);
         mma_commit(&B->v_empty[sv]);
         return true;
       };
-      bool ok = wait_ab(&B->q_full, 0, C, p.status) && issue_s(0);
-      if (ok && n > 1) ok = issue_s(1);
-      if (ok) ok = issue_dp(0);
+      bool ok = wait_ab(&B->q_full, 0, C, p.status) && issue_s(0) && issue_dp(0);
+      if (ok && n > 1) ok = issue_dp(1);
       for (int32_t j = 0; ok && j < n; j++) {
         const int sk = j % kDqNK;
         const uint64_t so = (uint64_t)(sk * (32768 >> 4));
-        if (!(ok = wait_ab(&B->ds_full, j & 1, C, p.status))) break;
+        if (j + 1 < n) {
+          if (!(ok = wait_ab(&B->s_free, j & 1, C, p.status))) break;
+          if (!(ok = issue_s(j + 1))) break;
+          if (j >= 1) {
+            // dP(j + 1) goes to the buffer whose dS the MMAs of dQ(j - 1) read; waiting for
+            // them costs nothing here (S(j + 1) keeps the tensor pipe busy meanwhile)
+            if (!(ok = wait_ab(&B->dq_done, (j - 1) & 1, C, p.status))) break;
+            if (!(ok = issue_dp(j + 1))) break;
+          }
+        }
+        if (!(ok = wait_ab(&B->ds_full[j & 1], (j >> 1) & 1, C, p.status))) break;
         tc_fence_after();
         // dQ += dS K  (K = 16 keys per MMA: 8 TMEM columns of dS, 2 swizzle atoms of K)
+        const uint32_t tDS = tbase + 128 + 128 * (j & 1);
         const int nk = 2 * j + 1 < ne ? 8 : 4;
 #pragma unroll
         for (int kk = 0; kk < 8; kk++)
           if (kk < nk)
-            mma_f16_ts(tDQ, tDP + kk * 8, bKm0 + so + (uint64_t)(kk * (2048 >> 4)), kIdDQ, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_f16_ts(tDQ, tDS + kk * 8, bKm0 + so + (uint64_t)(kk * (2048 >> 4)), kIdDQ, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&B->k_empty[sk]);
-        // dP of the next step overwrites dS only after the MMAs above have read it
-        if (j + 1 < n && !(ok = issue_dp(j + 1))) break;
-        if (j + 2 < n && !(ok = issue_s(j + 2))) break;
+        mma_commit(&B->dq_done);
       }
       if (ok) mma_commit(&B->acc_done);
       mma_commit(&B->drain);
@@ -699,7 +717,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int64_t row = (int64_t)row0 + r;
     const float lse2 = p.lse2t[((size_t)tile * p.Hq + h) * 128 + r];
     const float Dr = p.Dt[((size_t)tile * p.Hq + h) * 128 + r];
-    const uint32_t tDP = tbase + lane_off + 256;
     bool ok = true;
     octo_entry e_next{};
     if (n > 0 && c < ne) e_next = p.entries[e0 + c];
@@ -716,12 +733,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       }
       const bool all_vis = __all_sync(0xffffffffu, lo == 0 && hi == 64);
       const int b = j & 1;
-      if (!(ok = warp_wait_ab(&B->s_full[b], (j >> 1) & 1, C, p.status))) break;
+      const uint32_t tDP = tbase + lane_off + 128 + 128 * b;
+      if (!(ok = warp_wait_ab(&B->s_full, j & 1, C, p.status))) break;
       tc_fence_after();
       uint32_t x0[32], x1[32];
-      tmem_ld32(tbase + lane_off + 128 * b + 64 * c, x0);
-      tmem_ld32(tbase + lane_off + 128 * b + 64 * c + 32, x1);
+      tmem_ld32(tbase + lane_off + 64 * c, x0);
+      tmem_ld32(tbase + lane_off + 64 * c + 32, x1);
       tmem_wait_ld();
+      // S may be overwritten by the next step's S from here on
+      tc_fence_before();
+      mbar_arrive(&B->s_free);
       float P[64];
       auto p_phase = [&](auto masked) {
 #pragma unroll
@@ -757,7 +778,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         p_phase(std::false_type{});
       else
         p_phase(std::true_type{});
-      if (!(ok = warp_wait_ab(&B->dp_full, j & 1, C, p.status))) break;
+      if (!(ok = warp_wait_ab(&B->dp_full[b], (j >> 1) & 1, C, p.status))) break;
       tc_fence_after();
       uint32_t pk[32];
       auto ds_phase = [&](auto masked) {
@@ -787,16 +808,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         ds_phase(std::true_type{});
       if (c == 0) {
         tc_fence_before();
-        mbar_arrive(&B->dp_read);
+        mbar_arrive(&B->dp_read[b]);
       } else {
         // dS of keys 64-127 lands on dP columns that warpgroup 0 reads
-        if (!(ok = warp_wait_ab(&B->dp_read, j & 1, C, p.status))) break;
+        if (!(ok = warp_wait_ab(&B->dp_read[b], (j >> 1) & 1, C, p.status))) break;
         tc_fence_after();
       }
       tmem_st32(tDP + 32 * c, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&B->ds_full);
+      mbar_arrive(&B->ds_full[b]);
     }
     // epilogue: warpgroup c writes d columns [64 c, 64 c + 64) of this row's dQ
     if (n > 0) {
