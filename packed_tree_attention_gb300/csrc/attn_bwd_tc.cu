@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(128) k_pre_tiles(const __nv_bfloat16* __restri
 // =====================================================================================
 // dK / dV
 // =====================================================================================
-constexpr int kDkThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, warps 4-11 softmax
+constexpr int kDkThreads = 384;   // warp 0 TMA, warps 1-2 MMA issuers (1 also TMEM), warps 4-11 softmax
 // smem: ones blocks 2 x 4KB | 2 stages x row-statistics block 4KB | K pair 32KB | V pair 32KB |
 // 2 stages x (Q 32KB + dO 32KB).  The softmax warps read no memory per element: LSE and D
 // enter through one more K = 16 MMA step (ones x statistics block) of S^T and dP^T.
@@ -169,7 +169,7 @@ struct DkBars {
   uint64_t s_full, dp_full;   // S^T / dP^T of the current step in TMEM
   uint64_t s_read, dp_read;   // softmax warpgroup 0 has read its S^T / dP^T columns
   uint64_t p_full, ds_full;   // P^T / dS^T written back to TMEM
-  uint64_t acc_done;          // single use: every accumulation MMA has completed
+  uint64_t acc_done;          // single use, one arrival per issuer: every accumulation MMA has completed
   uint64_t drain;
   Ctl ctl;
 };
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     mbar_init(&B->kv_full, 1);
     for (int s = 0; s < 2; s++) {
       mbar_init(&B->qd_full[s], 1);
-      mbar_init(&B->qd_free[s], 1);
+      mbar_init(&B->qd_free[s], 2);   // both issuers' MMAs of the item have completed
     }
     mbar_init(&B->s_full, 1);
     mbar_init(&B->dp_full, 1);
@@ -204,8 +204,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     mbar_init(&B->dp_read, 128);
     mbar_init(&B->p_full, 256);
     mbar_init(&B->ds_full, 256);
-    mbar_init(&B->acc_done, 1);
-    mbar_init(&B->drain, 1);
+    mbar_init(&B->acc_done, 2);
+    mbar_init(&B->drain, 2);
     C->abort = 0;
     fence_mbar_init();
   }
@@ -274,65 +274,54 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       for (int32_t w = max(0, issued - 2); w < issued; w++)
         mbar_wait(&B->qd_full[w & 1], (w >> 1) & 1, p.status, OCTO_ETIMEOUT);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
+    // Two issuers with disjoint TMEM, so that a full tensor-core queue on one chain does
+    // not hold up the other.  A (warp 1): dV += P^T dO, then S^T of the next item over P^T;
+    // B (warp 2): dK += dS^T Q, then dP^T of the next item over dS^T.  Each thread's MMAs
+    // run in issue order, which orders every overwrite after the MMAs that read the columns.
+    const bool isA = warp == 1;
     if (lane == 0 && n > 0) {
-      const uint64_t aK = desc_sw128(sK, 16, 1024), aV = desc_sw128(sV, 16, 1024);
-      const uint64_t bQ0 = desc_sw128(sQD, 16, 1024), bDO0 = desc_sw128(sQD + 32768, 16, 1024);
-      const uint64_t bQm0 = desc_sw128(sQD, 16384, 1024), bDOm0 = desc_sw128(sQD + 32768, 16384, 1024);
-      const uint32_t tS = tbase, tDP = tbase + 128, tDV = tbase + 256, tDK = tbase + 384;
-      const uint64_t aOnesS = desc_noswz(smem_u32(smem + kDkOffOnesS), 2048, 128);
-      const uint64_t aOnesD = desc_noswz(smem_u32(smem + kDkOffOnesD), 2048, 128);
+      const uint64_t aX = desc_sw128(isA ? sK : sV, 16, 1024);   // K for S^T, V for dP^T
+      const uint64_t bX0 = desc_sw128(sQD + (isA ? 0 : 32768), 16, 1024);   // Q / dO, K-major
+      // the MN-major B operand of the accumulation: dO for dV, Q for dK
+      const uint64_t bY0 = desc_sw128(sQD + (isA ? 32768 : 0), 16384, 1024);
+      const uint32_t tX = tbase + (isA ? 0 : 128);     // S^T / dP^T (then P^T / dS^T)
+      const uint32_t tAcc = tbase + (isA ? 256 : 384); // dV / dK
+      // S'^T = K Q^T - LSE/scale  or  dP'^T = V dO^T - D
+      const uint64_t aOnes = desc_noswz(smem_u32(smem + (isA ? kDkOffOnesS : kDkOffOnesD)), 2048, 128);
       const uint64_t bAug0 = desc_noswz(smem_u32(smem + kDkOffAug), 2048, 128);
-      // S'^T = K Q^T - LSE/scale  and  dP'^T = V dO^T - D
-      auto issue_s = [&](int st) {
+      uint64_t* x_full = isA ? &B->s_full : &B->dp_full;
+      uint64_t* y_full = isA ? &B->p_full : &B->ds_full;
+      auto issue_x = [&](int st) {
         const uint64_t so = (uint64_t)(st * (kDkStageQD >> 4));
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          mma_f16_ss(tS, aK + o, bQ0 + so + o, kIdKR, kk > 0);
+          mma_f16_ss(tX, aX + o, bX0 + so + o, kIdKR, kk > 0);
         }
-        mma_f16_ss(tS, aOnesS, bAug0 + (uint64_t)(st * (4096 >> 4)), kIdKR, 1);
-        mma_commit(&B->s_full);
-      };
-      auto issue_dp = [&](int st) {
-        const uint64_t so = (uint64_t)(st * (kDkStageQD >> 4));
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++) {
-          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          mma_f16_ss(tDP, aV + o, bDO0 + so + o, kIdKR, kk > 0);
-        }
-        mma_f16_ss(tDP, aOnesD, bAug0 + (uint64_t)(st * (4096 >> 4)), kIdKR, 1);
-        mma_commit(&B->dp_full);
+        mma_f16_ss(tX, aOnes, bAug0 + (uint64_t)(st * (4096 >> 4)), kIdKR, 1);
+        mma_commit(x_full);
       };
       bool ok = wait_ab(&B->kv_full, 0, C, p.status) && wait_ab(&B->qd_full[0], 0, C, p.status);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
+        issue_x(0);
       }
       for (int32_t w = 0; ok && w < n; w++) {
         const int st = w & 1;
         const uint64_t so = (uint64_t)(st * (kDkStageQD >> 4));
-        if (!(ok = wait_ab(&B->p_full, w & 1, C, p.status))) break;
+        if (!(ok = wait_ab(y_full, w & 1, C, p.status))) break;
         tc_fence_after();
-        // dV += P^T dO   (K = 16 query rows per MMA: 8 TMEM columns of P^T, 2 swizzle atoms of dO)
+        // K = 16 query rows per MMA: 8 TMEM columns of P^T / dS^T, 2 swizzle atoms of dO / Q
 #pragma unroll
         for (int kk = 0; kk < 8; kk++)
-          mma_f16_ts(tDV, tS + kk * 8, bDOm0 + so + (uint64_t)(kk * (2048 >> 4)), kIdKD, (w > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts(tAcc, tX + kk * 8, bY0 + so + (uint64_t)(kk * (2048 >> 4)), kIdKD, (w > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&B->qd_free[st]);
         if (w + 1 < n) {
-          // S^T of the next step overwrites P^T only after the MMAs above have read it
           if (!(ok = wait_ab(&B->qd_full[st ^ 1], ((w + 1) >> 1) & 1, C, p.status))) break;
           tc_fence_after();
-          issue_s(st ^ 1);
+          issue_x(st ^ 1);
         }
-        if (!(ok = wait_ab(&B->ds_full, w & 1, C, p.status))) break;
-        tc_fence_after();
-        // dK += dS^T Q
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++)
-          mma_f16_ts(tDK, tDP + kk * 8, bQm0 + so + (uint64_t)(kk * (2048 >> 4)), kIdKD, (w > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&B->qd_free[st]);
-        if (w + 1 < n) issue_dp(st ^ 1);
       }
       if (ok) mma_commit(&B->acc_done);
       mma_commit(&B->drain);
@@ -502,7 +491,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
 // =====================================================================================
 // dQ
 // =====================================================================================
-constexpr int kDqThreads = 384;   // warp 0 TMA, warp 1 MMA + TMEM, warps 4-11 softmax
+constexpr int kDqThreads = 384;   // warp 0 TMA, warp 1 S/dP MMAs + TMEM, warp 2 dQ MMAs, warps 4-11 softmax
 constexpr int kDqNK = 3;          // K pairs in flight: step j's K lands while step j - 1 runs
 constexpr int kDqNV = 2;
 // smem: Q 32KB | dO 32KB | 3 stages x K pair 32KB | 2 stages x V pair 32KB
@@ -525,7 +514,7 @@ struct DqBars {
   // warpgroup 0 may finish step j + 1 before warpgroup 1 finishes step j, and its
   // arrivals must not complete step j's phase.
   uint64_t ds_full[2];
-  uint64_t dq_done;   // the dQ MMAs of a step have completed (their dS buffer may be rewritten)
+  uint64_t dq_done[2];   // dQ of a step has completed: its dS buffer may be rewritten
   uint64_t acc_done;  // single use: every dQ MMA has completed
   uint64_t drain;
   Ctl ctl;
@@ -535,10 +524,11 @@ struct DqBars {
 // a time: keys 0-63 of a step from the first entry, 64-127 from the second (an odd last
 // entry runs alone; its dQ MMAs stop at key 64).  TMEM: S [0, 128), dP of step j in
 // [128 + 128 (j % 2), +128) with dS as bf16 over its first 64 columns, dQ [384, 512);
-// lane = row.  MMA order per step j: S(j + 1) once the softmax has read S(j), dP(j + 1)
-// once dQ(j - 1) has completed (it read dS(j - 1) from that buffer), dQ(j) once dS(j) is
-// written; the softmax finds S(j + 1) and dP(j + 1) ready when it finishes step j.  K and
-// V have rings of their own, as V is free once dP has run while K is read again by dQ.
+// lane = row.  Two MMA issuers, so that a full tensor-core queue on one chain does not hold
+// up the other: A issues S(j + 1) once the softmax has read S(j) and dP(j + 1) once dQ(j - 1)
+// has completed (it read dS(j - 1) from that buffer); B issues dQ(j) once dS(j) is written.
+// The softmax finds S(j + 1) and dP(j + 1) ready when it finishes step j.  K and V have
+// rings of their own, as V is free once dP has run while K is read again by dQ.
 __global__ void __launch_bounds__(kDqThreads, 1)
     k_dq_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
             const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, BwdParams p) {
@@ -574,9 +564,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
     mbar_init(&B->ds_full[0], 256);
     mbar_init(&B->ds_full[1], 256);
-    mbar_init(&B->dq_done, 1);
+    mbar_init(&B->dq_done[0], 1);
+    mbar_init(&B->dq_done[1], 1);
     mbar_init(&B->acc_done, 1);
-    mbar_init(&B->drain, 1);
+    mbar_init(&B->drain, 2);
     C->abort = 0;
     fence_mbar_init();
   }
@@ -641,11 +632,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         mbar_wait(&B->v_full[j % kDqNV], (j / kDqNV) & 1, p.status, OCTO_ETIMEOUT);
     }
   } else if (warp == 1) {
+    // issuer A: S and dP (each thread's MMAs run in issue order; the two issuers touch
+    // disjoint TMEM, and A rewrites a dS buffer only after B's dQ that read it completed)
     if (lane == 0 && n > 0) {
       const uint64_t aQ = desc_sw128(sQ, 16, 1024), aDO = desc_sw128(sDO, 16, 1024);
       const uint64_t bK0 = desc_sw128(sK, 16, 1024), bV0 = desc_sw128(sV, 16, 1024);
-      const uint64_t bKm0 = desc_sw128(sK, 16384, 1024);   // K pair as the MN-major B operand [keys x d]
-      const uint32_t tDQ = tbase + 384;
       // S of step j: needs its K pair
       auto issue_s = [&](int32_t j) -> bool {
         const int sk = j % kDqNK;
@@ -677,22 +668,31 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       };
       bool ok = wait_ab(&B->q_full, 0, C, p.status) && issue_s(0) && issue_dp(0);
       if (ok && n > 1) ok = issue_dp(1);
+      for (int32_t j = 0; ok && j + 1 < n; j++) {
+        if (!(ok = wait_ab(&B->s_free, j & 1, C, p.status))) break;
+        if (!(ok = issue_s(j + 1))) break;
+        if (j >= 1) {
+          // dP(j + 1) rewrites the buffer dQ(j - 1) read
+          if (!(ok = wait_ab(&B->dq_done[(j - 1) & 1], ((j - 1) >> 1) & 1, C, p.status))) break;
+          if (!(ok = issue_dp(j + 1))) break;
+        }
+      }
+      mma_commit(&B->drain);
+      mbar_wait(&B->drain, 0, p.status, OCTO_ETIMEOUT);
+    }
+  } else if (warp == 2) {
+    // issuer B: dQ += dS K once the softmax has written dS(j)
+    if (lane == 0 && n > 0) {
+      const uint64_t bKm0 = desc_sw128(sK, 16384, 1024);   // K pair as the MN-major B operand [keys x d]
+      const uint32_t tDQ = tbase + 384;
+      bool ok = true;
       for (int32_t j = 0; ok && j < n; j++) {
         const int sk = j % kDqNK;
         const uint64_t so = (uint64_t)(sk * (32768 >> 4));
-        if (j + 1 < n) {
-          if (!(ok = wait_ab(&B->s_free, j & 1, C, p.status))) break;
-          if (!(ok = issue_s(j + 1))) break;
-          if (j >= 1) {
-            // dP(j + 1) goes to the buffer whose dS the MMAs of dQ(j - 1) read; waiting for
-            // them costs nothing here (S(j + 1) keeps the tensor pipe busy meanwhile)
-            if (!(ok = wait_ab(&B->dq_done, (j - 1) & 1, C, p.status))) break;
-            if (!(ok = issue_dp(j + 1))) break;
-          }
-        }
         if (!(ok = wait_ab(&B->ds_full[j & 1], (j >> 1) & 1, C, p.status))) break;
         tc_fence_after();
-        // dQ += dS K  (K = 16 keys per MMA: 8 TMEM columns of dS, 2 swizzle atoms of K)
+        // K = 16 keys per MMA: 8 TMEM columns of dS, 2 swizzle atoms of K.  S(j), the other
+        // reader of this K stage, completed before the softmax could write dS(j).
         const uint32_t tDS = tbase + 128 + 128 * (j & 1);
         const int nk = 2 * j + 1 < ne ? 8 : 4;
 #pragma unroll
@@ -700,7 +700,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (kk < nk)
             mma_f16_ts(tDQ, tDS + kk * 8, bKm0 + so + (uint64_t)(kk * (2048 >> 4)), kIdDQ, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&B->k_empty[sk]);
-        mma_commit(&B->dq_done);
+        mma_commit(&B->dq_done[j & 1]);
       }
       if (ok) mma_commit(&B->acc_done);
       mma_commit(&B->drain);
