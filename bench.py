@@ -124,6 +124,21 @@ def unique_tokens(entries, num_pages, P):
 
 
 # --------------------------------------------------------------------------------------
+L2_BYTES = 129 * 2**20   # GB300 L2
+
+WORKLOAD_DESC = {
+    "episode": "episode: 16K prefix, 7 branches x 32K owned tokens, 3 rewinds, 6 mounts",
+    "tree_fwd": "tree: 4K prefix, 4 x 8K branches, 2 mounts",
+    "train_step": "train step: 8 trees of ~140K owned tokens, fan-out 2-6, depth <= 3, mounts",
+    "tiny": "tiny: 64-token prefix, 2 x 32 branches, 1 mount",
+}
+
+
+def workload_desc(name, cfg):
+    return "%s; %dq/%dkv heads, d=%d, page %d, q-tile 128, %s fwd+bwd" % (
+        WORKLOAD_DESC.get(name, name), cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["P"], cfg.get("dtype", "bf16"))
+
+
 # workload construction (device tensors from the counter-based generator)
 # --------------------------------------------------------------------------------------
 def build_episode(pta, torch, name, seed, dev):
@@ -257,6 +272,7 @@ def run_ours(args, rank, world, dist):
     dv = torch.empty_like(dk)
     ws = torch.empty(max(1, plan.attn_bwd_workspace_size(Hq)), dtype=torch.uint8, device=dev)
     del plan
+    q_bytes = q.numel() * q.element_size()
     fwd_flops = 4.0 * d * Hq * pairs
     bwd_flops = 10.0 * d * Hq * pairs
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -415,10 +431,11 @@ def run_ours(args, rank, world, dist):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (counter-based generator, seed %d + rank)" % args.seed,
-        "config": {"workload": "episode: 16K prefix, 7 branches x 32K owned tokens, 3 rewinds, 6 mounts; "
-                               "16q/4kv heads, d=128, page 64, q-tile 128, bf16 fwd+bwd",
+        "config": {"workload": workload_desc(args.workload, cfg),
                    "packed_tokens": N, "visible_pairs": pairs, "useful_tflop_per_step": (fwd_flops + bwd_flops) / 1e12,
-                   "step": "plan compile + fwd + bwd", "l2": "inputs larger than L2 (Q alone 1 GB)",
+                   "step": "plan compile + fwd + bwd",
+                   "l2": ("inputs larger than L2 (Q alone %.0f MB)" if q_bytes > L2_BYTES else
+                          "inputs fit in L2 (Q %.0f MB): timings include L2 reuse") % (q_bytes / 1e6),
                    "parallelism": "replicas: one episode per GPU, no collective"},
         "breakdown_ms": {k: statistics.mean(v) for k, v in per.items()},
         "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,
@@ -452,8 +469,8 @@ def run_reference(args, rank, world):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(e for _, e in per),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (counter-based generator, seed %d)" % args.seed,
-           "config": {"workload": "episode: 16K prefix, 7 branches x 32K owned tokens, 3 rewinds, 6 mounts; "
-                                  "16q/4kv heads, d=128, page 64; each step a bounded row sample"},
+           "config": {"workload": workload_desc(args.workload, synth.CONFIGS[args.workload]) +
+                                  "; each step a bounded row sample"},
            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": desc},
            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
