@@ -167,15 +167,17 @@ struct DkBars {
   uint64_t qd_full[2];
   uint64_t qd_free[2];
   uint64_t s_full, dp_full;   // S^T / dP^T of the current step in TMEM
-  uint64_t s_read, dp_read;   // softmax warpgroup 0 has read its S^T / dP^T columns
   uint64_t p_full, ds_full;   // P^T / dS^T written back to TMEM
   uint64_t acc_done;          // single use, one arrival per issuer: every accumulation MMA has completed
   uint64_t drain;
   Ctl ctl;
 };
 
-// One CTA per (page pair, kv head).  TMEM: S^T [0,128) (P^T as bf16 over its first 64
-// columns), dP^T [128,256) (dS^T likewise), dV [256,384), dK [384,512); lane = key.
+// One CTA per (page pair, kv head).  TMEM: S^T [0,128), dP^T [128,256), dV [256,384),
+// dK [384,512); lane = key.  Softmax warpgroup c reads columns [64 c, 64 c + 64) of S^T and
+// dP^T and writes its 64 rows of P^T / dS^T as bf16 over the first 32 of them, so the A
+// operand of the accumulation MMAs sits at columns 0-31 and 64-95 of the region and no
+// warpgroup overwrites columns the other still reads.
 __global__ void __launch_bounds__(kDkThreads, 1)
     k_dkdv_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, BwdParams p) {
@@ -200,8 +202,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     }
     mbar_init(&B->s_full, 1);
     mbar_init(&B->dp_full, 1);
-    mbar_init(&B->s_read, 128);
-    mbar_init(&B->dp_read, 128);
     mbar_init(&B->p_full, 256);
     mbar_init(&B->ds_full, 256);
     mbar_init(&B->acc_done, 2);
@@ -312,10 +312,12 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         const uint64_t so = (uint64_t)(st * (kDkStageQD >> 4));
         if (!(ok = wait_ab(y_full, w & 1, C, p.status))) break;
         tc_fence_after();
-        // K = 16 query rows per MMA: 8 TMEM columns of P^T / dS^T, 2 swizzle atoms of dO / Q
+        // K = 16 query rows per MMA: 8 TMEM columns of P^T / dS^T (rows 64-127 at +64),
+        // 2 swizzle atoms of dO / Q
 #pragma unroll
         for (int kk = 0; kk < 8; kk++)
-          mma_f16_ts(tAcc, tX + kk * 8, bY0 + so + (uint64_t)(kk * (2048 >> 4)), kIdKD, (w > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts(tAcc, tX + kk * 8 + (kk >= 4 ? 32 : 0), bY0 + so + (uint64_t)(kk * (2048 >> 4)), kIdKD,
+                     (w > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&B->qd_free[st]);
         if (w + 1 < n) {
           if (!(ok = wait_ab(&B->qd_full[st ^ 1], ((w + 1) >> 1) & 1, C, p.status))) break;
@@ -356,10 +358,6 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       tmem_ld32(tS + 64 * c, x0);
       tmem_ld32(tS + 64 * c + 32, x1);
       tmem_wait_ld();
-      if (c == 0) {
-        tc_fence_before();
-        mbar_arrive(&B->s_read);
-      }
       // most steps see all 64 rows of this warpgroup for every key: no per-element mask
       const bool all_vis = __all_sync(0xffffffffu, rmin <= 64 * c && rmax >= 64 * c + 64);
       float P[64];
@@ -402,12 +400,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 32; i++) pk[i] = pack_bf16(P[2 * i], P[2 * i + 1]);
-      if (c == 1) {
-        // P^T of rows 64-127 lands on S^T columns that warpgroup 0 reads
-        if (!(ok = warp_wait_ab(&B->s_read, w & 1, C, p.status))) break;
-        tc_fence_after();
-      }
-      tmem_st32(tS + 32 * c, pk);
+      tmem_st32(tS + 64 * c, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&B->p_full);
@@ -443,14 +436,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
         ds_phase(std::false_type{});
       else
         ds_phase(std::true_type{});
-      if (c == 0) {
-        tc_fence_before();
-        mbar_arrive(&B->dp_read);
-      } else {
-        if (!(ok = warp_wait_ab(&B->dp_read, w & 1, C, p.status))) break;
-        tc_fence_after();
-      }
-      tmem_st32(tDP + 32 * c, pk);
+      tmem_st32(tDP + 64 * c, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&B->ds_full);
@@ -509,7 +495,6 @@ struct DqBars {
   uint64_t v_full[kDqNV], v_empty[kDqNV];
   uint64_t s_full, s_free;   // S of the current step in TMEM / read by every softmax thread
   uint64_t dp_full[2];
-  uint64_t dp_read[2];       // softmax warpgroup 0 has read its columns of that dP buffer
   // dS of that buffer written back by all 256 softmax threads.  One barrier per buffer:
   // warpgroup 0 may finish step j + 1 before warpgroup 1 finishes step j, and its
   // arrivals must not complete step j's phase.
@@ -523,8 +508,8 @@ struct DqBars {
 // One CTA per (query tile, query head), tiles heaviest first.  The tile's entries go two at
 // a time: keys 0-63 of a step from the first entry, 64-127 from the second (an odd last
 // entry runs alone; its dQ MMAs stop at key 64).  TMEM: S [0, 128), dP of step j in
-// [128 + 128 (j % 2), +128) with dS as bf16 over its first 64 columns, dQ [384, 512);
-// lane = row.  Two MMA issuers, so that a full tensor-core queue on one chain does not hold
+// [128 + 128 (j % 2), +128) with dS as bf16 at its columns 0-31 (keys 0-63) and 64-95
+// (keys 64-127), dQ [384, 512); lane = row.  Two MMA issuers, so that a full tensor-core queue on one chain does not hold
 // up the other: A issues S(j + 1) once the softmax has read S(j) and dP(j + 1) once dQ(j - 1)
 // has completed (it read dS(j - 1) from that buffer); B issues dQ(j) once dS(j) is written.
 // The softmax finds S(j + 1) and dP(j + 1) ready when it finishes step j.  K and V have
@@ -560,7 +545,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&B->s_free, 256);
     for (int b = 0; b < 2; b++) {
       mbar_init(&B->dp_full[b], 1);
-      mbar_init(&B->dp_read[b], 128);
     }
     mbar_init(&B->ds_full[0], 256);
     mbar_init(&B->ds_full[1], 256);
@@ -691,14 +675,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const uint64_t so = (uint64_t)(sk * (32768 >> 4));
         if (!(ok = wait_ab(&B->ds_full[j & 1], (j >> 1) & 1, C, p.status))) break;
         tc_fence_after();
-        // K = 16 keys per MMA: 8 TMEM columns of dS, 2 swizzle atoms of K.  S(j), the other
-        // reader of this K stage, completed before the softmax could write dS(j).
+        // K = 16 keys per MMA: 8 TMEM columns of dS (keys 64-127 at +64), 2 swizzle atoms of
+        // K.  S(j), the other reader of this K stage, completed before dS(j) was written.
         const uint32_t tDS = tbase + 128 + 128 * (j & 1);
         const int nk = 2 * j + 1 < ne ? 8 : 4;
 #pragma unroll
         for (int kk = 0; kk < 8; kk++)
           if (kk < nk)
-            mma_f16_ts(tDQ, tDS + kk * 8, bKm0 + so + (uint64_t)(kk * (2048 >> 4)), kIdDQ, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_f16_ts(tDQ, tDS + kk * 8 + (kk >= 4 ? 32 : 0), bKm0 + so + (uint64_t)(kk * (2048 >> 4)), kIdDQ,
+                       (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&B->k_empty[sk]);
         mma_commit(&B->dq_done[j & 1]);
       }
@@ -806,15 +791,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         ds_phase(std::false_type{});
       else
         ds_phase(std::true_type{});
-      if (c == 0) {
-        tc_fence_before();
-        mbar_arrive(&B->dp_read[b]);
-      } else {
-        // dS of keys 64-127 lands on dP columns that warpgroup 0 reads
-        if (!(ok = warp_wait_ab(&B->dp_read[b], (j >> 1) & 1, C, p.status))) break;
-        tc_fence_after();
-      }
-      tmem_st32(tDP + 32 * c, pk);
+      // dS of keys [64 c, 64 c + 64) over the first 32 of the dP columns this warpgroup read
+      tmem_st32(tDP + 64 * c, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&B->ds_full[b]);
