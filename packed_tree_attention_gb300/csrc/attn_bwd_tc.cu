@@ -84,8 +84,21 @@ __device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, Ctl* C, 
   atomicExch(status, OCTO_ETIMEOUT);
   return false;
 }
+// Barrier traffic of the softmax warps is kept to one lane per warp: while MMAs stream
+// their operands from shared memory, every other shared-memory access (mbarrier polls and
+// arrivals included) queues behind them.  Lane 0 waits and the warp sync passes the
+// acquired state on; for an arrival every lane's TMEM accesses are fenced and ordered before
+// the warp sync, and lane 0's arrive releases them.
 __device__ __forceinline__ bool warp_wait_ab(uint64_t* bar, uint32_t parity, Ctl* C, int32_t* status) {
-  return __all_sync(0xffffffffu, wait_ab(bar, parity, C, status));
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_ab(bar, parity, C, status);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok;
+}
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 // Row statistics in a tile-padded layout, one CTA per (tile, head): the log2-domain LSE and
@@ -202,8 +215,8 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     }
     mbar_init(&B->s_full, 1);
     mbar_init(&B->dp_full, 1);
-    mbar_init(&B->p_full, 256);
-    mbar_init(&B->ds_full, 256);
+    mbar_init(&B->p_full, 8);   // one arrival per softmax warp
+    mbar_init(&B->ds_full, 8);
     mbar_init(&B->acc_done, 2);
     mbar_init(&B->drain, 2);
     C->abort = 0;
@@ -403,7 +416,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       tmem_st32(tS + 64 * c, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&B->p_full);
+      warp_arrive(&B->p_full);
       if (!(ok = warp_wait_ab(&B->dp_full, w & 1, C, p.status))) break;
       tc_fence_after();
       auto ds_phase = [&](auto masked) {
@@ -439,7 +452,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
       tmem_st32(tDP + 64 * c, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&B->ds_full);
+      warp_arrive(&B->ds_full);
     }
     // epilogue: warpgroup c writes d columns [64 c, 64 c + 64) of this key's dV and dK rows
     if (n > 0) {
@@ -495,7 +508,7 @@ struct DqBars {
   uint64_t v_full[kDqNV], v_empty[kDqNV];
   uint64_t s_full, s_free;   // S of the current step in TMEM / read by every softmax thread
   uint64_t dp_full[2];
-  // dS of that buffer written back by all 256 softmax threads.  One barrier per buffer:
+  // dS of that buffer written back by all 8 softmax warps.  One barrier per buffer:
   // warpgroup 0 may finish step j + 1 before warpgroup 1 finishes step j, and its
   // arrivals must not complete step j's phase.
   uint64_t ds_full[2];
@@ -542,12 +555,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mbar_init(&B->v_empty[s], 1);
     }
     mbar_init(&B->s_full, 1);
-    mbar_init(&B->s_free, 256);
+    mbar_init(&B->s_free, 8);   // one arrival per softmax warp
     for (int b = 0; b < 2; b++) {
       mbar_init(&B->dp_full[b], 1);
     }
-    mbar_init(&B->ds_full[0], 256);
-    mbar_init(&B->ds_full[1], 256);
+    mbar_init(&B->ds_full[0], 8);
+    mbar_init(&B->ds_full[1], 8);
     mbar_init(&B->dq_done[0], 1);
     mbar_init(&B->dq_done[1], 1);
     mbar_init(&B->acc_done, 1);
@@ -727,7 +740,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       tmem_wait_ld();
       // S may be overwritten by the next step's S from here on
       tc_fence_before();
-      mbar_arrive(&B->s_free);
+      warp_arrive(&B->s_free);
       float P[64];
       auto p_phase = [&](auto masked) {
 #pragma unroll
@@ -795,7 +808,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       tmem_st32(tDP + 64 * c, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&B->ds_full[b]);
+      warp_arrive(&B->ds_full[b]);
     }
     // epilogue: warpgroup c writes d columns [64 c, 64 c + 64) of this row's dQ
     if (n > 0) {
