@@ -126,6 +126,29 @@ def unique_tokens(entries, num_pages, P):
 # --------------------------------------------------------------------------------------
 L2_BYTES = 129 * 2**20   # GB300 L2
 
+
+def profiled_traffic(workload, call):
+    """DRAM bytes per call of `call` from the committed ncu summary of the episode workload,
+    or None when the workload differs or a kernel source changed since the counters."""
+    import hashlib
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "dram_traffic_episode.md")
+    if workload != "episode" or not os.path.exists(path):
+        return None
+    want, got = {}, None
+    for line in open(path):
+        line = line.strip()
+        if " sha256/16: " in line:
+            name, h = line.split(" sha256/16: ")
+            want[name] = h
+        elif line.startswith(call + " bytes per call: "):
+            got = int(line.split(": ")[1])
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "packed_tree_attention_gb300", "csrc")
+    for name, h in want.items():
+        with open(os.path.join(src, name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != h:
+                return None
+    return got if want else None
+
 WORKLOAD_DESC = {
     "episode": "episode: 16K prefix, 7 branches x 32K owned tokens, 3 rewinds, 6 mounts",
     "tree_fwd": "tree: 4K prefix, 4 x 8K branches, 2 mounts",
@@ -442,7 +465,8 @@ def run_ours(args, rank, world, dist):
         "bwd_tflops": bwd_flops / (bwd_ms * 1e-3) / 1e12,
         "roofline": {"bound": "tensor", "kernel": "octo_attn_" + dom, "achieved": achieved, "peak": bf16s,
                      "unit": "TFLOP/s", "frac": achieved / bf16s, "peak_source": peak_src + " (sustained bf16)",
-                     "traffic": None},
+                     "traffic": profiled_traffic(args.workload, "octo_attn_" + dom),
+                     "traffic_unit": "bytes per call (ncu dram__bytes_read + write)"},
         "kernel_path": {"fwd": path_fwd, "bwd": path_bwd},
         "clocks": clocks,
         "gpu_launches": launches,
