@@ -373,6 +373,34 @@ def run_ours(args, rank, world, dist):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
         del hq, hdo, hk, hv, hdq, hdk, hdv, q2, do2
 
+    # ---------------- rotary embedding leg (rows of the episode plan) ----------------
+    rope = None
+    if not args.no_rope:
+        rplan = pool.pack_tree(ep.roots, 128)
+        rt = []
+
+        def rstep():
+            a, b, c = ev(), ev(), ev()
+            a.record(stream)
+            rplan.rope_rows(Hq, q, 10000.0, stream=stream)              # queries, bf16
+            b.record(stream)
+            rplan.rope_rows(Hq, dq, 10000.0, inverse=True, stream=stream)   # query gradients, fp32
+            c.record(stream)
+            rt.append((a, b, c))
+
+        timed(torch, stream, rstep, 5, 3, dist)
+        q_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in rt[3:])
+        g_ms = statistics.mean(b.elapsed_time(c) for _, b, c in rt[3:])
+        qb = 2 * q.numel() * q.element_size() + N * 4       # read + write + row positions
+        gb = 2 * dq.numel() * dq.element_size() + N * 4
+        rope = {"metric": "rotary embedding of packed rows, HBM GB/s",
+                "q_bf16": {"value": qb / (q_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": q_ms,
+                           "frac": qb / (q_ms * 1e-3) / 1e9 / hbm},
+                "dq_f32_inverse": {"value": gb / (g_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": g_ms,
+                                   "frac": gb / (g_ms * 1e-3) / 1e9 / hbm},
+                "peak": hbm, "peak_source": peak_src}
+        del rplan
+
     # free the training leg before the decode leg
     del pool, kp, vp, q, do, o, lse, dq, dk, dv, ws
     torch.cuda.empty_cache()
@@ -472,6 +500,7 @@ def run_ours(args, rank, world, dist):
         "gpu_launches": launches,
         "e2e": e2e,
         "decode": dec,
+        "rope": rope,
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -508,6 +537,7 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="episode")
+    ap.add_argument("--no-rope", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")

@@ -204,6 +204,39 @@ int octo_plan_copy_out(octo_plan_t plan, int32_t* seg_order, int32_t* seg_row_ba
  * plan on any other stream must have completed. */
 int octo_plan_destroy(octo_plan_t plan);
 
+/* ---- rotary position embedding at the packed positions ----
+ * Octopus project page, "Architecture & Co-Design" item 02 and the cross-branch sharing
+ * table: mounted sibling keys are read rotation-free (as stored) under the monotonic
+ * offset s = max(p_B, e_A + 1); only the reader's positions jump.  Without the jump a
+ * longer sibling's keys would sit at or after the reader's queries ("RoPE flip").  So keys
+ * are rotated once, when appended, at the position the pool gives each token, and queries
+ * at the position of their packed row.  Rotation, half-split form: for a head vector x of
+ * dimension d at position p and i < d/2, (x_i, x_{i+d/2}) turns by the angle
+ * p * base^(-2i/d), formed and reduced modulo 2 pi in double precision.  head_dim must be
+ * even and at most 128; base > 0 and finite (EINVAL otherwise). */
+
+/* octo_append with each K row rotated at the position its token receives (V copied as
+ * is); same pages, positions, zeroing and errors as octo_append. */
+int octo_append_rope(octo_pool_t pool, octo_cursor_t cur, int32_t n, const void* k, const void* v,
+                     float base, void* stream, int32_t* pos_out);
+
+/* Rotates in place x [n_rows][n_heads][head_dim] (dtype OCTO_DTYPE_BF16 or
+ * OCTO_DTYPE_F32, device) in the plan's packed row order, each row at its position: a
+ * pack plan's rows, or a decode plan's one row per cursor (its newest token).  inverse = 0
+ * before attention (queries); inverse = 1 turns back, mapping the gradient with respect
+ * to the rotated rows (octo_attn_bwd's dq) to the gradient with respect to the rows as
+ * given.  Async on stream. */
+int octo_rope_rows(octo_plan_t plan, int32_t n_heads, void* x, int32_t dtype, float base,
+                   int32_t inverse, void* stream);
+
+/* Turns key gradients from octo_attn_bwd (fp32, pool-shaped [num_pages][n_kv_heads]
+ * [page_size][head_dim]) back through the append rotation: every slot of every page the
+ * plan reads, at its token's position, with the inverse rotation; slots holding no token
+ * and pages the plan does not read are left as they are.  dv needs nothing (V is not
+ * rotated).  Uploads a host-built table of slot positions and waits for the stream before
+ * returning. */
+int octo_rope_pool_grad(octo_plan_t plan, float* dk_pool, float base, void* stream);
+
 /* ---- attention (device, async on stream) ---- */
 
 /* Forward over a packed plan.  For query head h the kv head is h / (n_q_heads /

@@ -76,6 +76,7 @@ def _load():
         L.orc_token_owner.argtypes = [P, IP, IP]
         L.orc_num_tokens.argtypes = [P]
         L.orc_set_kv.argtypes = [P, I, IP, DP, DP]
+        L.orc_rope.argtypes = [DP, I, I, I, IP, ctypes.c_double, I]
         _lib = L
     return _lib
 
@@ -175,7 +176,9 @@ class Oracle:
 
     # -- replay of a synth.Episode op log with its K/V rows (append order) --
     def replay(self, ep, K=None, V=None):
+        """Returns every appended token's position, in append order."""
         t = 0
+        positions = []
         for op in ep.ops:
             kind = op[0]
             if kind == "root":
@@ -184,7 +187,7 @@ class Oracle:
                 _, c, n = op
                 k = None if K is None else K[t:t + n]
                 v = None if V is None else V[t:t + n]
-                self.append(c, n, k, v)
+                positions.extend(self.append(c, n, k, v).tolist())
                 t += n
             elif kind == "fork":
                 self.fork(op[1], op[2])
@@ -200,6 +203,7 @@ class Oracle:
                 self.unpin(op[1])
             else:
                 raise ValueError(kind)
+        return np.array(positions, dtype=np.int32)
 
     # -- queries --
     @property
@@ -344,3 +348,16 @@ class OraclePlan:
         src = np.zeros(max(n, 1), dtype=np.int32)
         self.orc._L.orc_row_context(self.h, r, _ip(tok), _ip(src), n)
         return tok[:n], src[:n]
+
+
+def rope(x, pos, base, inverse=False):
+    """Rotary embedding of x [n][H][d] (any float array; returned as a new fp64 array),
+    row t at position pos[t] (orc_rope)."""
+    L = _load()
+    y = np.ascontiguousarray(np.array(x, dtype=np.float64))
+    n, H, d = y.shape
+    p = np.ascontiguousarray(np.asarray(pos, dtype=np.int32))
+    assert p.shape == (n,)
+    if L.orc_rope(_dp(y), n, H, d, _ip(p), float(base), 1 if inverse else 0):
+        raise ValueError("orc_rope: bad arguments")
+    return y

@@ -24,6 +24,10 @@
 //   * e_A is the exclusive end of the span in positions: pos(A, b-1) + 1;
 //   * rewind(k) on segment S makes a continuation child at k; S's tail stays.
 //
+//   * rotary embedding (the "RoPE flip" of unshifted zero-copy KV in the cross-branch
+//     sharing table; mounted keys are rotation-free): the half-split rotation, pair
+//     (i, i + d/2) turned by pos * base^(-2i/d).  A plain loop below, orc_rope.
+//
 // Every value here is computed the direct way: each row's context is materialised as
 // an explicit list of (token, source), and attention is a dense loop over that list.
 // The tile list is derived by brute force from the materialised visibility, not from a
@@ -785,5 +789,24 @@ void orc_token_owner(void* h, int* seg, int* idx) {
   std::copy(o->tok_idx.begin(), o->tok_idx.end(), idx);
 }
 int orc_num_tokens(void* h) { return (int)static_cast<Oracle*>(h)->tok_seg.size(); }
+
+// Rotary embedding of x [n][H][d] (fp64, in place): row t at position pos[t]; for each
+// head and i < d/2 the pair (x_i, x_{i+d/2}) is multiplied by the 2x2 rotation through
+// theta = pos * base^(-2i/d) (inverse != 0: through -theta).
+int orc_rope(double* x, int n, int H, int d, const int* pos, double base, int inverse) {
+  if (d < 2 || d % 2 != 0 || base <= 0) return 1;
+  const int half = d / 2;
+  for (int t = 0; t < n; t++)
+    for (int h = 0; h < H; h++)
+      for (int i = 0; i < half; i++) {
+        const double theta = (double)pos[t] * std::pow(base, -2.0 * i / d) * (inverse ? -1.0 : 1.0);
+        const double c = std::cos(theta), s = std::sin(theta);
+        double* row = x + ((size_t)t * H + h) * d;
+        const double a = row[i], b = row[i + half];
+        row[i] = c * a - s * b;
+        row[i + half] = s * a + c * b;
+      }
+  return 0;
+}
 
 }  // extern "C"

@@ -66,7 +66,8 @@ SYMBOLS = ("octo_pool_create", "octo_pool_destroy", "octo_root", "octo_append", 
            "octo_pack_tree", "octo_decode_plan", "octo_plan_info", "octo_plan_copy_out", "octo_plan_destroy",
            "octo_attn_fwd", "octo_attn_bwd_workspace_size", "octo_attn_bwd", "octo_decode_workspace_size",
            "octo_decode", "octo_strerror", "octo_last_cuda_error", "octo_sync", "octo_kernel_path",
-           "octo_launch_count", "octo_decode_noalloc")
+           "octo_launch_count", "octo_decode_noalloc", "octo_append_rope", "octo_rope_rows",
+           "octo_rope_pool_grad")
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
@@ -111,6 +112,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "octo_kernel_path": [P, I32, I32],
         "octo_launch_count": [],
         "octo_decode_noalloc": [P, I32, P, P, P, P, P, F, P],
+        "octo_append_rope": [P, I32, I32, P, P, F, P, IP],
+        "octo_rope_rows": [P, I32, P, I32, F, I32, P],
+        "octo_rope_pool_grad": [P, P, F, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -188,6 +192,15 @@ class Pool:
         if not check:
             return st
         _chk(st, "octo_append")
+        return pos[:n]
+
+    def append_rope(self, cur, n, k, v, base, stream=None, check=True):
+        """octo_append_rope: append with the K rows rotated at the positions they receive."""
+        pos = np.zeros(max(n, 1), dtype=np.int32)
+        st = self._L.octo_append_rope(self.h, cur, n, _ptr(k), _ptr(v), float(base), _stream(stream), _ip(pos))
+        if not check:
+            return st
+        _chk(st, "octo_append_rope")
         return pos[:n]
 
     def fork(self, cur, n, check=True):
@@ -330,6 +343,16 @@ class Plan:
         cannot allocate device memory (its partials use the library's static scratch)."""
         _chk(self._L.octo_decode_noalloc(self.h, n_q_heads, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(out),
                                          _ptr(lse), float(scale), _stream(stream)), "octo_decode_noalloc")
+
+    def rope_rows(self, n_heads, x, base, inverse=False, stream=None):
+        """octo_rope_rows: rotate the plan's packed rows of x (bf16 or fp32) in place."""
+        dt = DTYPE_F32 if x.element_size() == 4 else DTYPE_BF16
+        _chk(self._L.octo_rope_rows(self.h, n_heads, _ptr(x), dt, float(base), 1 if inverse else 0, _stream(stream)),
+             "octo_rope_rows")
+
+    def rope_pool_grad(self, dk_pool, base, stream=None):
+        """octo_rope_pool_grad: key gradients back through the append rotation."""
+        _chk(self._L.octo_rope_pool_grad(self.h, _ptr(dk_pool), float(base), _stream(stream)), "octo_rope_pool_grad")
 
     def sync(self, stream=None):
         _chk(self._L.octo_sync(self.h, _stream(stream)), "octo_sync")

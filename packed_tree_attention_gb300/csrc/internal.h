@@ -126,6 +126,10 @@ inline int cuda_status(cudaError_t e) {
 int launch_zero_pages(const octo_pool_desc& d, const int32_t* d_pages, int32_t n, cudaStream_t s);
 int launch_append_rows(const octo_pool_desc& d, const int32_t* d_dst_rows, int32_t n, const void* k,
                        const void* v, cudaStream_t s);
+// rotary embedding (rope.cu): K rotated at each appended token's position while copied
+int rope_validate(int32_t head_dim, float base);
+int launch_append_rope(const octo_pool_desc& d, const int32_t* d_dst_rows, const int32_t* d_pos, int32_t n,
+                       const void* k, const void* v, float base, cudaStream_t s);
 
 // plan compilation (compile.cu)
 int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t* seg_order, int32_t n_segs,

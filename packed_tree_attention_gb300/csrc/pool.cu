@@ -205,11 +205,13 @@ int octo_root(octo_pool_t p, octo_cursor_t* out) {
   return OCTO_OK;
 }
 
-int octo_append(octo_pool_t p, octo_cursor_t c, int32_t n, const void* k, const void* v, void* stream,
-                int32_t* pos_out) {
+// Appends n tokens; with `rope` the K rows are rotated at their positions on the way in.
+static int append_impl(octo_pool_t p, octo_cursor_t c, int32_t n, const void* k, const void* v, void* stream,
+                       int32_t* pos_out, bool rope, float base) {
   if (!p || n < 0 || c < 0 || c >= (int32_t)p->segs.size()) return OCTO_EINVAL;
   if (!writable(p, c)) return OCTO_ESTATE;
   if ((k == nullptr) != (v == nullptr)) return OCTO_EINVAL;
+  if (rope && octo::rope_validate(p->desc.head_dim, base)) return OCTO_EINVAL;
   Segment& g = p->segs[c];
   const int32_t P = p->desc.page_size;
   int64_t need = ((int64_t)g.len + n + P - 1) / P - (int64_t)g.pages.size();
@@ -222,11 +224,17 @@ int octo_append(octo_pool_t p, octo_cursor_t c, int32_t n, const void* k, const 
     p->free_pages.erase(it);
   }
   std::vector<int32_t> newp(g.pages.end() - need, g.pages.end());
-  std::vector<int32_t> dst;
-  if (k) dst.resize(n);
+  std::vector<int32_t> dst, pos;
+  if (k) {
+    dst.resize(n);
+    pos.resize(n);
+  }
   for (int32_t i = 0; i < n; i++) {
     int32_t idx = g.len + i;
-    if (k) dst[i] = g.pages[idx / P] * P + idx % P;
+    if (k) {
+      dst[i] = g.pages[idx / P] * P + idx % P;
+      pos[i] = g.p_next;
+    }
     if (pos_out) pos_out[i] = g.p_next;
     g.pos.push_back(g.p_next++);
   }
@@ -240,17 +248,30 @@ int octo_append(octo_pool_t p, octo_cursor_t c, int32_t n, const void* k, const 
     cudaStream_t s = (cudaStream_t)stream;
     std::vector<int32_t> host(newp);
     host.insert(host.end(), dst.begin(), dst.end());
+    if (rope) host.insert(host.end(), pos.begin(), pos.end());
     int32_t* d_buf = nullptr;
     OCTO_CUDA(cudaMallocAsync((void**)&d_buf, sizeof(int32_t) * host.size(), s));
     OCTO_CUDA(cudaMemcpyAsync(d_buf, host.data(), sizeof(int32_t) * host.size(), cudaMemcpyHostToDevice, s));
     int st = zero ? octo::launch_zero_pages(p->desc, d_buf, (int32_t)newp.size(), s) : OCTO_OK;
-    if (st == OCTO_OK && k && n > 0) st = octo::launch_append_rows(p->desc, d_buf + newp.size(), n, k, v, s);
+    if (st == OCTO_OK && k && n > 0)
+      st = rope ? octo::launch_append_rope(p->desc, d_buf + newp.size(), d_buf + newp.size() + n, n, k, v, base, s)
+                : octo::launch_append_rows(p->desc, d_buf + newp.size(), n, k, v, s);
     OCTO_CUDA(cudaFreeAsync(d_buf, s));
     // the host vector is pageable: make sure the copy has consumed it
     OCTO_CUDA(cudaStreamSynchronize(s));
     if (st != OCTO_OK) return st;
   }
   return OCTO_OK;
+}
+
+int octo_append(octo_pool_t p, octo_cursor_t c, int32_t n, const void* k, const void* v, void* stream,
+                int32_t* pos_out) {
+  return append_impl(p, c, n, k, v, stream, pos_out, false, 0.f);
+}
+
+int octo_append_rope(octo_pool_t p, octo_cursor_t c, int32_t n, const void* k, const void* v, float base,
+                     void* stream, int32_t* pos_out) {
+  return append_impl(p, c, n, k, v, stream, pos_out, true, base);
 }
 
 int octo_fork(octo_pool_t p, octo_cursor_t c, int32_t n, octo_cursor_t* out) {

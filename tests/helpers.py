@@ -43,15 +43,22 @@ def replay_host(pool, ep):
             pool.unpin(op[1])
 
 
-def replay_device(pool, ep, K_dev, V_dev, stream=None):
+def replay_device(pool, ep, K_dev, V_dev, stream=None, rope_base=None):
     """Replays the op log into a library pool, appending each token's K/V rows from
-    device tensors K_dev/V_dev [T, Hkv, d] (append order)."""
+    device tensors K_dev/V_dev [T, Hkv, d] (append order); with rope_base the K rows are
+    rotated at their positions on the way in (octo_append_rope).  Returns the positions
+    the pool gave the tokens, in append order."""
     t = 0
+    positions = []
     for op in ep.ops:
         k = op[0]
         if k == "append":
             _, c, n = op
-            pool.append(c, n, K_dev[t:t + n], V_dev[t:t + n], stream=stream)
+            if rope_base is None:
+                positions.extend(pool.append(c, n, K_dev[t:t + n], V_dev[t:t + n], stream=stream).tolist())
+            else:
+                positions.extend(pool.append_rope(c, n, K_dev[t:t + n], V_dev[t:t + n], rope_base,
+                                                  stream=stream).tolist())
             t += n
         elif k == "root":
             pool.root()
@@ -67,6 +74,7 @@ def replay_device(pool, ep, K_dev, V_dev, stream=None):
             pool.release(op[1])
         elif k == "unpin":
             pool.unpin(op[1])
+    return np.array(positions, dtype=np.int32)
 
 
 def compare_pools(pool, orc):
