@@ -56,16 +56,61 @@ __device__ __forceinline__ void st(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 // One block per row: the row's d/2 (cos, sin) pairs once, then every head.  sgn = -1 turns
-// the other way (the inverse rotation, for gradients).
+// the other way (the inverse rotation, for gradients).  Each thread takes 4 consecutive
+// pairs (8- or 16-byte loads from both halves) when d/2 is a multiple of 4 and x is
+// 16-byte aligned.
+template <typename T>
+struct Vec4;
+template <>
+struct Vec4<float> {
+  using type = float4;
+  __device__ static void unpack(const float4& v, float (&f)[4]) { f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w; }
+  __device__ static float4 pack(const float (&f)[4]) { return make_float4(f[0], f[1], f[2], f[3]); }
+};
+template <>
+struct Vec4<__nv_bfloat16> {
+  using type = uint2;
+  __device__ static void unpack(const uint2& v, float (&f)[4]) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  }
+  __device__ static uint2 pack(const float (&f)[4]) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]), b = __floats2bfloat162_rn(f[2], f[3]);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  }
+};
+
 template <typename T>
 __global__ void k_rope_rows(T* __restrict__ x, const int32_t* __restrict__ row_pos, int32_t H, RopeFreq f,
-                            float sgn) {
+                            float sgn, bool vec) {
   __shared__ float cs[64][2];
   const int64_t row = blockIdx.x;
   const int32_t half = f.half, d = 2 * half;
   if (threadIdx.x < half) rope_cs(row_pos[row], f.inv[threadIdx.x], cs[threadIdx.x][0], cs[threadIdx.x][1]);
   __syncthreads();
   T* xr = x + row * H * d;
+  if (vec) {
+    using V = typename Vec4<T>::type;
+    const int32_t q4 = half / 4;
+    for (int32_t e = threadIdx.x; e < H * q4; e += blockDim.x) {
+      const int32_t h = e / q4, i0 = (e % q4) * 4;
+      V* pa = reinterpret_cast<V*>(xr + (size_t)h * d + i0);
+      V* pb = reinterpret_cast<V*>(xr + (size_t)h * d + i0 + half);
+      float a[4], b[4], ya[4], yb[4];
+      Vec4<T>::unpack(*pa, a);
+      Vec4<T>::unpack(*pb, b);
+#pragma unroll
+      for (int t = 0; t < 4; t++) {
+        const float c = cs[i0 + t][0], s = sgn * cs[i0 + t][1];
+        ya[t] = a[t] * c - b[t] * s;
+        yb[t] = b[t] * c + a[t] * s;
+      }
+      *pa = Vec4<T>::pack(ya);
+      *pb = Vec4<T>::pack(yb);
+    }
+    return;
+  }
   for (int32_t e = threadIdx.x; e < H * half; e += blockDim.x) {
     const int32_t h = e / half, i = e % half;
     T* p = xr + (size_t)h * d + i;
@@ -153,10 +198,12 @@ int octo_rope_rows(octo_plan_t plan, int32_t n_heads, void* x, int32_t dtype, fl
   cudaStream_t s = (cudaStream_t)stream;
   plan->last_stream = s;
   const float sgn = inverse ? -1.f : 1.f;
+  const bool vec = (f.half % 4) == 0 && ((uintptr_t)x % 16) == 0;
   if (dtype == OCTO_DTYPE_F32)
-    octo::k_rope_rows<float><<<(unsigned)N, 256, 0, s>>>((float*)x, plan->row_pos, n_heads, f, sgn);
+    octo::k_rope_rows<float><<<(unsigned)N, 256, 0, s>>>((float*)x, plan->row_pos, n_heads, f, sgn, vec);
   else
-    octo::k_rope_rows<__nv_bfloat16><<<(unsigned)N, 256, 0, s>>>((__nv_bfloat16*)x, plan->row_pos, n_heads, f, sgn);
+    octo::k_rope_rows<__nv_bfloat16><<<(unsigned)N, 256, 0, s>>>((__nv_bfloat16*)x, plan->row_pos, n_heads, f, sgn,
+                                                                 vec);
   octo::count_launch();
   return octo::cuda_status(cudaGetLastError());
 }
