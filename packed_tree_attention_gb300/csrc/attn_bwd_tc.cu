@@ -51,7 +51,6 @@ struct BwdParams {
   const octo_entry* entries;
   const int32_t* csc_perm;
   const int32_t* page_off;
-  const int32_t* page_order;
   const int32_t* pair_pages;
   const int32_t* pair_item_off;
   const int32_t* pair_n_items;
@@ -901,7 +900,6 @@ int bwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const
   prm.entries = p->entries;
   prm.csc_perm = p->csc_perm;
   prm.page_off = p->page_off;
-  prm.page_order = p->page_order;
   prm.pair_pages = p->pair_pages;
   prm.pair_item_off = p->pair_item_off;
   prm.pair_n_items = p->pair_n_items;

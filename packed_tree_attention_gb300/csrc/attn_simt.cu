@@ -298,27 +298,6 @@ int bwd_simt_t(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, c
 
 }  // namespace
 
-int bwd_pre_launch(const octo_plan_s* p, int32_t Hq, const void* o, const void* dout, float* Dv, cudaStream_t s) {
-  const int64_t N = p->info.n_rows;
-  if (N == 0) return OCTO_OK;
-  const int64_t warps = N * Hq;
-  const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
-  if (p->pool->desc.dtype == OCTO_DTYPE_F32) {
-    if (p->pool->desc.head_dim == 64)
-      k_bwd_pre<float, 64><<<grid, 256, 0, s>>>((const float*)o, (const float*)dout, Dv, N, Hq);
-    else
-      k_bwd_pre<float, 128><<<grid, 256, 0, s>>>((const float*)o, (const float*)dout, Dv, N, Hq);
-  } else {
-    if (p->pool->desc.head_dim == 64)
-      k_bwd_pre<__nv_bfloat16, 64><<<grid, 256, 0, s>>>((const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, Dv, N, Hq);
-    else
-      k_bwd_pre<__nv_bfloat16, 128><<<grid, 256, 0, s>>>((const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, Dv, N,
-                                                         Hq);
-  }
-  count_launch();
-  return cuda_status(cudaGetLastError());
-}
-
 int fwd_simt(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const void* v, void* o, float* lse,
              float scale, bool decode, cudaStream_t s) {
   const octo_pool_desc& d = p->pool->desc;

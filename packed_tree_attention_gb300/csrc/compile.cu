@@ -685,25 +685,22 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
     count_launch();
   }
   OCTO_TRY(cuda_status(cudaGetLastError()));
-  // ---- launch orders: heaviest tiles / pages first (longest-processing-time first) ----
+  // ---- launch orders: heaviest tiles / page pairs first (longest-processing-time first) ----
   {
     std::vector<int32_t> toff(n_tiles + 1), poff((size_t)pl->num_pages + 1);
     OCTO_TRY(cuda_status(cudaMemcpyAsync(toff.data(), pl->tile_off, (n_tiles + 1) * 4, cudaMemcpyDeviceToHost, s)));
     OCTO_TRY(cuda_status(
         cudaMemcpyAsync(poff.data(), pl->page_off, ((size_t)pl->num_pages + 1) * 4, cudaMemcpyDeviceToHost, s)));
     OCTO_TRY(cuda_status(cudaStreamSynchronize(s)));
-    std::vector<int32_t> tord(n_tiles), pord;
+    std::vector<int32_t> tord(n_tiles);
     for (int64_t t = 0; t < n_tiles; t++) tord[t] = (int32_t)t;
     std::stable_sort(tord.begin(), tord.end(),
                      [&](int32_t a, int32_t b) { return toff[a + 1] - toff[a] > toff[b + 1] - toff[b]; });
-    for (int32_t pg = 0; pg < pl->num_pages; pg++)
-      if (poff[pg + 1] > poff[pg]) pord.push_back(pg);
-    std::stable_sort(pord.begin(), pord.end(),
-                     [&](int32_t a, int32_t b) { return poff[a + 1] - poff[a] > poff[b + 1] - poff[b]; });
+    const bool any_touched = pl->info.n_touched_pages > 0;
     // dK/dV work units: consecutive own pages of each segment, two at a time, among the
     // touched pages; a touched page without a touched partner runs alone
-    if (!is_decode && !pord.empty()) {
-      std::vector<int32_t> pp, pub;
+    if (!is_decode && any_touched) {
+      std::vector<int32_t> pp;
       std::vector<char> seen((size_t)pl->num_pages, 0);
       auto cnt = [&](int32_t pg) { return pg < 0 ? 0 : poff[pg + 1] - poff[pg]; };
       for (const Segment& g : pool->segs) {
@@ -752,12 +749,8 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
       OCTO_TRY(cuda_status(cudaGetLastError()));
     }
     OCTO_TRY(dalloc(pl, &pl->tile_order, n_tiles, s));
-    OCTO_TRY(dalloc(pl, &pl->page_order, pord.size(), s));
     if (n_tiles > 0)
       OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->tile_order, tord.data(), n_tiles * 4, cudaMemcpyHostToDevice, s)));
-    if (!pord.empty())
-      OCTO_TRY(
-          cuda_status(cudaMemcpyAsync(pl->page_order, pord.data(), pord.size() * 4, cudaMemcpyHostToDevice, s)));
     // decode plans: split each cursor's entries into runs of kSplitEntries
     std::vector<int32_t> sp_tile, sp_e0, sp_e1, sp_order, cur0(n_tiles + 1, 0);
     if (is_decode) {

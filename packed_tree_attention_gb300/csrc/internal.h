@@ -84,7 +84,6 @@ struct octo_plan_s {
   int32_t* page_off = nullptr;       // [num_pages+1]
   int32_t* touched = nullptr;        // [n_touched_pages] pages with >= 1 entry, ascending
   int32_t* tile_order = nullptr;     // [n_tiles] tiles by descending entry count (scheduling)
-  int32_t* page_order = nullptr;     // [n_touched] touched pages by descending entry count
   // dK/dV work units: pairs of consecutive own pages of a segment (second -1: one page)
   int32_t n_pairs = 0;
   int32_t* pair_pages = nullptr;     // [2 n_pairs]
