@@ -463,6 +463,31 @@ def run_ours(args, rank, world, dist):
         del dpool, dkp, dvp
         torch.cuda.empty_cache()
 
+    # ---------------- cursor view: the context of one 128K-token cursor ----------------
+    view = None
+    if not args.no_decode:
+        vpool = pta.Pool(2112, 64, Hkv, d, pta.DTYPE_BF16)    # metadata only: no K/V arrays
+        r0 = vpool.root()
+        vpool.append(r0, 16384)
+        kids = vpool.fork(r0, 2)
+        vpool.append(kids[0], 8192)
+        vpool.append(kids[1], 16384)
+        vpool.mount(kids[1], kids[0], 1024, 8192)          # a sibling span read in place
+        vpool.append(kids[1], 131072 - 16384 - 16384 - 7168)
+        vt = []
+        for i in range(8):
+            a, b = ev(), ev()
+            a.record(stream)
+            vp_ = vpool.decode_plan([kids[1]], stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            vt.append(a.elapsed_time(b))
+            ctx = vp_.info["pairs"]
+            del vp_
+        view = {"metric": "cursor view (context runs of one cursor, via the decode plan)",
+                "context_tokens": int(ctx), "ms": statistics.median(vt[2:])}
+        del vpool
+
     # ---------------- CPU baseline (rank 0, N = 1) ----------------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -501,6 +526,7 @@ def run_ours(args, rank, world, dist):
         "e2e": e2e,
         "decode": dec,
         "rope": rope,
+        "cursor_view": view,
         "cpu_baseline": cpu,
     }
     if rank == 0:
