@@ -154,6 +154,8 @@ WORKLOAD_DESC = {
     "tree_fwd": "tree: 4K prefix, 4 x 8K branches, 2 mounts",
     "train_step": "train step: 8 trees of ~140K owned tokens, fan-out 2-6, depth <= 3, mounts",
     "tiny": "tiny: 64-token prefix, 2 x 32 branches, 1 mount",
+    "decode": "paged decode: 32 episodes x 8 cursors, shared prefix 2-8K, paths 8-32K, 0-3 sibling mounts of 0.5-8K",
+    "decode_small": "paged decode: 4 episodes x 8 cursors, shared prefix 2-8K, paths 8-32K, 0-3 sibling mounts",
 }
 
 
@@ -269,6 +271,72 @@ def timed(torch, stream, fn, steps, warmup, dist=None):
     return t_all0.elapsed_time(t_all1), times
 
 
+def decode_leg(pta, torch, name, seed, dev, stream, steps, warmup, world, dist, hbm, peak_src):
+    """Paged decode of the cursors of decode workload `name`: kernel-only GB/s of the
+    algorithmic bytes (unique visible K/V tokens + queries, outputs, plan), then plan +
+    decode."""
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    cfg = synth.CONFIGS[name]
+    Hq, Hkv, d, P = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["P"]
+    scale = 1.0 / math.sqrt(d)
+    dep, dpool, dkp, dvp, dcfg = build_episode(pta, torch, name, seed, dev)
+    curs = dep.cursors
+    n = len(curs)
+    qd = synth.hash_fill(synth.STREAM_DECODE_Q + 16 * seed, (n, Hq, d), torch.bfloat16, dev, 0.5)
+    od = torch.empty_like(qd)
+    ld = torch.empty((n, Hq), dtype=torch.float32, device=dev)
+    dplan = dpool.decode_plan(curs)
+    wsn = dplan.decode_workspace_size(Hq)
+    wsd = torch.empty(max(1, wsn), dtype=torch.uint8, device=dev)
+    ent = dplan.copy_out()["entries"]
+    uniq = unique_tokens(ent, dpool.num_pages, P)
+    logical = int((ent["kv_hi"].astype(np.int64) - ent["kv_lo"]).sum())
+    tok_bytes = 2 * Hkv * d * 2
+    alg_bytes = uniq * tok_bytes + 2 * qd.numel() * 2 + ld.numel() * 4 + len(ent) * 24
+    # timed: the decode kernel alone (plan reused), then plan + decode
+    dec_times = []
+
+    def dstep():
+        a, b = ev(), ev()
+        a.record(stream)
+        dplan.decode(Hq, qd, od, ld, scale, wsd, wsn, stream=stream)
+        b.record(stream)
+        dec_times.append((a, b))
+
+    dl0 = pta.launch_count()
+    dclk = ClockSampler(dev.index)
+    dclk.start()
+    dtot, _ = timed(torch, stream, dstep, steps, warmup, dist)
+    dclocks = dclk.stop()
+    dlaunch = pta.launch_count() - dl0
+    kern_ms = statistics.mean([a.elapsed_time(b) for a, b in dec_times[warmup:]])
+    plan_ms_list = []
+
+    def pstep():
+        a, b = ev(), ev()
+        a.record(stream)
+        p2 = dpool.decode_plan(curs, stream)
+        p2.decode(Hq, qd, od, ld, scale, wsd, wsn, stream=stream)
+        b.record(stream)
+        plan_ms_list.append((a, b, p2))
+
+    timed(torch, stream, pstep, 3, 1, dist)
+    full_ms = statistics.mean([a.elapsed_time(b) for a, b, _ in plan_ms_list[1:]])
+    world_bytes = world * alg_bytes
+    dec = {"metric": "paged decode HBM GB/s", "value": world_bytes / (kern_ms * 1e-3) / 1e9, "unit": "GB/s",
+           "workload": WORKLOAD_DESC[name] + "; 16q/4kv heads, d=128, page 64, bf16",
+           "ms_per_step": kern_ms, "ms_per_step_with_plan": full_ms,
+           "cursors": n, "unique_kv_tokens": uniq, "logical_kv_tokens": logical,
+           "algorithmic_bytes": alg_bytes, "logical_bytes": logical * tok_bytes,
+           "roofline": {"bound": "hbm", "achieved": alg_bytes / (kern_ms * 1e-3) / 1e9, "peak": hbm,
+                        "unit": "GB/s", "frac": alg_bytes / (kern_ms * 1e-3) / 1e9 / hbm,
+                        "peak_source": peak_src, "traffic": None},
+           "gpu_launches": dlaunch, "clocks": dclocks, "kernel_path": dplan.kernel_path(Hq, 2)}
+    del dpool, dkp, dvp
+    torch.cuda.empty_cache()
+    return dec
+
+
 def run_ours(args, rank, world, dist):
     import torch
     import packed_tree_attention_gb300 as pta
@@ -278,6 +346,19 @@ def run_ours(args, rank, world, dist):
     stream = torch.cuda.current_stream()
     hbm, bf16, bf16s, peak_src = peaks()
     seed = rank_seed(args.seed, rank)
+
+    if args.decode_only:
+        dec = decode_leg(pta, torch, args.decode_workload, seed, dev, stream, args.decode_steps, args.warmup,
+                         world, dist, hbm, peak_src)
+        if rank == 0:
+            print(json.dumps({"metric": dec["metric"], "value": dec["value"], "unit": dec["unit"], "n_gpus": world,
+                              "steps": args.decode_steps, "warmup": args.warmup, "ms_per_step": dec["ms_per_step"],
+                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                              "data": "synthetic (counter-based generator, seed %d + rank)" % args.seed,
+                              "config": {"workload": dec["workload"],
+                                         "l2": "K/V read larger than L2 (%d MB unique)" % (dec["algorithmic_bytes"] // 10**6)},
+                              "decode": dec}))
+        return
 
     # ---------------- training leg: episode fwd + bwd ----------------
     ep, pool, kp, vp, cfg = build_episode(pta, torch, args.workload, seed, dev)
@@ -408,60 +489,8 @@ def run_ours(args, rank, world, dist):
     # ---------------- decode leg ----------------
     dec = None
     if not args.no_decode:
-        dep, dpool, dkp, dvp, dcfg = build_episode(pta, torch, "decode", seed, dev)
-        curs = dep.cursors
-        n = len(curs)
-        qd = synth.hash_fill(synth.STREAM_DECODE_Q + 16 * seed, (n, Hq, d), torch.bfloat16, dev, 0.5)
-        od = torch.empty_like(qd)
-        ld = torch.empty((n, Hq), dtype=torch.float32, device=dev)
-        dplan = dpool.decode_plan(curs)
-        wsn = dplan.decode_workspace_size(Hq)
-        wsd = torch.empty(max(1, wsn), dtype=torch.uint8, device=dev)
-        ent = dplan.copy_out()["entries"]
-        uniq = unique_tokens(ent, dpool.num_pages, P)
-        logical = int((ent["kv_hi"].astype(np.int64) - ent["kv_lo"]).sum())
-        tok_bytes = 2 * Hkv * d * 2
-        alg_bytes = uniq * tok_bytes + 2 * qd.numel() * 2 + ld.numel() * 4 + len(ent) * 24
-        # timed: the decode kernel alone (plan reused), then plan + decode
-        dec_times = []
-
-        def dstep():
-            a, b = ev(), ev()
-            a.record(stream)
-            dplan.decode(Hq, qd, od, ld, scale, wsd, wsn, stream=stream)
-            b.record(stream)
-            dec_times.append((a, b))
-
-        dl0 = pta.launch_count()
-        dclk = ClockSampler(dev.index)
-        dclk.start()
-        dtot, _ = timed(torch, stream, dstep, args.decode_steps, args.warmup, dist)
-        dclocks = dclk.stop()
-        dlaunch = pta.launch_count() - dl0
-        kern_ms = statistics.mean([a.elapsed_time(b) for a, b in dec_times[args.warmup:]])
-        plan_ms_list = []
-
-        def pstep():
-            a, b = ev(), ev()
-            a.record(stream)
-            p2 = dpool.decode_plan(curs, stream)
-            p2.decode(Hq, qd, od, ld, scale, wsd, wsn, stream=stream)
-            b.record(stream)
-            plan_ms_list.append((a, b, p2))
-
-        timed(torch, stream, pstep, 3, 1, dist)
-        full_ms = statistics.mean([a.elapsed_time(b) for a, b, _ in plan_ms_list[1:]])
-        world_bytes = world * alg_bytes
-        dec = {"metric": "paged decode HBM GB/s", "value": world_bytes / (kern_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "ms_per_step": kern_ms, "ms_per_step_with_plan": full_ms,
-               "cursors": n, "unique_kv_tokens": uniq, "logical_kv_tokens": logical,
-               "algorithmic_bytes": alg_bytes, "logical_bytes": logical * tok_bytes,
-               "roofline": {"bound": "hbm", "achieved": alg_bytes / (kern_ms * 1e-3) / 1e9, "peak": hbm,
-                            "unit": "GB/s", "frac": alg_bytes / (kern_ms * 1e-3) / 1e9 / hbm,
-                            "peak_source": peak_src, "traffic": None},
-               "gpu_launches": dlaunch, "clocks": dclocks, "kernel_path": dplan.kernel_path(Hq, 2)}
-        del dpool, dkp, dvp
-        torch.cuda.empty_cache()
+        dec = decode_leg(pta, torch, args.decode_workload, seed, dev, stream, args.decode_steps, args.warmup,
+                         world, dist, hbm, peak_src)
 
     # ---------------- cursor view: the context of one 128K-token cursor ----------------
     view = None
@@ -567,6 +596,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--decode-only", action="store_true", help="only the decode leg (profiling runs)")
+    ap.add_argument("--decode-workload", default="decode", help="decode or decode_small (32 cursors)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=8.0)

@@ -337,6 +337,13 @@ __global__ void k_csc_scatter(const octo_entry* __restrict__ entries, int64_t n,
 }
 
 // one block per touched page: sort its CSC slice ascending (bitonic in shared memory)
+// kv_page of the first entry of each split (decode plans)
+__global__ void k_split_first_page(const octo_entry* __restrict__ entries, const int32_t* __restrict__ split_e0,
+                                   int32_t n, int32_t* __restrict__ out) {
+  const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = (int32_t)entries[split_e0[i]].kv_page;
+}
+
 __global__ void k_csc_sort(const int32_t* __restrict__ touched, const int32_t* __restrict__ page_off,
                            int32_t* __restrict__ csc, int32_t cap) {
   extern __shared__ int32_t sm[];
@@ -754,21 +761,15 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
     // decode plans: split each cursor's entries into runs of kSplitEntries
     std::vector<int32_t> sp_tile, sp_e0, sp_e1, sp_order, cur0(n_tiles + 1, 0);
     if (is_decode) {
-      int32_t max_k = 0;
       for (int64_t t = 0; t < n_tiles; t++) {
         cur0[t] = (int32_t)sp_tile.size();
-        int32_t k = 0;
-        for (int32_t e = toff[t]; e < toff[t + 1]; e += kSplitEntries, k++) {
+        for (int32_t e = toff[t]; e < toff[t + 1]; e += kSplitEntries) {
           sp_tile.push_back((int32_t)t);
           sp_e0.push_back(e);
           sp_e1.push_back(std::min(e + kSplitEntries, toff[t + 1]));
         }
-        max_k = std::max(max_k, k);
       }
       cur0[n_tiles] = (int32_t)sp_tile.size();
-      for (int32_t k = 0; k < max_k; k++)
-        for (int64_t t = 0; t < n_tiles; t++)
-          if (cur0[t] + k < cur0[t + 1]) sp_order.push_back(cur0[t] + k);
       pl->n_splits = (int32_t)sp_tile.size();
       OCTO_TRY(dalloc(pl, &pl->split_tile, sp_tile.size(), s));
       OCTO_TRY(dalloc(pl, &pl->split_e0, sp_tile.size(), s));
@@ -776,10 +777,25 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
       OCTO_TRY(dalloc(pl, &pl->split_order, sp_tile.size(), s));
       OCTO_TRY(dalloc(pl, &pl->cur_split0, cur0.size(), s));
       if (!sp_tile.empty()) {
+        const int32_t ns = (int32_t)sp_tile.size();
         size_t b = sp_tile.size() * 4;
         OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_tile, sp_tile.data(), b, cudaMemcpyHostToDevice, s)));
         OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_e0, sp_e0.data(), b, cudaMemcpyHostToDevice, s)));
         OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_e1, sp_e1.data(), b, cudaMemcpyHostToDevice, s)));
+        // Launch order: by the first page a split reads (then cursor, then split).  Entries
+        // are page-sorted within a cursor, so the splits that read the same pages -- a
+        // shared prefix, or a mounted span and its owner's own run -- start together and
+        // the repeated reads are served from L2.  The order array goes to split_order's
+        // buffer first as the first-page keys.
+        k_split_first_page<<<(ns + 255) / 256, 256, 0, s>>>(pl->entries, pl->split_e0, ns, pl->split_order);
+        count_launch();
+        OCTO_TRY(cuda_status(cudaGetLastError()));
+        std::vector<int32_t> first(ns);
+        OCTO_TRY(cuda_status(cudaMemcpyAsync(first.data(), pl->split_order, b, cudaMemcpyDeviceToHost, s)));
+        OCTO_TRY(cuda_status(cudaStreamSynchronize(s)));
+        sp_order.resize(ns);
+        for (int32_t i = 0; i < ns; i++) sp_order[i] = i;
+        std::stable_sort(sp_order.begin(), sp_order.end(), [&](int32_t a, int32_t c) { return first[a] < first[c]; });
         OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_order, sp_order.data(), b, cudaMemcpyHostToDevice, s)));
       }
       OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->cur_split0, cur0.data(), cur0.size() * 4, cudaMemcpyHostToDevice, s)));

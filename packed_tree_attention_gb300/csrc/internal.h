@@ -96,7 +96,7 @@ struct octo_plan_s {
   int32_t* split_tile = nullptr;     // [n_splits] cursor (tile) of the split
   int32_t* split_e0 = nullptr;       // [n_splits] first entry
   int32_t* split_e1 = nullptr;       // [n_splits] one past the last entry
-  int32_t* split_order = nullptr;    // [n_splits] launch order: split index within cursor, then cursor
+  int32_t* split_order = nullptr;    // [n_splits] launch order: first page read, then cursor, then split
   int32_t* cur_split0 = nullptr;     // [n_tiles+1] first split of each cursor
   std::vector<void*> allocs;
   cudaStream_t last_stream = nullptr;  // stream of the last call that used the plan

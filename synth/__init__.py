@@ -117,6 +117,8 @@ CONFIGS = {
     "train_step": dict(Hq=16, Hkv=4, d=128, P=64, dtype="bf16", scale=0.5),
     # paged decode, 256 cursors
     "decode": dict(Hq=16, Hkv=4, d=128, P=64, dtype="bf16", scale=0.5),
+    # the same cursor shape, 4 episodes x 8 cursors (about 1 GB of K/V: profiling runs)
+    "decode_small": dict(Hq=16, Hkv=4, d=128, P=64, dtype="bf16", scale=0.5),
 }
 
 
@@ -355,6 +357,8 @@ def make_preset(name: str, seed: int = 0) -> Episode:
         return _train_step(seed)
     if name == "decode":
         return _decode(seed)
+    if name == "decode_small":
+        return _decode(seed, n_episodes=4)
     raise KeyError(name)
 
 

@@ -255,3 +255,26 @@ def test_decode_values(lib, oracle_mod, dtype):
     want, wl = r.orc.decode(curs, q.astype(np.float64), r.scale)
     assert_close(out.float().cpu().numpy(), want, dtype, "decode out")
     assert_close(lse.cpu().numpy(), wl, dtype, "decode lse")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (6, 2), (8, 2), (12, 2), (16, 2)])
+def test_decode_group_sizes(lib, oracle_mod, Hq, Hkv):
+    """bf16 decode for query groups of 1, 2, 3, 4, 6 and 8 heads per kv head: every head of
+    a group is computed in one pass over the K/V rows, groups that are not a power of two
+    padded with zero queries whose results are dropped."""
+    ep = synth.random_dag(17 + Hq + Hkv, page_size=64, max_segments=12, max_len=400)
+    r = Run(lib, oracle_mod, ep, Hq, Hkv, 128, "bf16", 5)
+    curs = [s for s in range(r.orc.n_segments) if r.orc.seg_info(s)["len"] > 0]
+    q = synth.make_decode_q(len(curs), Hq, 128, "bf16", 0.5, 11)
+    dp = r.pool.decode_plan(curs)
+    assert dp.kernel_path(Hq, 2) == 2
+    out = torch.empty((len(curs), Hq, 128), dtype=r.tdt, device="cuda")
+    lse = torch.empty((len(curs), Hq), dtype=torch.float32, device="cuda")
+    ws_n = dp.decode_workspace_size(Hq)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device="cuda")
+    dp.decode(Hq, r.dev(q), out, lse, r.scale, ws, ws_n)
+    dp.sync()
+    want, wl = r.orc.decode(curs, q.astype(np.float64), r.scale)
+    assert_close(out.float().cpu().numpy(), want, "bf16", "decode out")
+    assert_close(lse.cpu().numpy(), wl, "bf16", "decode lse")
