@@ -127,12 +127,12 @@ def unique_tokens(entries, num_pages, P):
 L2_BYTES = 129 * 2**20   # GB300 L2
 
 
-def profiled_traffic(workload, call):
-    """DRAM bytes per call of `call` from the committed ncu summary of the episode workload,
+def profiled_traffic(workload, call, profile="dram_traffic_episode.md", profiled_workload="episode"):
+    """DRAM bytes per call of `call` from a committed ncu summary of the full-size workload,
     or None when the workload differs or a kernel source changed since the counters."""
     import hashlib
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "dram_traffic_episode.md")
-    if workload != "episode" or not os.path.exists(path):
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", profile)
+    if workload != profiled_workload or not os.path.exists(path):
         return None
     want, got = {}, None
     for line in open(path):
@@ -148,6 +148,7 @@ def profiled_traffic(workload, call):
             if hashlib.sha256(f.read()).hexdigest()[:16] != h:
                 return None
     return got if want else None
+
 
 WORKLOAD_DESC = {
     "episode": "episode: 16K prefix, 7 branches x 32K owned tokens, 3 rewinds, 6 mounts",
@@ -330,7 +331,9 @@ def decode_leg(pta, torch, name, seed, dev, stream, steps, warmup, world, dist, 
            "algorithmic_bytes": alg_bytes, "logical_bytes": logical * tok_bytes,
            "roofline": {"bound": "hbm", "achieved": alg_bytes / (kern_ms * 1e-3) / 1e9, "peak": hbm,
                         "unit": "GB/s", "frac": alg_bytes / (kern_ms * 1e-3) / 1e9 / hbm,
-                        "peak_source": peak_src, "traffic": None},
+                        "peak_source": peak_src,
+                        "traffic": profiled_traffic(name, "octo_decode", "ncu_decode.md", "decode"),
+                        "traffic_unit": "bytes per call (ncu dram__bytes_read + write)"},
            "gpu_launches": dlaunch, "clocks": dclocks, "kernel_path": dplan.kernel_path(Hq, 2)}
     del dpool, dkp, dvp
     torch.cuda.empty_cache()

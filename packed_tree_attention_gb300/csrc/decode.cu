@@ -11,7 +11,7 @@
 //                    kSplitEntries consecutive entries of one cursor, staged in shared
 //                    memory when the CTA starts.  One thread streams each entry's visible
 //                    K and V rows (contiguous in the pool: one bulk copy each, completing on
-//                    the stage's mbarrier) into a 3-stage ring.  Warp w takes keys
+//                    the stage's mbarrier) into a 2- or 3-stage ring.  Warp w takes keys
 //                    [16 w, 16 w + 16) of every page and all G query heads of the group at
 //                    once, so each K and V element is converted once and feeds G fused
 //                    multiply-adds (packed f32x2):
@@ -44,7 +44,6 @@ namespace {
 constexpr int kD = 128;
 constexpr int kP = 64;
 constexpr int kStageBytes = 2 * kP * kD * 2;  // K + V rows of one page and kv head, bf16
-constexpr int kStages = 3;
 constexpr int kWarps = 4;                     // 16 keys of each page per warp
 constexpr int kRec = 4 + kD;                  // floats per (split, head) partial, 16-byte aligned
 
@@ -100,23 +99,29 @@ __device__ __forceinline__ bool wait_full(uint64_t* bar, uint32_t parity, int32_
 }
 
 // GP = query heads per kv head rounded up to a power of two (heads >= G are zero queries
-// whose results are dropped); L = lanes per key in the score pass.
+// whose results are dropped).  Eight lanes per key keep the query slices at 16 d per head
+// (64 registers for GP = 4), so three CTAs fit on an SM with a 2-stage ring (12 warps: the
+// kernel is latency-bound, and more warps beat a deeper ring, measured); GP = 8 keeps two
+// CTAs with 3 stages.
 template <int GP>
 struct DecShape {
-  static constexpr int L = GP <= 4 ? 4 : 8;
+  static constexpr int L = 8;             // lanes per key in the score pass
   static constexpr int NC = 16 / L;       // 16-byte chunks of d per lane (d slice 8 NC)
   static constexpr int KPP = 32 / L;      // keys per score pass
   static constexpr int NPASS = 16 / KPP;  // passes over the warp's 16 keys
   static constexpr int SPREAD = L / GP;   // lanes that end with the same head
+  static constexpr int ST = GP <= 4 ? 2 : 3;          // ring stages
+  static constexpr int MIN_CTAS = GP <= 4 ? 3 : 2;    // CTAs per SM the registers allow
+  static constexpr int SMEM = ST * kStageBytes + kWarps * 16 * GP * 8 + kSplitEntries * (int)sizeof(octo_entry) + ST * 8;
 };
 
 template <int GP>
-__global__ void __launch_bounds__(kWarps * 32, 2) k_decode_split(DecParams p) {
+__global__ void __launch_bounds__(kWarps * 32, DecShape<GP>::MIN_CTAS) k_decode_split(DecParams p) {
   using S = DecShape<GP>;
   extern __shared__ __align__(128) uint8_t sm[];
   // shared memory: stages | (p, p) pairs [warp][16 keys][GP] | the split's entries | full barriers
-  uint64_t* pbuf = reinterpret_cast<uint64_t*>(sm + kStages * kStageBytes) + (threadIdx.x >> 5) * 16 * GP;
-  octo_entry* ents = reinterpret_cast<octo_entry*>(sm + kStages * kStageBytes + kWarps * 16 * GP * 8);
+  uint64_t* pbuf = reinterpret_cast<uint64_t*>(sm + S::ST * kStageBytes) + (threadIdx.x >> 5) * 16 * GP;
+  octo_entry* ents = reinterpret_cast<octo_entry*>(sm + S::ST * kStageBytes + kWarps * 16 * GP * 8);
   uint64_t* full = reinterpret_cast<uint64_t*>(ents + kSplitEntries);
 
   const int split = p.split_order[blockIdx.x / p.Hkv];
@@ -132,14 +137,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_decode_split(DecParams p) {
     for (int i = threadIdx.x; i < n * (int)(sizeof(octo_entry) / 4); i += blockDim.x) dst[i] = src[i];
   }
   if (threadIdx.x == 0) {
-    for (int st = 0; st < kStages; st++) tc::mbar_init(&full[st], 1);
+    for (int st = 0; st < S::ST; st++) tc::mbar_init(&full[st], 1);
     tc::fence_mbar_init();
   }
   __syncthreads();
   // entry jj's visible rows [lo, hi) of K and V: one bulk copy each, rows at their slot
   auto issue = [&](int jj) {
     const octo_entry& e = ents[jj];
-    const int st = jj % kStages;
+    const int st = jj % S::ST;
     const uint32_t rows = e.kv_hi - e.kv_lo;
     const size_t off = (((size_t)e.kv_page * p.Hkv + g) * kP + e.kv_lo) * kD;
     uint8_t* dk = sm + st * kStageBytes + e.kv_lo * 256;
@@ -148,12 +153,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_decode_split(DecParams p) {
     tc::bulk_load(dk + kP * 256, p.vp + off, rows * 256, &full[st]);
   };
   if (threadIdx.x == 0)
-    for (int jj = 0; jj < kStages - 1 && jj < n; jj++) issue(jj);
+    for (int jj = 0; jj < S::ST - 1 && jj < n; jj++) issue(jj);
 
   // score-pass lane roles: key kk of the pass, d slice s; the head this lane ends with.
-  // The lane's i-th 16-byte chunk of d is L ((i + kk) % NC) + s: the four (or eight) keys
-  // of a pass start at different chunk columns, so the unswizzled rows are read without
-  // bank conflicts.
+  // The lane's i-th 16-byte chunk of d is L ((i + kk) % NC) + s: the keys of a pass start
+  // at different chunk columns, so the unswizzled rows are read without bank conflicts.
   const int s = lane % S::L, kk = lane / S::L;
   const int hs = s / S::SPREAD;
   uint32_t coff[S::NC];
@@ -185,11 +189,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_decode_split(DecParams p) {
 
   int j = 0;
   for (; j < n; j++) {
-    const bool ok = wait_full(&full[j % kStages], (j / kStages) & 1, p.status);
+    const bool ok = wait_full(&full[j % S::ST], (j / S::ST) & 1, p.status);
     // every thread has entry j; every warp is done with entry j - 1, whose stage is refilled
     if (!__syncthreads_and(ok)) break;
-    if (threadIdx.x == 0 && j + kStages - 1 < n) issue(j + kStages - 1);
-    const uint8_t* stk = sm + (j % kStages) * kStageBytes;
+    if (threadIdx.x == 0 && j + S::ST - 1 < n) issue(j + S::ST - 1);
+    const uint8_t* stk = sm + (j % S::ST) * kStageBytes;
     const uint8_t* stv = stk + kP * 256;
     const int lo = ents[j].kv_lo, hi = ents[j].kv_hi;
 
@@ -287,8 +291,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) k_decode_split(DecParams p) {
   if (j < n) {
     // a wait gave up: let the copies already issued land before the CTA exits
     if (threadIdx.x == 0)
-      for (int jj = j; jj < n && jj < j + kStages - 1; jj++)
-        wait_full(&full[jj % kStages], (jj / kStages) & 1, p.status);
+      for (int jj = j; jj < n && jj < j + S::ST - 1; jj++)
+        wait_full(&full[jj % S::ST], (jj / S::ST) & 1, p.status);
     return;
   }
   __syncthreads();  // stages free: reuse stage 0 for the merge of the four warps
@@ -361,8 +365,7 @@ __global__ void k_decode_combine(const float* __restrict__ part, const int32_t* 
 
 template <int GP>
 int launch_split(const DecParams& prm, dim3 grid, cudaStream_t s) {
-  const int smem = kStages * kStageBytes + kWarps * 16 * GP * 8 + kSplitEntries * (int)sizeof(octo_entry) +
-                   kStages * 8;
+  const int smem = DecShape<GP>::SMEM;
   static bool attr = false;
   if (!attr) {
     OCTO_CUDA(cudaFuncSetAttribute(k_decode_split<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
