@@ -485,6 +485,45 @@ def run_ours(args, rank, world, dist):
                 "peak": hbm, "peak_source": peak_src}
         del rplan
 
+    # ---------------- per-token log-probability / loss leg (rows of the episode plan) ----
+    logprob = None
+    if not args.no_logprob:
+        lplan = pool.pack_tree(ep.roots, 128)
+        V, R = 151936, min(16384, N)
+        lx = synth.hash_fill(synth.STREAM_Q + 101 + 16 * seed, (R, V), torch.bfloat16, dev, 3.0, chunk_rows=1024)
+        lg = torch.empty_like(lx)
+        rng = np.random.default_rng(seed)
+        lids = torch.from_numpy(rng.integers(0, V, N).astype(np.int32)).to(dev)
+        lw = torch.from_numpy(rng.uniform(0, 1, N).astype(np.float32)).to(dev)
+        llogp = torch.empty(N, dtype=torch.float32, device=dev)
+        lloss = torch.empty(1, dtype=torch.float32, device=dev)
+        lws = torch.empty(lplan.token_logprob_workspace_size(R), dtype=torch.uint8, device=dev)
+        lt = []
+
+        def lstep():
+            a, b, c = ev(), ev(), ev()
+            a.record(stream)
+            lplan.token_logprob(0, R, lx, V, lids, lw, llogp, lws, loss=lloss, stream=stream)   # terms only
+            b.record(stream)
+            lplan.token_logprob(0, R, lx, V, lids, lw, llogp, lws, dlogits=lg, loss=lloss, stream=stream)
+            c.record(stream)
+            lt.append((a, b, c))
+
+        timed(torch, stream, lstep, 6, 3, dist)
+        f_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in lt[3:])
+        g_ms = statistics.mean(b.elapsed_time(c) for _, b, c in lt[3:])
+        small = 3 * N * 4 + R * 4                       # ids, weights, logp; loss partials
+        fb = lx.numel() * 2 + small                      # one read of the logits
+        gb = 2 * lx.numel() * 2 + small                  # + one write of the gradient
+        logprob = {"metric": "per-token log-prob / loss over packed rows, HBM GB/s",
+                   "workload": "%d episode rows x vocabulary %d, bf16 logits (%.1f GB)" % (R, V, lx.numel() * 2 / 1e9),
+                   "terms": {"value": fb / (f_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": f_ms,
+                             "frac": fb / (f_ms * 1e-3) / 1e9 / hbm},
+                   "terms_and_gradient": {"value": gb / (g_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": g_ms,
+                                          "frac": gb / (g_ms * 1e-3) / 1e9 / hbm},
+                   "peak": hbm, "peak_source": peak_src}
+        del lplan, lx, lg, lids, lw, llogp, lloss, lws
+
     # free the training leg before the decode leg
     del pool, kp, vp, q, do, o, lse, dq, dk, dv, ws
     torch.cuda.empty_cache()
@@ -558,6 +597,7 @@ def run_ours(args, rank, world, dist):
         "e2e": e2e,
         "decode": dec,
         "rope": rope,
+        "token_logprob": logprob,
         "cursor_view": view,
         "cpu_baseline": cpu,
     }
@@ -596,6 +636,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="episode")
     ap.add_argument("--no-rope", action="store_true")
+    ap.add_argument("--no-logprob", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")

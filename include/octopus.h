@@ -237,6 +237,39 @@ int octo_rope_rows(octo_plan_t plan, int32_t n_heads, void* x, int32_t dtype, fl
  * returning. */
 int octo_rope_pool_grad(octo_plan_t plan, float* dk_pool, float base, void* stream);
 
+/* ---- per-token log-probability and loss over the packed rows ----
+ * Octopus project page, "Architecture & Co-Design" item 03 (1D packed DAG-GRPO): every
+ * branch trains in one packed pass and single-ownership masking counts a shared prefix
+ * once; the five-primitives table, row done, has an untrainable close reminder (mask
+ * m = 0).  Each packed row t is one owned token, with id ids[t] and weight w[t] (the
+ * caller's m * advantage; NULL weight = 1).  Its term uses the logits row of pred(t), the
+ * row of the token before it on its path: t - 1 inside a segment; for a segment's first
+ * row the parent's row at the fork point minus one (through forks at point 0); none for a
+ * root's first token, whose logp is 0 and which adds nothing.  Mounted spans change no
+ * predecessor.  With lse(r) = log sum_v exp(x[r][v]):
+ *     logp[t] = x[pred t][ids t] - lse(pred t),   loss = - sum_t w[t] logp[t],
+ *     dlogits[r][v] = grad_scale * (W_r softmax(x[r])_v - sum over t with pred t = r and
+ *                     ids t = v of w[t]),  W_r = sum over t with pred t = r of w[t]. */
+
+/* Workspace (bytes) for octo_token_logprob over n_rows rows. */
+int octo_token_logprob_workspace_size(int32_t n_rows, size_t* bytes);
+
+/* Rows [row0, row0 + n_rows) of a pack plan (not a decode plan): logits [n_rows][ld]
+ * (dtype OCTO_DTYPE_BF16 or OCTO_DTYPE_F32, device, 16-byte aligned, ld * element size a
+ * multiple of 16, ld >= vocab), row row0 + i at logits + i * ld.  ids, weight, logp:
+ * device arrays over ALL rows of the plan (a row's successor can lie past the chunk).
+ * Writes logp[t] for every t whose predecessor is in the chunk, and 0 for the chunk's path
+ * starts; row_lse [n_rows] (natural log, optional); dlogits (optional, same dtype, layout
+ * and alignment as logits; may be logits itself: the gradient then overwrites the logits);
+ * loss (optional, one device float: - sum of w[t] logp[t] over the chunk's rows' successors,
+ * summed in a fixed order).  ws: device workspace of the size above.  Ids outside
+ * [0, vocab) give NaN logp, no gradient term, and OCTO_EINVAL at the next octo_sync.
+ * OCTO_ENOTSUP if a row of the plan has more than 64 successors.  Async on stream. */
+int octo_token_logprob(octo_plan_t plan, int32_t row0, int32_t n_rows, const void* logits, int32_t dtype,
+                       int64_t ld, int32_t vocab, const int32_t* ids, const float* weight, float* logp,
+                       float* row_lse, void* dlogits, float grad_scale, float* loss, void* ws, size_t ws_bytes,
+                       void* stream);
+
 /* ---- attention (device, async on stream) ---- */
 
 /* Forward over a packed plan.  For query head h the kv head is h / (n_q_heads /

@@ -67,7 +67,7 @@ SYMBOLS = ("octo_pool_create", "octo_pool_destroy", "octo_root", "octo_append", 
            "octo_attn_fwd", "octo_attn_bwd_workspace_size", "octo_attn_bwd", "octo_decode_workspace_size",
            "octo_decode", "octo_strerror", "octo_last_cuda_error", "octo_sync", "octo_kernel_path",
            "octo_launch_count", "octo_decode_noalloc", "octo_append_rope", "octo_rope_rows",
-           "octo_rope_pool_grad")
+           "octo_rope_pool_grad", "octo_token_logprob_workspace_size", "octo_token_logprob")
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
@@ -115,6 +115,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "octo_append_rope": [P, I32, I32, P, P, F, P, IP],
         "octo_rope_rows": [P, I32, P, I32, F, I32, P],
         "octo_rope_pool_grad": [P, P, F, P],
+        "octo_token_logprob_workspace_size": [I32, ctypes.POINTER(SZ)],
+        "octo_token_logprob": [P, I32, I32, P, I32, ctypes.c_int64, I32, P, P, P, P, P, F, P, P, SZ, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -353,6 +355,21 @@ class Plan:
     def rope_pool_grad(self, dk_pool, base, stream=None):
         """octo_rope_pool_grad: key gradients back through the append rotation."""
         _chk(self._L.octo_rope_pool_grad(self.h, _ptr(dk_pool), float(base), _stream(stream)), "octo_rope_pool_grad")
+
+    def token_logprob_workspace_size(self, n_rows):
+        n = ctypes.c_size_t(0)
+        _chk(self._L.octo_token_logprob_workspace_size(n_rows, ctypes.byref(n)), "octo_token_logprob_workspace_size")
+        return n.value
+
+    def token_logprob(self, row0, n_rows, logits, vocab, ids, weight, logp, ws, row_lse=None, dlogits=None,
+                      grad_scale=1.0, loss=None, stream=None):
+        """octo_token_logprob: per-token log-probabilities (and loss, gradient) of the rows
+        [row0, row0 + n_rows) whose logits rows are `logits` [n_rows][ld] (bf16 or fp32)."""
+        dt = DTYPE_F32 if logits.element_size() == 4 else DTYPE_BF16
+        _chk(self._L.octo_token_logprob(self.h, row0, n_rows, _ptr(logits), dt, logits.stride(0), vocab,
+                                        _ptr(ids), _ptr(weight), _ptr(logp), _ptr(row_lse), _ptr(dlogits),
+                                        float(grad_scale), _ptr(loss), _ptr(ws), ws.numel() * ws.element_size(),
+                                        _stream(stream)), "octo_token_logprob")
 
     def sync(self, stream=None):
         _chk(self._L.octo_sync(self.h, _stream(stream)), "octo_sync")

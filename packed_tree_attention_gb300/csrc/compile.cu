@@ -607,6 +607,52 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
   if (n_segs > 0)
     OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->seg_order, order_src, n_segs * 4, cudaMemcpyHostToDevice, s)));
 
+  // ---- path predecessors of the packed rows (training plans) ----
+  std::vector<int32_t> spred, ep, er;  // pageable sources of async copies: kept to the end
+  if (!is_decode && n_segs > 0) {
+    std::vector<int32_t> rbase(n_segs), kpos(nseg_all, -1);
+    spred.assign(n_segs, -1);
+    int32_t acc = 0;
+    for (int32_t k = 0; k < n_segs; k++) {
+      rbase[k] = acc;
+      kpos[seg_order_host[k]] = k;
+      acc += pool->segs[seg_order_host[k]].len;
+    }
+    std::vector<std::pair<int32_t, int32_t>> ex;
+    for (int32_t k = 0; k < n_segs; k++) {
+      const Segment& g = pool->segs[seg_order_host[k]];
+      if (g.len == 0) continue;
+      int32_t par = g.parent, f = g.fork;
+      while (par >= 0 && f == 0) {  // a fork at point 0 sees none of the parent's own tokens
+        f = pool->segs[par].fork;
+        par = pool->segs[par].parent;
+      }
+      if (par >= 0 && kpos[par] >= 0) {
+        spred[k] = rbase[kpos[par]] + f - 1;
+        ex.push_back({spred[k], rbase[k]});
+      }
+    }
+    std::sort(ex.begin(), ex.end());
+    int32_t run = 0;
+    for (size_t i = 0; i < ex.size(); i++) {
+      run = (i > 0 && ex[i].first == ex[i - 1].first) ? run + 1 : 1;
+      pl->max_succ = std::max(pl->max_succ, run + 1);  // + the next own row
+    }
+    pl->max_succ = std::max(pl->max_succ, 1);
+    ep.resize(ex.size());
+    er.resize(ex.size());
+    for (size_t i = 0; i < ex.size(); i++) ep[i] = ex[i].first, er[i] = ex[i].second;
+    pl->n_succ_extra = (int32_t)ex.size();
+    OCTO_TRY(dalloc(pl, &pl->seg_pred, n_segs, s));
+    OCTO_TRY(dalloc(pl, &pl->succ_pred, std::max<size_t>(ex.size(), 1), s));
+    OCTO_TRY(dalloc(pl, &pl->succ_row, std::max<size_t>(ex.size(), 1), s));
+    OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->seg_pred, spred.data(), n_segs * 4, cudaMemcpyHostToDevice, s)));
+    if (!ex.empty()) {
+      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->succ_pred, ep.data(), ep.size() * 4, cudaMemcpyHostToDevice, s)));
+      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->succ_row, er.data(), er.size() * 4, cudaMemcpyHostToDevice, s)));
+    }
+  }
+
   // ---- layout ----
   if (is_decode) {
     if (n_segs > 0) {

@@ -91,6 +91,13 @@ struct octo_plan_s {
   int32_t* pair_n_items = nullptr;   // [n_pairs] items actually written
   int32_t* pair_order = nullptr;     // [n_pairs] launch order, heaviest first
   octo::PairItem* pair_items = nullptr;  // [n_entries]
+  // path predecessors of the packed rows (per-token log-probability): row r's successors
+  // are r + 1 inside its segment plus the first rows of the segments continuing from r
+  int32_t* seg_pred = nullptr;       // [n_segments] row before the packed segment's first row, -1 none
+  int32_t n_succ_extra = 0;
+  int32_t* succ_pred = nullptr;      // [n_succ_extra] predecessor row, ascending
+  int32_t* succ_row = nullptr;       // [n_succ_extra] first row of the continuing segment
+  int32_t max_succ = 0;              // most successors of one row
   // decode plans: runs of up to kSplitEntries entries of one cursor (split-KV)
   int32_t n_splits = 0;
   int32_t* split_tile = nullptr;     // [n_splits] cursor (tile) of the split
