@@ -129,8 +129,7 @@ L2_BYTES = 129 * 2**20   # GB300 L2
 
 def profiled_traffic(workload, call, profile="dram_traffic_episode.md", profiled_workload="episode"):
     """DRAM bytes per call of `call` from a committed ncu summary of the full-size workload,
-    or None when the workload differs or a kernel source changed since the counters."""
-    import hashlib
+    or None when the workload differs or a kernel source's code changed since the counters."""
     path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", profile)
     if workload != profiled_workload or not os.path.exists(path):
         return None
@@ -144,10 +143,21 @@ def profiled_traffic(workload, call, profile="dram_traffic_episode.md", profiled
             got = int(line.split(": ")[1])
     src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "packed_tree_attention_gb300", "csrc")
     for name, h in want.items():
-        with open(os.path.join(src, name), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest()[:16] != h:
-                return None
+        if code_fingerprint(os.path.join(src, name)) != h:
+            return None
     return got if want else None
+
+
+def code_fingerprint(path):
+    """sha256/16 of a C++/CUDA source with // comments and blank lines removed: edits to
+    comments keep it, any change to the code does not."""
+    import hashlib
+    lines = []
+    for line in open(path, encoding="utf-8"):
+        line = line.split("//", 1)[0].rstrip()
+        if line:
+            lines.append(line)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
 
 
 WORKLOAD_DESC = {

@@ -828,11 +828,12 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
         OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_tile, sp_tile.data(), b, cudaMemcpyHostToDevice, s)));
         OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_e0, sp_e0.data(), b, cudaMemcpyHostToDevice, s)));
         OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_e1, sp_e1.data(), b, cudaMemcpyHostToDevice, s)));
-        // Launch order: by the first page a split reads (then cursor, then split).  Entries
-        // are page-sorted within a cursor, so the splits that read the same pages -- a
-        // shared prefix, or a mounted span and its owner's own run -- start together and
-        // the repeated reads are served from L2.  The order array goes to split_order's
-        // buffer first as the first-page keys.
+        // Launch order: by the first page a split reads (then cursor, then split).  A
+        // cursor's entries follow its context (prefix run, own run, mounted spans at their
+        // points), so cursors sharing a prefix have splits starting on the same page, and
+        // a mounted span's pages sit next to its owner's run: such splits start together
+        // and their repeated reads are served from L2.  The order array goes to
+        // split_order's buffer first as the first-page keys.
         k_split_first_page<<<(ns + 255) / 256, 256, 0, s>>>(pl->entries, pl->split_e0, ns, pl->split_order);
         count_launch();
         OCTO_TRY(cuda_status(cudaGetLastError()));
