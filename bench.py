@@ -181,7 +181,7 @@ def build_episode(pta, torch, name, seed, dev):
     cfg = synth.CONFIGS[name]
     Hq, Hkv, d, P = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["P"]
     ep = synth.make_preset(name, seed=seed)
-    npages = sum((L + P - 1) // P for L in ep.length) + 8
+    npages = sum((L + P - 1) // P for L in ep.length) + 8 + 4 * len(ep.cursors)   # room for decode steps
     kp = torch.empty((npages, Hkv, P, d), dtype=torch.bfloat16, device=dev)
     vp = torch.empty_like(kp)
     pool = pta.Pool(npages, P, Hkv, d, pta.DTYPE_BF16, kp, vp)
@@ -224,7 +224,7 @@ def oracle_sample(name, seed, budget_s=15.0, n_rows_max=256):
     Hq, Hkv, d, P = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["P"]
     ep = synth.make_preset(name, seed=seed)
     T = ep.n_tokens
-    npages = sum((L + P - 1) // P for L in ep.length) + 8
+    npages = sum((L + P - 1) // P for L in ep.length) + 8 + 4 * len(ep.cursors)   # room for decode steps
     orc = oracle.Oracle(P, npages, Hkv, d)
     K = synth.hash_rows(synth.STREAM_K + 16 * seed, np.arange(T), Hkv * d, torch.bfloat16, 0.5).reshape(T, Hkv, d)
     V = synth.hash_rows(synth.STREAM_V + 16 * seed, np.arange(T), Hkv * d, torch.bfloat16, 0.5).reshape(T, Hkv, d)
@@ -333,10 +333,31 @@ def decode_leg(pta, torch, name, seed, dev, stream, steps, warmup, world, dist, 
 
     timed(torch, stream, pstep, 3, 1, dist)
     full_ms = statistics.mean([a.elapsed_time(b) for a, b, _ in plan_ms_list[1:]])
+    # plan upkeep per decoded token: every cursor one token longer (layout only), then the
+    # plan advanced in place vs compiled afresh (both synchronous: wall time)
+    upkeep = None
+    if all(dpool.append(c, 1, check=False) == pta.OK for c in curs):
+        adv_t, fresh_t = [], []
+        for it in range(4):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            if dplan.advance(stream, check=False) != pta.OK:
+                break
+            t1 = time.perf_counter()
+            p3 = dpool.decode_plan(curs, stream)
+            t2 = time.perf_counter()
+            adv_t.append(t1 - t0)
+            fresh_t.append(t2 - t1)
+            del p3
+            if it < 3 and not all(dpool.append(c, 1, check=False) == pta.OK for c in curs):
+                break
+        if adv_t:
+            upkeep = {"advance_ms": 1e3 * statistics.median(adv_t),
+                      "fresh_plan_ms": 1e3 * statistics.median(fresh_t)}
     world_bytes = world * alg_bytes
     dec = {"metric": "paged decode HBM GB/s", "value": world_bytes / (kern_ms * 1e-3) / 1e9, "unit": "GB/s",
            "workload": WORKLOAD_DESC[name] + "; 16q/4kv heads, d=128, page 64, bf16",
-           "ms_per_step": kern_ms, "ms_per_step_with_plan": full_ms,
+           "ms_per_step": kern_ms, "ms_per_step_with_plan": full_ms, "plan_upkeep": upkeep,
            "cursors": n, "unique_kv_tokens": uniq, "logical_kv_tokens": logical,
            "algorithmic_bytes": alg_bytes, "logical_bytes": logical * tok_bytes,
            "roofline": {"bound": "hbm", "achieved": alg_bytes / (kern_ms * 1e-3) / 1e9, "peak": hbm,

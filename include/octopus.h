@@ -190,6 +190,20 @@ int octo_pack_tree(octo_pool_t pool, const octo_cursor_t* roots, int32_t n_roots
 int octo_decode_plan(octo_pool_t pool, const octo_cursor_t* cursors, int32_t n, void* stream,
                      octo_plan_t* out);
 
+/* Moves a decode plan on by one token per cursor, after each of its cursors had exactly
+ * one token appended (octo_append / octo_append_rope) since the plan was built or last
+ * advanced: the result equals octo_decode_plan on the same cursors, array for array and
+ * bit for bit (octopus project page, "Architecture & Co-Design" item 01: a turn extends
+ * a cursor over the same shared pages, so the view needs only the new token; the pages
+ * quote 128K prompt assembly in 1.44 ms).  Only the newest token's page entry changes
+ * per cursor; the CSC view, launch orders and split-KV runs are rebuilt from the entries.
+ * OCTO_ESTATE, with the plan unchanged, when a cursor is not exactly one token longer, was
+ * freed, or has a mount at or after the point of its new token (its context then grows by
+ * more than that token): build a fresh plan instead.  On any other error the plan must be
+ * destroyed.  The plan can have more split-KV runs afterwards: query
+ * octo_decode_workspace_size again.  Synchronises `stream` (twice). */
+int octo_decode_plan_advance(octo_plan_t plan, void* stream);
+
 int octo_plan_info(octo_plan_t plan, octo_plan_info_t* info);
 
 /* Copies the plan to host buffers (each may be NULL); synchronous.  Sizes: seg_order,

@@ -67,7 +67,8 @@ SYMBOLS = ("octo_pool_create", "octo_pool_destroy", "octo_root", "octo_append", 
            "octo_attn_fwd", "octo_attn_bwd_workspace_size", "octo_attn_bwd", "octo_decode_workspace_size",
            "octo_decode", "octo_strerror", "octo_last_cuda_error", "octo_sync", "octo_kernel_path",
            "octo_launch_count", "octo_decode_noalloc", "octo_append_rope", "octo_rope_rows",
-           "octo_rope_pool_grad", "octo_token_logprob_workspace_size", "octo_token_logprob")
+           "octo_rope_pool_grad", "octo_token_logprob_workspace_size", "octo_token_logprob",
+           "octo_decode_plan_advance")
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
@@ -117,6 +118,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "octo_rope_pool_grad": [P, P, F, P],
         "octo_token_logprob_workspace_size": [I32, ctypes.POINTER(SZ)],
         "octo_token_logprob": [P, I32, I32, P, I32, ctypes.c_int64, I32, P, P, P, P, P, F, P, P, SZ, P],
+        "octo_decode_plan_advance": [P, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -287,9 +289,12 @@ class Plan:
 
     def __init__(self, pool: Pool, h):
         self.pool, self._L, self.h = pool, pool._L, h
+        self.info = self._info()
+
+    def _info(self):
         i = _PlanInfo()
-        _chk(self._L.octo_plan_info(h, ctypes.byref(i)), "octo_plan_info")
-        self.info = {n: getattr(i, n) for n, _ in _PlanInfo._fields_}
+        _chk(self._L.octo_plan_info(self.h, ctypes.byref(i)), "octo_plan_info")
+        return {n: getattr(i, n) for n, _ in _PlanInfo._fields_}
 
     def close(self):
         if getattr(self, "h", None):
@@ -355,6 +360,15 @@ class Plan:
     def rope_pool_grad(self, dk_pool, base, stream=None):
         """octo_rope_pool_grad: key gradients back through the append rotation."""
         _chk(self._L.octo_rope_pool_grad(self.h, _ptr(dk_pool), float(base), _stream(stream)), "octo_rope_pool_grad")
+
+    def advance(self, stream=None, check=True):
+        """octo_decode_plan_advance: the decode plan one token further on every cursor."""
+        st = self._L.octo_decode_plan_advance(self.h, _stream(stream))
+        if st == OK:
+            self.info = self._info()
+        if check:
+            _chk(st, "octo_decode_plan_advance")
+        return st
 
     def token_logprob_workspace_size(self, n_rows):
         n = ctypes.c_size_t(0)

@@ -337,6 +337,43 @@ __global__ void k_csc_scatter(const octo_entry* __restrict__ entries, int64_t n,
 }
 
 // one block per touched page: sort its CSC slice ascending (bitonic in shared memory)
+// Advances a decode plan by one token per cursor, one warp per cursor: the cursor's
+// entries move to their new place; its newest token either widens the entry of its own
+// page (kv_hi + 1) or, on a fresh page, adds that page's entry at the end of the list (own
+// pages follow everything else in context order); the row moves to the new token.
+// adv[2 i] = the token's page, adv[2 i + 1] = 1 if the page is fresh.
+__global__ void k_decode_advance(const octo_entry* __restrict__ old_e, const int32_t* __restrict__ old_off,
+                                 const int32_t* __restrict__ new_off, const int32_t* __restrict__ adv, int32_t n,
+                                 octo_entry* __restrict__ out, int32_t* __restrict__ tile_t0,
+                                 int32_t* __restrict__ row_pos) {
+  const int32_t i = (int32_t)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (i >= n) return;
+  const int32_t a = old_off[i], b = old_off[i + 1], o = new_off[i];
+  const int32_t page = adv[2 * i], fresh = adv[2 * i + 1];
+  for (int32_t k = lane; k < b - a; k += 32) {
+    octo_entry e = old_e[a + k];
+    if (!fresh && e.kv_page == (uint32_t)page && e.src == -1) e.kv_hi = (uint16_t)(e.kv_hi + 1);
+    out[o + k] = e;
+  }
+  if (lane == 0) {
+    if (fresh) {
+      octo_entry e;
+      e.q_tile = (uint32_t)i;
+      e.kv_page = (uint32_t)page;
+      e.kv_lo = 0;
+      e.kv_hi = 1;
+      e.q_lo = 0;
+      e.flags = 0;
+      e.diag = 0;
+      e.src = -1;
+      out[o + (b - a)] = e;
+    }
+    tile_t0[i] += 1;
+    row_pos[i] += 1;
+  }
+}
+
 // kv_page of the first entry of each split (decode plans)
 __global__ void k_split_first_page(const octo_entry* __restrict__ entries, const int32_t* __restrict__ split_e0,
                                    int32_t n, int32_t* __restrict__ out) {
@@ -509,6 +546,22 @@ int dalloc(octo_plan_s* pl, T** ptr, size_t n, cudaStream_t s) {
   return OCTO_OK;
 }
 
+// an allocation of the entry-derived part of a plan (rebuilt when a decode plan advances)
+template <typename T>
+int dalloc_b(octo_plan_s* pl, T** ptr, size_t n, cudaStream_t s) {
+  if (int st = dalloc(pl, ptr, n, s)) return st;
+  pl->b_allocs.push_back(*ptr);
+  return OCTO_OK;
+}
+
+// frees one of the plan's allocations, stream-ordered
+void dfree(octo_plan_s* pl, void* p, cudaStream_t s) {
+  auto it = std::find(pl->allocs.begin(), pl->allocs.end(), p);
+  if (it == pl->allocs.end()) return;
+  pl->allocs.erase(it);
+  cudaFreeAsync(p, s);
+}
+
 }  // namespace
 
 #define OCTO_TRY(x)                 \
@@ -519,6 +572,176 @@ int dalloc(octo_plan_s* pl, T** ptr, size_t n, cudaStream_t s) {
       return _s;                    \
     }                               \
   } while (0)
+
+#define OCTO_RET(x)                 \
+  do {                              \
+    int _s = (x);                   \
+    if (_s != OCTO_OK) return _s;   \
+  } while (0)
+
+// The parts of a plan that follow from its entries: the CSC view, the pair count and page
+// statistics, the launch orders, and the dK/dV page pairs (training plans) or the split-KV
+// runs (decode plans).  Everything it allocates is listed in b_allocs, so that a decode
+// plan advanced by a token can drop and rebuild it.  Ends with a stream synchronisation.
+int finish_plan(octo_plan_s* pl, cudaStream_t s) {
+  octo_pool_s* pool = pl->pool;
+  const bool is_decode = pl->info.is_decode != 0;
+  const int64_t n_tiles = pl->info.n_tiles;
+  const int32_t n_entries = pl->info.n_entries;
+  int32_t* d_cnt = pl->d_cnt;
+  int32_t* d_scratch = pl->d_scratch;
+  OCTO_RET(dalloc_b(pl, &pl->csc_perm, n_entries, s));
+  // ---- CSC ----
+  OCTO_RET(cuda_status(cudaMemsetAsync(d_cnt, 0, (size_t)pl->num_pages * 4, s)));
+  if (n_entries > 0) {
+    k_page_hist<<<(n_entries + 255) / 256, 256, 0, s>>>(pl->entries, n_entries, pl->tile_rows, d_cnt,
+                                                        (unsigned long long*)(d_scratch + 4));
+    count_launch();
+  }
+  k_scan<<<1, 1024, 0, s>>>(d_cnt, pl->num_pages, pl->page_off, d_scratch + 2);
+  count_launch();
+  OCTO_RET(cuda_status(cudaMemsetAsync(d_cnt, 0, (size_t)pl->num_pages * 4, s)));
+  if (n_entries > 0) {
+    k_csc_scatter<<<(n_entries + 255) / 256, 256, 0, s>>>(pl->entries, n_entries, pl->page_off, d_cnt,
+                                                          pl->csc_perm);
+    count_launch();
+  }
+  k_touched<<<1, 1024, 0, s>>>(pl->page_off, pl->num_pages, pl->touched, d_scratch + 3);
+  count_launch();
+  OCTO_RET(cuda_status(cudaGetLastError()));
+  int32_t hs2[6];
+  OCTO_RET(cuda_status(cudaMemcpyAsync(hs2, d_scratch, 24, cudaMemcpyDeviceToHost, s)));
+  OCTO_RET(cuda_status(cudaStreamSynchronize(s)));
+  pl->info.max_page_entries = hs2[2];
+  pl->info.n_touched_pages = hs2[3];
+  unsigned long long pairs;
+  std::memcpy(&pairs, &hs2[4], 8);
+  pl->info.pairs = (int64_t)pairs;
+  if (hs2[2] > kSortCap) return OCTO_ENOTSUP;
+  if (hs2[3] > 0 && hs2[2] > 1) {
+    int32_t m = 1;
+    while (m < hs2[2]) m <<= 1;
+    size_t smem = (size_t)m * 4;
+    if (smem > 48 * 1024) OCTO_RET(cuda_status(cudaFuncSetAttribute(k_csc_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)));
+    k_csc_sort<<<hs2[3], 512, smem, s>>>(pl->touched, pl->page_off, pl->csc_perm, m);
+    count_launch();
+  }
+  OCTO_RET(cuda_status(cudaGetLastError()));
+  // ---- launch orders: heaviest tiles / page pairs first (longest-processing-time first) ----
+  {
+    std::vector<int32_t> toff(n_tiles + 1), poff((size_t)pl->num_pages + 1);
+    OCTO_RET(cuda_status(cudaMemcpyAsync(toff.data(), pl->tile_off, (n_tiles + 1) * 4, cudaMemcpyDeviceToHost, s)));
+    OCTO_RET(cuda_status(
+        cudaMemcpyAsync(poff.data(), pl->page_off, ((size_t)pl->num_pages + 1) * 4, cudaMemcpyDeviceToHost, s)));
+    OCTO_RET(cuda_status(cudaStreamSynchronize(s)));
+    if (is_decode) pl->h_toff = toff;
+    std::vector<int32_t> tord(n_tiles);
+    for (int64_t t = 0; t < n_tiles; t++) tord[t] = (int32_t)t;
+    std::stable_sort(tord.begin(), tord.end(),
+                     [&](int32_t a, int32_t b) { return toff[a + 1] - toff[a] > toff[b + 1] - toff[b]; });
+    const bool any_touched = pl->info.n_touched_pages > 0;
+    // dK/dV work units: consecutive own pages of each segment, two at a time, among the
+    // touched pages; a touched page without a touched partner runs alone
+    if (!is_decode && any_touched) {
+      std::vector<int32_t> pp;
+      std::vector<char> seen((size_t)pl->num_pages, 0);
+      auto cnt = [&](int32_t pg) { return pg < 0 ? 0 : poff[pg + 1] - poff[pg]; };
+      for (const Segment& g : pool->segs) {
+        if (g.freed) continue;
+        int32_t pend = -1;
+        for (int32_t pg : g.pages) {
+          if (pg < 0 || pg >= pl->num_pages || cnt(pg) == 0 || seen[pg]) {
+            if (pend >= 0) { pp.push_back(pend); pp.push_back(-1); pend = -1; }
+            continue;
+          }
+          seen[pg] = 1;
+          if (pend < 0) {
+            pend = pg;
+          } else {
+            pp.push_back(pend);
+            pp.push_back(pg);
+            pend = -1;
+          }
+        }
+        if (pend >= 0) { pp.push_back(pend); pp.push_back(-1); }
+      }
+      for (int32_t pg = 0; pg < pl->num_pages; pg++)
+        if (cnt(pg) > 0 && !seen[pg]) { pp.push_back(pg); pp.push_back(-1); }
+      const int32_t np = (int32_t)(pp.size() / 2);
+      std::vector<int32_t> poff2(np + 1, 0), pord2(np);
+      for (int32_t i = 0; i < np; i++) {
+        poff2[i + 1] = poff2[i] + cnt(pp[2 * i]) + cnt(pp[2 * i + 1]);
+        pord2[i] = i;
+      }
+      std::stable_sort(pord2.begin(), pord2.end(), [&](int32_t a, int32_t b) {
+        return poff2[a + 1] - poff2[a] > poff2[b + 1] - poff2[b];
+      });
+      pl->n_pairs = np;
+      OCTO_RET(dalloc_b(pl, &pl->pair_pages, pp.size(), s));
+      OCTO_RET(dalloc_b(pl, &pl->pair_item_off, poff2.size(), s));
+      OCTO_RET(dalloc_b(pl, &pl->pair_n_items, np, s));
+      OCTO_RET(dalloc_b(pl, &pl->pair_order, np, s));
+      OCTO_RET(dalloc_b(pl, &pl->pair_items, (size_t)n_entries, s));
+      OCTO_RET(cuda_status(cudaMemcpyAsync(pl->pair_pages, pp.data(), pp.size() * 4, cudaMemcpyHostToDevice, s)));
+      OCTO_RET(cuda_status(
+          cudaMemcpyAsync(pl->pair_item_off, poff2.data(), poff2.size() * 4, cudaMemcpyHostToDevice, s)));
+      OCTO_RET(cuda_status(cudaMemcpyAsync(pl->pair_order, pord2.data(), np * 4, cudaMemcpyHostToDevice, s)));
+      k_pair_items<<<np, 256, 0, s>>>(pl->pair_pages, pl->pair_item_off, pl->page_off, pl->csc_perm, pl->entries,
+                                      n_entries, pl->tile_row0, pl->tile_rows, pl->pair_items, pl->pair_n_items);
+      count_launch();
+      OCTO_RET(cuda_status(cudaGetLastError()));
+    }
+    OCTO_RET(dalloc_b(pl, &pl->tile_order, n_tiles, s));
+    if (n_tiles > 0)
+      OCTO_RET(cuda_status(cudaMemcpyAsync(pl->tile_order, tord.data(), n_tiles * 4, cudaMemcpyHostToDevice, s)));
+    // decode plans: split each cursor's entries into runs of kSplitEntries
+    std::vector<int32_t> sp_tile, sp_e0, sp_e1, sp_order, cur0(n_tiles + 1, 0);
+    if (is_decode) {
+      for (int64_t t = 0; t < n_tiles; t++) {
+        cur0[t] = (int32_t)sp_tile.size();
+        for (int32_t e = toff[t]; e < toff[t + 1]; e += kSplitEntries) {
+          sp_tile.push_back((int32_t)t);
+          sp_e0.push_back(e);
+          sp_e1.push_back(std::min(e + kSplitEntries, toff[t + 1]));
+        }
+      }
+      cur0[n_tiles] = (int32_t)sp_tile.size();
+      pl->n_splits = (int32_t)sp_tile.size();
+      OCTO_RET(dalloc_b(pl, &pl->split_tile, sp_tile.size(), s));
+      OCTO_RET(dalloc_b(pl, &pl->split_e0, sp_tile.size(), s));
+      OCTO_RET(dalloc_b(pl, &pl->split_e1, sp_tile.size(), s));
+      OCTO_RET(dalloc_b(pl, &pl->split_order, sp_tile.size(), s));
+      OCTO_RET(dalloc_b(pl, &pl->cur_split0, cur0.size(), s));
+      if (!sp_tile.empty()) {
+        const int32_t ns = (int32_t)sp_tile.size();
+        size_t b = sp_tile.size() * 4;
+        OCTO_RET(cuda_status(cudaMemcpyAsync(pl->split_tile, sp_tile.data(), b, cudaMemcpyHostToDevice, s)));
+        OCTO_RET(cuda_status(cudaMemcpyAsync(pl->split_e0, sp_e0.data(), b, cudaMemcpyHostToDevice, s)));
+        OCTO_RET(cuda_status(cudaMemcpyAsync(pl->split_e1, sp_e1.data(), b, cudaMemcpyHostToDevice, s)));
+        // Launch order: by the first page a split reads (then cursor, then split).  A
+        // cursor's entries follow its context (prefix run, own run, mounted spans at their
+        // points), so cursors sharing a prefix have splits starting on the same page, and
+        // a mounted span's pages sit next to its owner's run: such splits start together
+        // and their repeated reads are served from L2.  The order array goes to
+        // split_order's buffer first as the first-page keys.
+        k_split_first_page<<<(ns + 255) / 256, 256, 0, s>>>(pl->entries, pl->split_e0, ns, pl->split_order);
+        count_launch();
+        OCTO_RET(cuda_status(cudaGetLastError()));
+        std::vector<int32_t> first(ns);
+        OCTO_RET(cuda_status(cudaMemcpyAsync(first.data(), pl->split_order, b, cudaMemcpyDeviceToHost, s)));
+        OCTO_RET(cuda_status(cudaStreamSynchronize(s)));
+        sp_order.resize(ns);
+        for (int32_t i = 0; i < ns; i++) sp_order[i] = i;
+        std::stable_sort(sp_order.begin(), sp_order.end(), [&](int32_t a, int32_t c) { return first[a] < first[c]; });
+        OCTO_RET(cuda_status(cudaMemcpyAsync(pl->split_order, sp_order.data(), b, cudaMemcpyHostToDevice, s)));
+      }
+      OCTO_RET(cuda_status(cudaMemcpyAsync(pl->cur_split0, cur0.data(), cur0.size() * 4, cudaMemcpyHostToDevice, s)));
+    }
+    // the host vectors are pageable and go out of scope
+    OCTO_RET(cuda_status(cudaStreamSynchronize(s)));
+  }
+  return OCTO_OK;
+}
 
 int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t* seg_order_host, int32_t n_segs,
                  bool is_decode, int32_t bm, cudaStream_t s, octo_plan_s** out) {
@@ -693,163 +916,19 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
   pl->info.n_entries = n_entries;
   pl->info.max_tile_entries = hs[1];
   OCTO_TRY(dalloc(pl, &pl->entries, n_entries, s));
-  OCTO_TRY(dalloc(pl, &pl->csc_perm, n_entries, s));
   if (n_tiles > 0) {
     k_fill<<<grid_t, 32 * wpb, 0, s>>>(w, pl->tile_seg, pl->tile_t0, pl->tile_rows, (int32_t)n_tiles, pl->tile_off,
                                        pl->entries, d_status);
     count_launch();
   }
-  // ---- CSC ----
-  OCTO_TRY(cuda_status(cudaMemsetAsync(d_cnt, 0, (size_t)pl->num_pages * 4, s)));
-  if (n_entries > 0) {
-    k_page_hist<<<(n_entries + 255) / 256, 256, 0, s>>>(pl->entries, n_entries, pl->tile_rows, d_cnt,
-                                                        (unsigned long long*)(d_scratch + 4));
-    count_launch();
+  pl->d_cnt = d_cnt;
+  pl->d_scratch = d_scratch;
+  if (is_decode) {
+    pl->cur_seg.assign(tile_segs_host, tile_segs_host + n_segs);
+    pl->cur_len.resize(n_segs);
+    for (int32_t i = 0; i < n_segs; i++) pl->cur_len[i] = pool->segs[tile_segs_host[i]].len;
   }
-  k_scan<<<1, 1024, 0, s>>>(d_cnt, pl->num_pages, pl->page_off, d_scratch + 2);
-  count_launch();
-  OCTO_TRY(cuda_status(cudaMemsetAsync(d_cnt, 0, (size_t)pl->num_pages * 4, s)));
-  if (n_entries > 0) {
-    k_csc_scatter<<<(n_entries + 255) / 256, 256, 0, s>>>(pl->entries, n_entries, pl->page_off, d_cnt,
-                                                          pl->csc_perm);
-    count_launch();
-  }
-  k_touched<<<1, 1024, 0, s>>>(pl->page_off, pl->num_pages, pl->touched, d_scratch + 3);
-  count_launch();
-  OCTO_TRY(cuda_status(cudaGetLastError()));
-  int32_t hs2[6];
-  OCTO_TRY(cuda_status(cudaMemcpyAsync(hs2, d_scratch, 24, cudaMemcpyDeviceToHost, s)));
-  OCTO_TRY(cuda_status(cudaStreamSynchronize(s)));
-  pl->info.max_page_entries = hs2[2];
-  pl->info.n_touched_pages = hs2[3];
-  unsigned long long pairs;
-  std::memcpy(&pairs, &hs2[4], 8);
-  pl->info.pairs = (int64_t)pairs;
-  if (hs2[2] > kSortCap) {
-    octo_plan_destroy(pl);
-    return OCTO_ENOTSUP;
-  }
-  if (hs2[3] > 0 && hs2[2] > 1) {
-    int32_t m = 1;
-    while (m < hs2[2]) m <<= 1;
-    size_t smem = (size_t)m * 4;
-    if (smem > 48 * 1024) OCTO_TRY(cuda_status(cudaFuncSetAttribute(k_csc_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)));
-    k_csc_sort<<<hs2[3], 512, smem, s>>>(pl->touched, pl->page_off, pl->csc_perm, m);
-    count_launch();
-  }
-  OCTO_TRY(cuda_status(cudaGetLastError()));
-  // ---- launch orders: heaviest tiles / page pairs first (longest-processing-time first) ----
-  {
-    std::vector<int32_t> toff(n_tiles + 1), poff((size_t)pl->num_pages + 1);
-    OCTO_TRY(cuda_status(cudaMemcpyAsync(toff.data(), pl->tile_off, (n_tiles + 1) * 4, cudaMemcpyDeviceToHost, s)));
-    OCTO_TRY(cuda_status(
-        cudaMemcpyAsync(poff.data(), pl->page_off, ((size_t)pl->num_pages + 1) * 4, cudaMemcpyDeviceToHost, s)));
-    OCTO_TRY(cuda_status(cudaStreamSynchronize(s)));
-    std::vector<int32_t> tord(n_tiles);
-    for (int64_t t = 0; t < n_tiles; t++) tord[t] = (int32_t)t;
-    std::stable_sort(tord.begin(), tord.end(),
-                     [&](int32_t a, int32_t b) { return toff[a + 1] - toff[a] > toff[b + 1] - toff[b]; });
-    const bool any_touched = pl->info.n_touched_pages > 0;
-    // dK/dV work units: consecutive own pages of each segment, two at a time, among the
-    // touched pages; a touched page without a touched partner runs alone
-    if (!is_decode && any_touched) {
-      std::vector<int32_t> pp;
-      std::vector<char> seen((size_t)pl->num_pages, 0);
-      auto cnt = [&](int32_t pg) { return pg < 0 ? 0 : poff[pg + 1] - poff[pg]; };
-      for (const Segment& g : pool->segs) {
-        if (g.freed) continue;
-        int32_t pend = -1;
-        for (int32_t pg : g.pages) {
-          if (pg < 0 || pg >= pl->num_pages || cnt(pg) == 0 || seen[pg]) {
-            if (pend >= 0) { pp.push_back(pend); pp.push_back(-1); pend = -1; }
-            continue;
-          }
-          seen[pg] = 1;
-          if (pend < 0) {
-            pend = pg;
-          } else {
-            pp.push_back(pend);
-            pp.push_back(pg);
-            pend = -1;
-          }
-        }
-        if (pend >= 0) { pp.push_back(pend); pp.push_back(-1); }
-      }
-      for (int32_t pg = 0; pg < pl->num_pages; pg++)
-        if (cnt(pg) > 0 && !seen[pg]) { pp.push_back(pg); pp.push_back(-1); }
-      const int32_t np = (int32_t)(pp.size() / 2);
-      std::vector<int32_t> poff2(np + 1, 0), pord2(np);
-      for (int32_t i = 0; i < np; i++) {
-        poff2[i + 1] = poff2[i] + cnt(pp[2 * i]) + cnt(pp[2 * i + 1]);
-        pord2[i] = i;
-      }
-      std::stable_sort(pord2.begin(), pord2.end(), [&](int32_t a, int32_t b) {
-        return poff2[a + 1] - poff2[a] > poff2[b + 1] - poff2[b];
-      });
-      pl->n_pairs = np;
-      OCTO_TRY(dalloc(pl, &pl->pair_pages, pp.size(), s));
-      OCTO_TRY(dalloc(pl, &pl->pair_item_off, poff2.size(), s));
-      OCTO_TRY(dalloc(pl, &pl->pair_n_items, np, s));
-      OCTO_TRY(dalloc(pl, &pl->pair_order, np, s));
-      OCTO_TRY(dalloc(pl, &pl->pair_items, (size_t)n_entries, s));
-      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->pair_pages, pp.data(), pp.size() * 4, cudaMemcpyHostToDevice, s)));
-      OCTO_TRY(cuda_status(
-          cudaMemcpyAsync(pl->pair_item_off, poff2.data(), poff2.size() * 4, cudaMemcpyHostToDevice, s)));
-      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->pair_order, pord2.data(), np * 4, cudaMemcpyHostToDevice, s)));
-      k_pair_items<<<np, 256, 0, s>>>(pl->pair_pages, pl->pair_item_off, pl->page_off, pl->csc_perm, pl->entries,
-                                      n_entries, pl->tile_row0, pl->tile_rows, pl->pair_items, pl->pair_n_items);
-      count_launch();
-      OCTO_TRY(cuda_status(cudaGetLastError()));
-    }
-    OCTO_TRY(dalloc(pl, &pl->tile_order, n_tiles, s));
-    if (n_tiles > 0)
-      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->tile_order, tord.data(), n_tiles * 4, cudaMemcpyHostToDevice, s)));
-    // decode plans: split each cursor's entries into runs of kSplitEntries
-    std::vector<int32_t> sp_tile, sp_e0, sp_e1, sp_order, cur0(n_tiles + 1, 0);
-    if (is_decode) {
-      for (int64_t t = 0; t < n_tiles; t++) {
-        cur0[t] = (int32_t)sp_tile.size();
-        for (int32_t e = toff[t]; e < toff[t + 1]; e += kSplitEntries) {
-          sp_tile.push_back((int32_t)t);
-          sp_e0.push_back(e);
-          sp_e1.push_back(std::min(e + kSplitEntries, toff[t + 1]));
-        }
-      }
-      cur0[n_tiles] = (int32_t)sp_tile.size();
-      pl->n_splits = (int32_t)sp_tile.size();
-      OCTO_TRY(dalloc(pl, &pl->split_tile, sp_tile.size(), s));
-      OCTO_TRY(dalloc(pl, &pl->split_e0, sp_tile.size(), s));
-      OCTO_TRY(dalloc(pl, &pl->split_e1, sp_tile.size(), s));
-      OCTO_TRY(dalloc(pl, &pl->split_order, sp_tile.size(), s));
-      OCTO_TRY(dalloc(pl, &pl->cur_split0, cur0.size(), s));
-      if (!sp_tile.empty()) {
-        const int32_t ns = (int32_t)sp_tile.size();
-        size_t b = sp_tile.size() * 4;
-        OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_tile, sp_tile.data(), b, cudaMemcpyHostToDevice, s)));
-        OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_e0, sp_e0.data(), b, cudaMemcpyHostToDevice, s)));
-        OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_e1, sp_e1.data(), b, cudaMemcpyHostToDevice, s)));
-        // Launch order: by the first page a split reads (then cursor, then split).  A
-        // cursor's entries follow its context (prefix run, own run, mounted spans at their
-        // points), so cursors sharing a prefix have splits starting on the same page, and
-        // a mounted span's pages sit next to its owner's run: such splits start together
-        // and their repeated reads are served from L2.  The order array goes to
-        // split_order's buffer first as the first-page keys.
-        k_split_first_page<<<(ns + 255) / 256, 256, 0, s>>>(pl->entries, pl->split_e0, ns, pl->split_order);
-        count_launch();
-        OCTO_TRY(cuda_status(cudaGetLastError()));
-        std::vector<int32_t> first(ns);
-        OCTO_TRY(cuda_status(cudaMemcpyAsync(first.data(), pl->split_order, b, cudaMemcpyDeviceToHost, s)));
-        OCTO_TRY(cuda_status(cudaStreamSynchronize(s)));
-        sp_order.resize(ns);
-        for (int32_t i = 0; i < ns; i++) sp_order[i] = i;
-        std::stable_sort(sp_order.begin(), sp_order.end(), [&](int32_t a, int32_t c) { return first[a] < first[c]; });
-        OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->split_order, sp_order.data(), b, cudaMemcpyHostToDevice, s)));
-      }
-      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->cur_split0, cur0.data(), cur0.size() * 4, cudaMemcpyHostToDevice, s)));
-    }
-    // the host vectors are pageable and go out of scope
-    OCTO_TRY(cuda_status(cudaStreamSynchronize(s)));
-  }
+  OCTO_TRY(finish_plan(pl, s));
   *out = pl;
   return OCTO_OK;
 }
@@ -888,6 +967,60 @@ int octo_decode_plan(octo_pool_t pool, const octo_cursor_t* cursors, int32_t n, 
     if (pool->segs[c].len == 0) return OCTO_EINVAL;
   }
   return octo::compile_plan(pool, cursors, nullptr, n, true, 1, (cudaStream_t)stream, out);
+}
+
+int octo_decode_plan_advance(octo_plan_t pl, void* stream) {
+  using namespace octo;
+  if (!pl || !pl->info.is_decode) return OCTO_EINVAL;
+  octo_pool_s* pool = pl->pool;
+  const int32_t n = (int32_t)pl->info.n_tiles, P = pool->desc.page_size;
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((int32_t)pl->cur_seg.size() != n || (int32_t)pl->h_toff.size() != n + 1) return OCTO_ESTATE;
+  if (n == 0) return OCTO_OK;
+  // every cursor exactly one token longer, and nothing else in its context: no mount at or
+  // after the point where the new token sits (a mount at that point becomes visible to it)
+  std::vector<int32_t> adv(2 * (size_t)n), off((size_t)n + 1, 0);
+  int32_t mx = 0;
+  for (int32_t i = 0; i < n; i++) {
+    const int32_t c = pl->cur_seg[i], L = pl->cur_len[i];
+    if (c < 0 || c >= (int32_t)pool->segs.size()) return OCTO_ESTATE;
+    const Segment& g = pool->segs[c];
+    if (g.freed || g.len != L + 1 || L / P >= (int32_t)g.pages.size()) return OCTO_ESTATE;
+    for (int32_t mid : g.mounts)
+      if (pool->mounts[mid].m >= L) return OCTO_ESTATE;
+    adv[2 * i] = g.pages[L / P];
+    adv[2 * i + 1] = (L % P == 0) ? 1 : 0;
+    const int32_t cnt = pl->h_toff[i + 1] - pl->h_toff[i] + adv[2 * i + 1];
+    off[i + 1] = off[i] + cnt;
+    mx = std::max(mx, cnt);
+  }
+  // from here on the plan changes; an error leaves it unusable (destroy it)
+  pl->last_stream = s;
+  int32_t *d_adv = nullptr, *d_off = nullptr;
+  octo_entry* d_e = nullptr;
+  int st;
+  if ((st = dalloc(pl, &d_adv, adv.size(), s)) || (st = dalloc(pl, &d_off, off.size(), s)) ||
+      (st = dalloc(pl, &d_e, (size_t)off[n], s)))
+    return st;
+  OCTO_CUDA(cudaMemcpyAsync(d_adv, adv.data(), adv.size() * 4, cudaMemcpyHostToDevice, s));
+  OCTO_CUDA(cudaMemcpyAsync(d_off, off.data(), off.size() * 4, cudaMemcpyHostToDevice, s));
+  k_decode_advance<<<(unsigned)(((int64_t)n * 32 + 255) / 256), 256, 0, s>>>(pl->entries, pl->tile_off, d_off, d_adv, n,
+                                                                           d_e, pl->tile_t0, pl->row_pos);
+  count_launch();
+  OCTO_CUDA(cudaGetLastError());
+  dfree(pl, pl->entries, s);
+  dfree(pl, pl->tile_off, s);
+  dfree(pl, d_adv, s);
+  pl->entries = d_e;
+  pl->tile_off = d_off;
+  for (int32_t i = 0; i < n; i++) pl->cur_len[i] += 1;
+  pl->info.n_entries = off[n];
+  pl->info.max_tile_entries = mx;
+  // the entry-derived part, rebuilt exactly as a fresh compile builds it
+  for (void* p : pl->b_allocs) dfree(pl, p, s);
+  pl->b_allocs.clear();
+  OCTO_CUDA(cudaMemsetAsync(pl->d_scratch, 0, 8 * sizeof(int32_t), s));
+  return finish_plan(pl, s);  // ends with a stream synchronisation: adv and off outlive their copies
 }
 
 int octo_plan_info(octo_plan_t plan, octo_plan_info_t* info) {

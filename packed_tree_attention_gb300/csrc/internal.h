@@ -106,6 +106,13 @@ struct octo_plan_s {
   int32_t* split_order = nullptr;    // [n_splits] launch order: first page read, then cursor, then split
   int32_t* cur_split0 = nullptr;     // [n_tiles+1] first split of each cursor
   std::vector<void*> allocs;
+  // allocations of the entry-derived part (CSC, orders, pairs, splits): rebuilt on advance
+  std::vector<void*> b_allocs;
+  int32_t* d_cnt = nullptr;          // [max(n_tiles, num_pages)] compile scratch
+  int32_t* d_scratch = nullptr;      // [8] compile scratch (status, maxima, counts, pairs)
+  // decode plans: the cursors, their lengths when the plan was built or last advanced, and
+  // a host copy of tile_off
+  std::vector<int32_t> cur_seg, cur_len, h_toff;
   cudaStream_t last_stream = nullptr;  // stream of the last call that used the plan
 };
 
