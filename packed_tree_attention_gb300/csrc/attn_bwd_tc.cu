@@ -31,6 +31,7 @@
 
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "internal.h"
@@ -918,18 +919,17 @@ int bwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const
   prm.scale = scale;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.status = p->pool->d_status;
-  static bool attr = false;
-  if (!attr) {
-    OCTO_CUDA(cudaFuncSetAttribute(k_dkdv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDkSmem));
-    OCTO_CUDA(cudaFuncSetAttribute(k_dq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmem));
-    // the block sizes must fit the compiled register counts
-    cudaFuncAttributes fa;
+  if (int st = set_smem_limit((const void*)k_dkdv_tc, (int)kDkSmem)) return st;
+  if (int st = set_smem_limit((const void*)k_dq_tc, (int)kDqSmem)) return st;
+  // the block sizes must fit the compiled register counts (a property of the binary)
+  static std::atomic<int> fits{-1};
+  if (fits.load() < 0) {
+    cudaFuncAttributes fa, fb;
     OCTO_CUDA(cudaFuncGetAttributes(&fa, k_dkdv_tc));
-    if (fa.maxThreadsPerBlock < kDkThreads) return OCTO_ENOTSUP;
-    OCTO_CUDA(cudaFuncGetAttributes(&fa, k_dq_tc));
-    if (fa.maxThreadsPerBlock < kDqThreads) return OCTO_ENOTSUP;
-    attr = true;
+    OCTO_CUDA(cudaFuncGetAttributes(&fb, k_dq_tc));
+    fits.store(fa.maxThreadsPerBlock >= kDkThreads && fb.maxThreadsPerBlock >= kDqThreads ? 1 : 0);
   }
+  if (fits.load() == 0) return OCTO_ENOTSUP;
   const int64_t g1 = (int64_t)p->n_pairs * d.n_kv_heads;
   if (g1 > 0) {
     k_dkdv_tc<<<(unsigned)g1, kDkThreads, kDkSmem, s>>>(mq, mdo, mk, mv, prm);

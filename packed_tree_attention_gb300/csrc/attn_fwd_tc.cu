@@ -428,11 +428,7 @@ int fwd_tc(const octo_plan_s* p, int32_t Hq, const void* q, const void* k, const
   prm.G = Hq / d.n_kv_heads;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.status = p->pool->d_status;
-  static bool attr = false;
-  if (!attr) {
-    OCTO_CUDA(cudaFuncSetAttribute(k_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
-    attr = true;
-  }
+  if (int st = set_smem_limit((const void*)k_fwd_tc, (int)kSmemBytes)) return st;
   const int64_t grid = p->info.n_tiles * d.n_kv_heads * (prm.G / 2);
   if (grid > INT32_MAX) return OCTO_EINVAL;
   k_fwd_tc<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, prm);

@@ -366,11 +366,7 @@ __global__ void k_decode_combine(const float* __restrict__ part, const int32_t* 
 template <int GP>
 int launch_split(const DecParams& prm, dim3 grid, cudaStream_t s) {
   const int smem = DecShape<GP>::SMEM;
-  static bool attr = false;
-  if (!attr) {
-    OCTO_CUDA(cudaFuncSetAttribute(k_decode_split<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    attr = true;
-  }
+  if (int st = set_smem_limit((const void*)k_decode_split<GP>, smem)) return st;
   k_decode_split<GP><<<grid, kWarps * 32, smem, s>>>(prm);
   count_launch();
   return OCTO_OK;

@@ -120,6 +120,9 @@ namespace octo {
 
 extern thread_local int g_last_cuda_error;
 void count_launch(int n = 1);
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current device, once per
+// (kernel, device, size): the attribute is per device, and one process may drive several.
+int set_smem_limit(const void* func, int bytes);
 
 inline int cuda_status(cudaError_t e) {
   if (e != cudaSuccess) {

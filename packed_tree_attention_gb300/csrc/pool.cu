@@ -12,6 +12,9 @@
 #include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <mutex>
+#include <set>
+#include <tuple>
 
 #include "internal.h"
 
@@ -20,6 +23,19 @@ namespace octo {
 thread_local int g_last_cuda_error = 0;
 static std::atomic<int64_t> g_launches{0};
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int set_smem_limit(const void* func, int bytes) {
+  int dev = 0;
+  OCTO_CUDA(cudaGetDevice(&dev));
+  static std::mutex mu;
+  static std::set<std::tuple<const void*, int, int>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(func, dev, bytes);
+  if (done.count(key)) return OCTO_OK;
+  OCTO_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+  done.insert(key);
+  return OCTO_OK;
+}
 
 namespace {
 

@@ -365,14 +365,11 @@ int octo_token_logprob(octo_plan_t plan, int32_t row0, int32_t n_rows, const voi
   p.status = plan->pool->d_status;
   cudaStream_t s = (cudaStream_t)stream;
   plan->last_stream = s;
-  static bool attr = false;
-  if (!attr) {
-    OCTO_CUDA(cudaFuncSetAttribute(k_token_logprob<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kKeepBytes));
-    OCTO_CUDA(cudaFuncSetAttribute(k_token_logprob<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKeepBytes));
-    attr = true;
-  }
   const int smem = dlogits ? kKeepBytes : 0;
+  if (smem) {
+    const void* f = dtype == OCTO_DTYPE_BF16 ? (const void*)k_token_logprob<__nv_bfloat16> : (const void*)k_token_logprob<float>;
+    if (int st = set_smem_limit(f, smem)) return st;
+  }
   if (dtype == OCTO_DTYPE_BF16)
     k_token_logprob<__nv_bfloat16><<<n_rows, kThreads, smem, s>>>(p);
   else
