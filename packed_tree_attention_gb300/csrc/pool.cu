@@ -28,9 +28,9 @@ int set_smem_limit(const void* func, int bytes) {
   int dev = 0;
   OCTO_CUDA(cudaGetDevice(&dev));
   static std::mutex mu;
-  static std::set<std::tuple<const void*, int, int>> done;
+  static std::set<std::tuple<uintptr_t, int, int>> done;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_tuple(func, dev, bytes);
+  const auto key = std::make_tuple(reinterpret_cast<uintptr_t>(func), dev, bytes);
   if (done.count(key)) return OCTO_OK;
   OCTO_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
   done.insert(key);
