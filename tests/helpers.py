@@ -21,6 +21,17 @@ def header_symbols():
     return sorted(set(re.findall(r"\b(octo_[a-z_0-9]+)\s*\(", txt)))
 
 
+def header_param_counts():
+    """Number of parameters of every octo_ function the header declares (void = 0)."""
+    txt = open(os.path.join(ROOT, "include", "octopus.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(octo_[a-z_0-9]+)\s*\(([^;{]*?)\)\s*;", txt, flags=re.S):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
 def replay_host(pool, ep):
     """Replays the op log into a library pool without K/V (metadata only)."""
     for op in ep.ops:

@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 import synth
-from helpers import compare_pools, header_symbols, replay_host
+from helpers import compare_pools, header_param_counts, header_symbols, replay_host
 
 
 @pytest.fixture(scope="module")
@@ -22,6 +22,16 @@ def test_exports_every_header_symbol(lib):
     for s in syms:
         assert hasattr(L, s), s
     assert set(syms) == set(lib.SYMBOLS)
+
+
+def test_binding_argument_counts_match_header(lib):
+    """Every ctypes signature of the binding has as many arguments as the declaration."""
+    L = lib.load()
+    counts = header_param_counts()
+    assert set(counts) == set(lib.SYMBOLS)
+    for name, n in counts.items():
+        argtypes = getattr(L, name).argtypes
+        assert argtypes is not None and len(argtypes) == n, (name, n, argtypes)
 
 
 def test_strerror(lib):
