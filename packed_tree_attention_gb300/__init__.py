@@ -139,10 +139,16 @@ def launch_count() -> int:
 
 
 def _ptr(x):
+    """Address of a tensor argument.  The library reads plain pointers with the dense
+    layouts its header gives, so a view with gaps or reordered strides is refused here
+    rather than read wrongly."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if not x.is_contiguous():
+        raise ValueError("tensor arguments must be contiguous (got strides %s for shape %s)"
+                         % (tuple(x.stride()), tuple(x.shape)))
     return x.data_ptr()
 
 

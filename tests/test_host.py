@@ -34,6 +34,16 @@ def test_binding_argument_counts_match_header(lib):
         assert argtypes is not None and len(argtypes) == n, (name, n, argtypes)
 
 
+def test_tensor_arguments_must_be_dense(lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros((4, 6))
+    assert lib._ptr(x) == x.data_ptr()
+    assert lib._ptr(x[1:3]) == x[1:3].data_ptr()          # leading-row slices stay dense
+    for bad in (x.t(), x[:, :5], x[::2]):
+        with pytest.raises(ValueError):
+            lib._ptr(bad)
+
+
 def test_strerror(lib):
     L = lib.load()
     for code in range(7):
