@@ -67,5 +67,9 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
 
 
 if __name__ == "__main__":
+    # -v: ptxas register / spill report; --simt-only: the diagnostic build whose attention
+    # calls all take the CUDA-core kernels (forces a rebuild; rebuild without it afterwards)
     v = "-v" in sys.argv
-    print(build(force="-f" in sys.argv, verbose=v, extra=["-Xptxas", "-v"] if v else []))
+    simt = "--simt-only" in sys.argv
+    extra = (["-Xptxas", "-v"] if v else []) + (["-DOCTO_SIMT_ONLY"] if simt else [])
+    print(build(force="-f" in sys.argv or simt, verbose=v, extra=extra))
