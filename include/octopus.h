@@ -107,6 +107,8 @@ typedef struct {
   int32_t max_page_entries;
   int32_t n_touched_pages; /* pages some entry reads */
   int32_t is_decode;
+  int32_t n_rec_runs;      /* pack plans: runs of the recurrent layer (rows with one path predecessor chain) */
+  int32_t n_rec_chunks;    /* pack plans: their chunks of up to 64 rows */
 } octo_plan_info_t;
 
 /* ---- pool (host metadata; primitives table of the project page) ---- */
@@ -133,6 +135,18 @@ int octo_root(octo_pool_t pool, octo_cursor_t* out);
  * frozen, rewound away from or released. */
 int octo_append(octo_pool_t pool, octo_cursor_t cur, int32_t n, const void* k, const void* v,
                 void* stream, int32_t* pos_out);
+
+/* One token appended to each of n distinct cursors (a decode step's new tokens): the same
+ * pages, positions and zeroing as n octo_append calls of one token, in one call and two
+ * kernels.  k, v: device [n][n_kv_heads][head_dim] of the pool dtype, row i for cursors[i];
+ * both NULL = layout only.  rope_base > 0: the K rows are rotated at the positions their
+ * tokens receive, as octo_append_rope does; 0 = copied as given.  pos_out (host, n entries,
+ * may be NULL) receives the positions.  All or nothing: EINVAL (a cursor listed twice or
+ * out of range, a bad rope_base), ESTATE (a cursor frozen, rewound away from or
+ * released) and ENOMEM (fewer free pages than the cursors that open one) leave the pool
+ * unchanged.  Queued on `stream` without waiting for the device. */
+int octo_append_step(octo_pool_t pool, const octo_cursor_t* cursors, int32_t n, const void* k,
+                     const void* v, float rope_base, void* stream, int32_t* pos_out);
 
 /* fork: n children that each see the parent's current tokens and the mounts the parent
  * holds now (O(1): no page is allocated or copied; the parent's refcount grows by n).
@@ -166,9 +180,28 @@ int octo_unpin(octo_pool_t pool, octo_cursor_t cur);
  * are dropped in turn. */
 int octo_release(octo_pool_t pool, octo_cursor_t cur);
 
+/* Pool state in one call: the primitives table's refcounts ("+K refs" on fork, the pin of
+ * done) and page ownership.  Inputs: seg_capacity, and the optional host arrays refcount
+ * and n_pages ([seg_capacity] entries, indexed by segment id; EINVAL if seg_capacity is
+ * below the number of segments while either is given) and page_owner ([num_pages]: the
+ * segment owning each page, -1 for a free page).  Outputs: the counts. */
+typedef struct {
+  int32_t n_segments;    /* out: segments created so far (freed ones included) */
+  int32_t free_pages;    /* out */
+  int32_t n_mounts;      /* out: mounts made so far */
+  int32_t num_pages;     /* out */
+  int32_t seg_capacity;  /* in */
+  int32_t* refcount;     /* in/out, may be NULL: live cursor + live children + mounts reading it + pin (0 when freed) */
+  int32_t* n_pages;      /* in/out, may be NULL: pages the segment owns */
+  int32_t* page_owner;   /* in/out, may be NULL */
+} octo_pool_state;
+int octo_pool_query(octo_pool_t pool, octo_pool_state* state);
+
+/* The counts of octo_pool_query alone. */
 int octo_pool_info(octo_pool_t pool, int32_t* n_segments, int32_t* free_pages,
                    int32_t* n_mounts);
-/* pos (len entries) and pages (n_pages entries) are optional host outputs. */
+/* One segment: its record, and the optional host outputs pos (len entries: each token's
+ * position) and pages (n_pages entries: its own pages in token order). */
 int octo_seg_query(octo_pool_t pool, octo_cursor_t seg, octo_seg_info* info, int32_t* pos,
                    int32_t* pages);
 
@@ -194,14 +227,20 @@ int octo_decode_plan(octo_pool_t pool, const octo_cursor_t* cursors, int32_t n, 
  * one token appended (octo_append / octo_append_rope) since the plan was built or last
  * advanced: the result equals octo_decode_plan on the same cursors, array for array and
  * bit for bit (octopus project page, "Architecture & Co-Design" item 01: a turn extends
- * a cursor over the same shared pages, so the view needs only the new token; the pages
- * quote 128K prompt assembly in 1.44 ms).  Only the newest token's page entry changes
- * per cursor; the CSC view, launch orders and split-KV runs are rebuilt from the entries.
+ * a cursor over the same shared pages, so the view changes only by the new token; the
+ * pages quote 128K prompt assembly in 1.44 ms).  Per cursor, the newest token either
+ * widens the entry of its own last page or, when it opens a page, adds that page's entry
+ * at the end of the cursor's list.  When no cursor opens a page this is one kernel that
+ * updates the plan in place; otherwise the entries, the CSC view, page offsets and touched
+ * pages are rebuilt by device kernels from the old ones, and the split-KV runs and launch
+ * orders from host copies kept with the plan.  It never waits for the device; the work is
+ * queued on `stream`, ordered after the work queued on the stream that last used the plan.
  * OCTO_ESTATE, with the plan unchanged, when a cursor is not exactly one token longer, was
- * freed, or has a mount at or after the point of its new token (its context then grows by
- * more than that token): build a fresh plan instead.  On any other error the plan must be
- * destroyed.  The plan can have more split-KV runs afterwards: query
- * octo_decode_workspace_size again.  Synchronises `stream` (twice). */
+ * freed, has a mount at or after the point of its new token (its context then grows by
+ * more than that token), or is listed twice in the plan: build a fresh plan instead.
+ * Segments whose pages the plan reads must not be released in between.  On any other
+ * error the plan must be destroyed.  The plan can have more split-KV runs afterwards:
+ * query octo_decode_workspace_size again. */
 int octo_decode_plan_advance(octo_plan_t plan, void* stream);
 
 int octo_plan_info(octo_plan_t plan, octo_plan_info_t* info);
@@ -284,7 +323,50 @@ int octo_token_logprob(octo_plan_t plan, int32_t row0, int32_t n_rows, const voi
                        float* row_lse, void* dlogits, float grad_scale, float* loss, void* ws, size_t ws_bytes,
                        void* stream);
 
-/* ---- attention (device, async on stream) ---- */
+/* ---- tree-packed recurrent layer (gated delta rule), device, async on stream ----
+ * ia.com.br summary, associative versus working memory: the hybrid model pairs attention
+ * with linear-recurrent layers (Gated DeltaNet / Mamba-2) whose state is the branch's
+ * working memory.  Octopus project page, five-primitives table: fork clones the recurrent
+ * checkpoint at the fork point, rewind restores the exact state of step k, and
+ * read_thread's mounted span is skipped by the recurrent layers; "Architecture &
+ * Co-Design" item 03: the packed pass carries the recurrent boundary checkpoints.
+ * Per head, state S [head_dim x head_dim] (rows: value dimension):
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = S_t q_t,
+ * S_{t-1} the state after the row before t on its path (the previous own row; for a
+ * segment's first row the parent's row at the fork or rewind point minus one, through
+ * forks at point 0), S = 0 before a path's first row; mounts change nothing.  The gate
+ * activations, feature maps and normalisation are the caller's: q, k, v, alpha, beta
+ * arrive as they enter the recurrence.  Computed in chunks of 64 rows along runs of the
+ * pack plan, fp32 on the CUDA cores. */
+
+/* Workspace bytes of octo_recurrent_fwd / bwd for this pack plan (0 on bad arguments). */
+size_t octo_recurrent_workspace_size(octo_plan_t plan, int32_t n_heads, int32_t head_dim);
+
+/* Forward over a pack plan's rows: q, k, v, o fp32 [n_rows][n_heads][head_dim]; alpha, beta
+ * fp32 [n_rows][n_heads], alpha in (0, 1] (its log is taken), beta any finite value.
+ * head_dim 64 or 128 (EINVAL otherwise, and for a decode plan).  ws: device workspace of
+ * octo_recurrent_workspace_size bytes; the forward leaves in it the chunk states the
+ * backward reads, so pass the same ws, unchanged, to octo_recurrent_bwd.  Deterministic. */
+int octo_recurrent_fwd(octo_plan_t plan, int32_t n_heads, int32_t head_dim, const float* q,
+                       const float* k, const float* v, const float* alpha, const float* beta,
+                       float* o, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of octo_recurrent_fwd for the same inputs and workspace: with dout the gradient
+ * of the loss with respect to o, writes dq, dk, dv [n_rows][n_heads][head_dim] and dalpha,
+ * dbeta [n_rows][n_heads] (fp32).  A row with several successors (a fork or rewind point)
+ * receives the sum of their state gradients, taken in a fixed order. */
+int octo_recurrent_bwd(octo_plan_t plan, int32_t n_heads, int32_t head_dim, const float* q,
+                       const float* k, const float* v, const float* alpha, const float* beta,
+                       const float* dout, float* dq, float* dk, float* dv, float* dalpha,
+                       float* dbeta, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- packed DAG attention (device, async on stream) ----
+ * Octopus project page, "Architecture & Co-Design" item 03 (Training): one unpadded 1D
+ * packed forward/backward pass over the branched trees and their live mount edges, with
+ * single-ownership masking (every token stored and owned once; each query row sees its
+ * tree-ancestor path and the spans mounted on it), the reader's gradients routed directly
+ * into the producer's KV; the ia.com.br summary calls it a block-sparse attention pass.
+ * The schedule is the plan's entry list; attention itself is softmax(scale q k^T) v. */
 
 /* Forward over a packed plan.  For query head h the kv head is h / (n_q_heads /
  * n_kv_heads).  q, o: [n_rows][n_q_heads][head_dim] of the pool dtype; lse: fp32
@@ -308,16 +390,39 @@ int octo_attn_bwd(octo_plan_t plan, int32_t n_q_heads, const void* q, const void
                   float* dq, float* dk_pool, float* dv_pool, float scale, void* ws,
                   size_t ws_bytes, void* stream);
 
-/* Workspace bytes octo_decode needs. */
+/* ---- paged decode over cursors ----
+ * Octopus project page, "Architecture & Co-Design" item 01 (Runtime): cursors stay resident
+ * on the serving side over shared KV pages, and each turn extends a cursor; item 02 and
+ * the primitives table, row read_thread: a reader's attention also sees its mounted
+ * sibling spans, read in place.  Decoding one token per cursor is the last row of a packed
+ * pass over that cursor's context.  The decode takes a plan (octo_decode_plan) so that the
+ * context walk is done once and the plan moved on by one token per step
+ * (octo_decode_plan_advance) while the kernel streams the pages; octo_decode_cursors does
+ * all of it in one call. */
+
+/* Workspace bytes octo_decode needs for this plan and head count (split-KV partials). */
 size_t octo_decode_workspace_size(octo_plan_t plan, int32_t n_q_heads);
 
 /* Paged decode over a decode plan: for cursor i and query head h, out[i][h] =
  * softmax(scale * q[i][h] . K_ctx) V_ctx over the cursor's context (its last token
- * included).  q, out: [n][n_q_heads][head_dim] of the pool dtype; lse: fp32
- * [n][n_q_heads] (may be NULL). */
+ * included), kv head h / (n_q_heads / n_kv_heads).  q, out: [n][n_q_heads][head_dim] of
+ * the pool dtype (device); lse: fp32 [n][n_q_heads] natural log (may be NULL).  ws: device
+ * workspace of octo_decode_workspace_size bytes (EINVAL if smaller).  k_pool / v_pool NULL
+ * = the pool's arrays.  Async on stream; the split partials are combined in a fixed
+ * order, so results are deterministic. */
 int octo_decode(octo_plan_t plan, int32_t n_q_heads, const void* q, const void* k_pool,
                 const void* v_pool, void* out, float* lse, float scale, void* ws,
                 size_t ws_bytes, void* stream);
+
+/* The decode straight from cursors: octo_decode_plan, octo_decode, octo_plan_destroy in one
+ * call (arguments as there).  ws may be NULL: the library then takes the workspace from
+ * the stream-ordered allocator (cudaMallocAsync on `stream`) and returns it after the
+ * decode.  Synchronises the stream once (the plan compile).  A caller decoding the same
+ * cursors step after step keeps a plan and advances it instead. */
+int octo_decode_cursors(octo_pool_t pool, const octo_cursor_t* cursors, int32_t n,
+                        int32_t n_q_heads, const void* q, const void* k_pool, const void* v_pool,
+                        void* out, float* lse, float scale, void* ws, size_t ws_bytes,
+                        void* stream);
 
 /* Allocation-free variant of octo_decode, for callers that must not allocate device
  * memory: engines whose device memory is all handed out by their own allocator at
@@ -329,8 +434,9 @@ int octo_decode(octo_plan_t plan, int32_t n_q_heads, const void* q, const void* 
  * bytes (32 MiB) that every GPU which loads the library holds until the process exits.
  * A call needs octo_decode_workspace_size(plan, n_q_heads) bytes of it; larger requests
  * return OCTO_ESCRATCH and launch nothing.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture.  The call itself allocates nothing.  Every call
+ * array's device address (cudaGetSymbolAddress) with that device current, once per CUDA
+ * context (again after the context is destroyed and made anew, e.g. by cudaDeviceReset);
+ * make that first call before any stream capture.  The call itself allocates nothing.  Every call
  * shares the one array and each call overwrites the part it reads before reading it, so
  * nothing needs clearing between calls -- but calls that overlap on the GPU (on different
  * streams, or on different host threads) race on it and must be serialised by the
@@ -346,6 +452,14 @@ int octo_last_cuda_error(void);   /* last cudaError_t seen by the library */
 /* Waits for the stream, then returns the device status word of the pool's plans
  * (OCTO_ETIMEOUT if a bounded wait expired) and clears it. */
 int octo_sync(octo_plan_t plan, void* stream);
+/* Self-test of the failure path of the kernels' bounded waits (the pages have no
+ * counterpart): one CTA waits, through the same bounded mbarrier wait the tensor-core and
+ * decode kernels use, on a barrier phase that nothing completes, gives up after max_polls
+ * polls (1 .. 2^27), records OCTO_ETIMEOUT in the status word of the plan's pool and
+ * returns.  No copy or MMA is in flight and nothing else is written, so the context stays
+ * usable: the next octo_sync on the plan returns OCTO_ETIMEOUT (and clears it), and later
+ * calls run normally.  Async on stream. */
+int octo_wait_selftest(octo_plan_t plan, uint32_t max_polls, void* stream);
 /* Which kernel family octo_attn_fwd / bwd / decode will use for this plan:
  * 0 = CUDA-core (SIMT) kernels, 1 = tcgen05 tensor-core kernels (the backward takes them
  * only with a nonzero scale), 2 = split-KV decode kernels.  which: 0 fwd, 1 bwd,

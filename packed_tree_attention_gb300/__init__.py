@@ -48,12 +48,19 @@ class _SegInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("parent", "fork", "len", "n_pages", "refcount", "p_next", "flags")]
 
 
+class _PoolState(ctypes.Structure):
+    _fields_ = [("n_segments", ctypes.c_int32), ("free_pages", ctypes.c_int32), ("n_mounts", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("seg_capacity", ctypes.c_int32),
+                ("refcount", ctypes.POINTER(ctypes.c_int32)), ("n_pages", ctypes.POINTER(ctypes.c_int32)),
+                ("page_owner", ctypes.POINTER(ctypes.c_int32))]
+
+
 class _PlanInfo(ctypes.Structure):
     _fields_ = [("n_rows", ctypes.c_int64), ("n_tiles", ctypes.c_int64), ("n_entries", ctypes.c_int64),
                 ("n_segments", ctypes.c_int64), ("pairs", ctypes.c_int64), ("bm", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("max_tile_entries", ctypes.c_int32),
                 ("max_page_entries", ctypes.c_int32), ("n_touched_pages", ctypes.c_int32),
-                ("is_decode", ctypes.c_int32)]
+                ("is_decode", ctypes.c_int32), ("n_rec_runs", ctypes.c_int32), ("n_rec_chunks", ctypes.c_int32)]
 
 
 ENTRY_DTYPE = np.dtype([("q_tile", "<u4"), ("kv_page", "<u4"), ("kv_lo", "<u2"), ("kv_hi", "<u2"),
@@ -68,7 +75,8 @@ SYMBOLS = ("octo_pool_create", "octo_pool_destroy", "octo_root", "octo_append", 
            "octo_decode", "octo_strerror", "octo_last_cuda_error", "octo_sync", "octo_kernel_path",
            "octo_launch_count", "octo_decode_noalloc", "octo_append_rope", "octo_rope_rows",
            "octo_rope_pool_grad", "octo_token_logprob_workspace_size", "octo_token_logprob",
-           "octo_decode_plan_advance")
+           "octo_decode_plan_advance", "octo_pool_query", "octo_decode_cursors", "octo_recurrent_workspace_size",
+           "octo_recurrent_fwd", "octo_recurrent_bwd", "octo_wait_selftest", "octo_append_step")
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
@@ -119,6 +127,13 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "octo_token_logprob_workspace_size": [I32, ctypes.POINTER(SZ)],
         "octo_token_logprob": [P, I32, I32, P, I32, ctypes.c_int64, I32, P, P, P, P, P, F, P, P, SZ, P],
         "octo_decode_plan_advance": [P, P],
+        "octo_pool_query": [P, ctypes.POINTER(_PoolState)],
+        "octo_decode_cursors": [P, IP, I32, I32, P, P, P, P, P, F, P, SZ, P],
+        "octo_recurrent_workspace_size": [P, I32, I32],
+        "octo_wait_selftest": [P, ctypes.c_uint32, P],
+        "octo_append_step": [P, IP, I32, P, P, F, P, IP],
+        "octo_recurrent_fwd": [P, I32, I32, P, P, P, P, P, P, P, SZ, P],
+        "octo_recurrent_bwd": [P, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -127,6 +142,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.octo_strerror.restype = ctypes.c_char_p
     L.octo_attn_bwd_workspace_size.restype = SZ
     L.octo_decode_workspace_size.restype = SZ
+    L.octo_recurrent_workspace_size.restype = SZ
     L.octo_launch_count.argtypes = []
     L.octo_launch_count.restype = ctypes.c_int64
     _lib = L
@@ -213,6 +229,17 @@ class Pool:
         _chk(st, "octo_append_rope")
         return pos[:n]
 
+    def append_step(self, cursors, k=None, v=None, rope_base=0.0, stream=None, check=True):
+        """octo_append_step: one token for each of the (distinct) cursors in one call."""
+        c = np.ascontiguousarray(cursors, dtype=np.int32)
+        pos = np.zeros(max(len(c), 1), dtype=np.int32)
+        st = self._L.octo_append_step(self.h, _ip(c), len(c), _ptr(k), _ptr(v), float(rope_base), _stream(stream),
+                                      _ip(pos))
+        if not check:
+            return st
+        _chk(st, "octo_append_step")
+        return pos[:len(c)]
+
     def fork(self, cur, n, check=True):
         out = np.zeros(max(n, 1), dtype=np.int32)
         st = self._L.octo_fork(self.h, cur, n, _ip(out))
@@ -259,6 +286,30 @@ class Pool:
         a, b, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
         _chk(self._L.octo_pool_info(self.h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)), "octo_pool_info")
         return dict(n_segments=a.value, free_pages=b.value, n_mounts=c.value)
+
+    def query(self):
+        """octo_pool_query: counts, every segment's refcount and page count, and the owner
+        of every page (-1 free)."""
+        n = self.info()["n_segments"]
+        rc = np.zeros(max(n, 1), dtype=np.int32)
+        npg = np.zeros(max(n, 1), dtype=np.int32)
+        own = np.zeros(self.num_pages, dtype=np.int32)
+        st = _PoolState(0, 0, 0, 0, len(rc), _ip(rc), _ip(npg), _ip(own))
+        _chk(self._L.octo_pool_query(self.h, ctypes.byref(st)), "octo_pool_query")
+        return dict(n_segments=st.n_segments, free_pages=st.free_pages, n_mounts=st.n_mounts,
+                    num_pages=st.num_pages, refcount=rc[:st.n_segments], n_pages=npg[:st.n_segments],
+                    page_owner=own)
+
+    def decode_cursors(self, cursors, n_q_heads, q, out, lse, scale, ws=None, ws_bytes=None, k_pool=None,
+                       v_pool=None, stream=None):
+        """octo_decode_cursors: plan, decode and plan release in one call (ws None: the
+        library takes the workspace from the stream-ordered allocator)."""
+        c = np.ascontiguousarray(cursors, dtype=np.int32)
+        if ws_bytes is None:
+            ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+        _chk(self._L.octo_decode_cursors(self.h, _ip(c), len(c), n_q_heads, _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                         _ptr(out), _ptr(lse), float(scale), _ptr(ws), ws_bytes, _stream(stream)),
+             "octo_decode_cursors")
 
     def seg_info(self, s):
         i = _SegInfo()
@@ -391,8 +442,30 @@ class Plan:
                                         float(grad_scale), _ptr(loss), _ptr(ws), ws.numel() * ws.element_size(),
                                         _stream(stream)), "octo_token_logprob")
 
+    def recurrent_workspace_size(self, n_heads, head_dim):
+        return int(self._L.octo_recurrent_workspace_size(self.h, n_heads, head_dim))
+
+    def recurrent_fwd(self, n_heads, head_dim, q, k, v, alpha, beta, o, ws, stream=None):
+        """octo_recurrent_fwd: the gated delta rule over the packed rows (fp32); ws keeps what
+        the backward needs."""
+        _chk(self._L.octo_recurrent_fwd(self.h, n_heads, head_dim, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                                        _ptr(beta), _ptr(o), _ptr(ws), ws.numel() * ws.element_size(),
+                                        _stream(stream)), "octo_recurrent_fwd")
+
+    def recurrent_bwd(self, n_heads, head_dim, q, k, v, alpha, beta, dout, dq, dk, dv, dalpha, dbeta, ws,
+                      stream=None):
+        """octo_recurrent_bwd: gradients of octo_recurrent_fwd (same inputs and workspace)."""
+        _chk(self._L.octo_recurrent_bwd(self.h, n_heads, head_dim, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                                        _ptr(beta), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha),
+                                        _ptr(dbeta), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+             "octo_recurrent_bwd")
+
     def sync(self, stream=None):
         _chk(self._L.octo_sync(self.h, _stream(stream)), "octo_sync")
+
+    def wait_selftest(self, max_polls, stream=None):
+        """octo_wait_selftest: a bounded device wait that expires (OCTO_ETIMEOUT at the next sync)."""
+        _chk(self._L.octo_wait_selftest(self.h, max_polls, _stream(stream)), "octo_wait_selftest")
 
     def kernel_path(self, n_q_heads, which):
         return int(self._L.octo_kernel_path(self.h, n_q_heads, which))

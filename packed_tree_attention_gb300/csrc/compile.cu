@@ -374,6 +374,77 @@ __global__ void k_decode_advance(const octo_entry* __restrict__ old_e, const int
   }
 }
 
+// Advance of a decode plan in which no cursor's newest token opens a page: in place, one
+// thread per cursor.  The newest token sits on the cursor's last own page, whose entry is
+// the last path entry (src -1) of the cursor's list (mounts placed after it in context
+// order come later and are skipped); it widens by one slot, and the row moves on.
+__global__ void k_decode_widen(octo_entry* __restrict__ entries, const int32_t* __restrict__ tile_off, int32_t n,
+                               int32_t* __restrict__ tile_t0, int32_t* __restrict__ row_pos) {
+  const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  for (int32_t k = tile_off[i + 1] - 1; k >= tile_off[i]; k--)
+    if (entries[k].src == -1) {
+      entries[k].kv_hi = (uint16_t)(entries[k].kv_hi + 1);
+      break;
+    }
+  tile_t0[i] += 1;
+  row_pos[i] += 1;
+}
+
+// number of values of the ascending array a[0, n) below x
+__device__ __forceinline__ int32_t count_below(const int32_t* __restrict__ a, int32_t n, int32_t x) {
+  int32_t lo = 0, hi = n;
+  while (lo < hi) {
+    const int32_t mid = (lo + hi) >> 1;
+    if (a[mid] < x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// CSC of an advanced decode plan whose fresh pages (ascending, none read before) each get
+// one entry: an old position k of page p moves up by the fresh pages below p and its entry
+// index by the entries inserted before its cursor; each fresh page lists its new entry.
+// Threads [0, n_old) move the old positions, [n_old, n_old + n) place the cursors' new
+// entries.  adv[2 i] = cursor i's newest page, adv[2 i + 1] = 1 if it is fresh.
+__global__ void k_csc_advance(const int32_t* __restrict__ old_csc, const octo_entry* __restrict__ old_e,
+                              int32_t n_old, const int32_t* __restrict__ old_off, const int32_t* __restrict__ new_off,
+                              const int32_t* __restrict__ old_page_off, const int32_t* __restrict__ fresh_pages,
+                              int32_t m, const int32_t* __restrict__ adv, int32_t n, int32_t* __restrict__ out) {
+  const int32_t k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k < n_old) {
+    const int32_t e = old_csc[k];
+    const octo_entry x = old_e[e];
+    const int32_t t = (int32_t)x.q_tile;
+    out[k + count_below(fresh_pages, m, (int32_t)x.kv_page)] = e + (new_off[t] - old_off[t]);
+  } else if (k < n_old + n) {
+    const int32_t i = k - n_old;
+    if (adv[2 * i + 1]) {
+      const int32_t p = adv[2 * i];
+      out[old_page_off[p] + count_below(fresh_pages, m, p)] = new_off[i + 1] - 1;
+    }
+  }
+}
+
+// page_off after adding one entry on each fresh page
+__global__ void k_pageoff_advance(const int32_t* __restrict__ old_page_off, int32_t num_pages,
+                                  const int32_t* __restrict__ fresh_pages, int32_t m, int32_t* __restrict__ out) {
+  const int32_t p = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p <= num_pages) out[p] = old_page_off[p] + count_below(fresh_pages, m, p);
+}
+
+// ascending merge of the touched pages with the fresh ones
+__global__ void k_touched_advance(const int32_t* __restrict__ old_t, int32_t n_old,
+                                  const int32_t* __restrict__ fresh_pages, int32_t m, int32_t* __restrict__ out) {
+  const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n_old) {
+    out[i + count_below(fresh_pages, m, old_t[i])] = old_t[i];
+  } else if (i < n_old + m) {
+    const int32_t k = i - n_old;
+    out[count_below(old_t, n_old, fresh_pages[k]) + k] = fresh_pages[k];
+  }
+}
+
 // kv_page of the first entry of each split (decode plans)
 __global__ void k_split_first_page(const octo_entry* __restrict__ entries, const int32_t* __restrict__ split_e0,
                                    int32_t n, int32_t* __restrict__ out) {
@@ -546,14 +617,6 @@ int dalloc(octo_plan_s* pl, T** ptr, size_t n, cudaStream_t s) {
   return OCTO_OK;
 }
 
-// an allocation of the entry-derived part of a plan (rebuilt when a decode plan advances)
-template <typename T>
-int dalloc_b(octo_plan_s* pl, T** ptr, size_t n, cudaStream_t s) {
-  if (int st = dalloc(pl, ptr, n, s)) return st;
-  pl->b_allocs.push_back(*ptr);
-  return OCTO_OK;
-}
-
 // frees one of the plan's allocations, stream-ordered
 void dfree(octo_plan_s* pl, void* p, cudaStream_t s) {
   auto it = std::find(pl->allocs.begin(), pl->allocs.end(), p);
@@ -581,8 +644,8 @@ void dfree(octo_plan_s* pl, void* p, cudaStream_t s) {
 
 // The parts of a plan that follow from its entries: the CSC view, the pair count and page
 // statistics, the launch orders, and the dK/dV page pairs (training plans) or the split-KV
-// runs (decode plans).  Everything it allocates is listed in b_allocs, so that a decode
-// plan advanced by a token can drop and rebuild it.  Ends with a stream synchronisation.
+// runs (decode plans, whose host copies are kept for octo_decode_plan_advance).  Ends with
+// a stream synchronisation.
 int finish_plan(octo_plan_s* pl, cudaStream_t s) {
   octo_pool_s* pool = pl->pool;
   const bool is_decode = pl->info.is_decode != 0;
@@ -590,7 +653,7 @@ int finish_plan(octo_plan_s* pl, cudaStream_t s) {
   const int32_t n_entries = pl->info.n_entries;
   int32_t* d_cnt = pl->d_cnt;
   int32_t* d_scratch = pl->d_scratch;
-  OCTO_RET(dalloc_b(pl, &pl->csc_perm, n_entries, s));
+  OCTO_RET(dalloc(pl, &pl->csc_perm, n_entries, s));
   // ---- CSC ----
   OCTO_RET(cuda_status(cudaMemsetAsync(d_cnt, 0, (size_t)pl->num_pages * 4, s)));
   if (n_entries > 0) {
@@ -677,11 +740,11 @@ int finish_plan(octo_plan_s* pl, cudaStream_t s) {
         return poff2[a + 1] - poff2[a] > poff2[b + 1] - poff2[b];
       });
       pl->n_pairs = np;
-      OCTO_RET(dalloc_b(pl, &pl->pair_pages, pp.size(), s));
-      OCTO_RET(dalloc_b(pl, &pl->pair_item_off, poff2.size(), s));
-      OCTO_RET(dalloc_b(pl, &pl->pair_n_items, np, s));
-      OCTO_RET(dalloc_b(pl, &pl->pair_order, np, s));
-      OCTO_RET(dalloc_b(pl, &pl->pair_items, (size_t)n_entries, s));
+      OCTO_RET(dalloc(pl, &pl->pair_pages, pp.size(), s));
+      OCTO_RET(dalloc(pl, &pl->pair_item_off, poff2.size(), s));
+      OCTO_RET(dalloc(pl, &pl->pair_n_items, np, s));
+      OCTO_RET(dalloc(pl, &pl->pair_order, np, s));
+      OCTO_RET(dalloc(pl, &pl->pair_items, (size_t)n_entries, s));
       OCTO_RET(cuda_status(cudaMemcpyAsync(pl->pair_pages, pp.data(), pp.size() * 4, cudaMemcpyHostToDevice, s)));
       OCTO_RET(cuda_status(
           cudaMemcpyAsync(pl->pair_item_off, poff2.data(), poff2.size() * 4, cudaMemcpyHostToDevice, s)));
@@ -691,7 +754,7 @@ int finish_plan(octo_plan_s* pl, cudaStream_t s) {
       count_launch();
       OCTO_RET(cuda_status(cudaGetLastError()));
     }
-    OCTO_RET(dalloc_b(pl, &pl->tile_order, n_tiles, s));
+    OCTO_RET(dalloc(pl, &pl->tile_order, n_tiles, s));
     if (n_tiles > 0)
       OCTO_RET(cuda_status(cudaMemcpyAsync(pl->tile_order, tord.data(), n_tiles * 4, cudaMemcpyHostToDevice, s)));
     // decode plans: split each cursor's entries into runs of kSplitEntries
@@ -707,11 +770,11 @@ int finish_plan(octo_plan_s* pl, cudaStream_t s) {
       }
       cur0[n_tiles] = (int32_t)sp_tile.size();
       pl->n_splits = (int32_t)sp_tile.size();
-      OCTO_RET(dalloc_b(pl, &pl->split_tile, sp_tile.size(), s));
-      OCTO_RET(dalloc_b(pl, &pl->split_e0, sp_tile.size(), s));
-      OCTO_RET(dalloc_b(pl, &pl->split_e1, sp_tile.size(), s));
-      OCTO_RET(dalloc_b(pl, &pl->split_order, sp_tile.size(), s));
-      OCTO_RET(dalloc_b(pl, &pl->cur_split0, cur0.size(), s));
+      OCTO_RET(dalloc(pl, &pl->split_tile, sp_tile.size(), s));
+      OCTO_RET(dalloc(pl, &pl->split_e0, sp_tile.size(), s));
+      OCTO_RET(dalloc(pl, &pl->split_e1, sp_tile.size(), s));
+      OCTO_RET(dalloc(pl, &pl->split_order, sp_tile.size(), s));
+      OCTO_RET(dalloc(pl, &pl->cur_split0, cur0.size(), s));
       if (!sp_tile.empty()) {
         const int32_t ns = (int32_t)sp_tile.size();
         size_t b = sp_tile.size() * 4;
@@ -734,8 +797,14 @@ int finish_plan(octo_plan_s* pl, cudaStream_t s) {
         for (int32_t i = 0; i < ns; i++) sp_order[i] = i;
         std::stable_sort(sp_order.begin(), sp_order.end(), [&](int32_t a, int32_t c) { return first[a] < first[c]; });
         OCTO_RET(cuda_status(cudaMemcpyAsync(pl->split_order, sp_order.data(), b, cudaMemcpyHostToDevice, s)));
+        pl->h_sp_first = first;
       }
       OCTO_RET(cuda_status(cudaMemcpyAsync(pl->cur_split0, cur0.data(), cur0.size() * 4, cudaMemcpyHostToDevice, s)));
+      pl->h_sp_tile = sp_tile;
+      pl->h_sp_e0 = sp_e0;
+      pl->h_sp_e1 = sp_e1;
+      pl->h_sp_order = sp_order;
+      pl->h_cur0 = cur0;
     }
     // the host vectors are pageable and go out of scope
     OCTO_RET(cuda_status(cudaStreamSynchronize(s)));
@@ -832,6 +901,7 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
 
   // ---- path predecessors of the packed rows (training plans) ----
   std::vector<int32_t> spred, ep, er;  // pageable sources of async copies: kept to the end
+  std::vector<int32_t> runs, chunks, lruns, coff, clist;
   if (!is_decode && n_segs > 0) {
     std::vector<int32_t> rbase(n_segs), kpos(nseg_all, -1);
     spred.assign(n_segs, -1);
@@ -873,6 +943,66 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
     if (!ex.empty()) {
       OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->succ_pred, ep.data(), ep.size() * 4, cudaMemcpyHostToDevice, s)));
       OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->succ_row, er.data(), er.size() * 4, cudaMemcpyHostToDevice, s)));
+    }
+    // runs and chunks of the recurrent layer: cut at every segment start and after every
+    // row another segment continues from (a row with several successors)
+    std::vector<char> cut((size_t)acc + 1, 0);
+    for (int32_t k = 0; k < n_segs; k++) {
+      cut[rbase[k]] = 1;
+      if (spred[k] >= 0) cut[spred[k] + 1] = 1;
+    }
+    std::vector<int32_t> end_run((size_t)acc, -1);
+    std::vector<int32_t> lvl;
+    for (int32_t k = 0; k < n_segs; k++) {
+      const int32_t b = rbase[k], e = b + pool->segs[seg_order_host[k]].len;
+      for (int32_t r0 = b; r0 < e;) {
+        int32_t r1 = r0 + 1;
+        while (r1 < e && !cut[r1]) r1++;
+        const int32_t pred = (r0 == b) ? spred[k] : r0 - 1;
+        const int32_t pr = pred >= 0 ? end_run[pred] : -1;
+        const int32_t id = (int32_t)(runs.size() / 4);
+        runs.insert(runs.end(), {r0, r1, pr, (int32_t)(chunks.size() / 2)});
+        for (int32_t c = r0; c < r1; c += kRecChunk) chunks.insert(chunks.end(), {c, std::min(kRecChunk, r1 - c)});
+        lvl.push_back(pr >= 0 ? lvl[pr] + 1 : 0);
+        end_run[r1 - 1] = id;
+        r0 = r1;
+      }
+    }
+    const int32_t nr = (int32_t)lvl.size();
+    pl->n_runs = nr;
+    pl->n_chunks = (int32_t)(chunks.size() / 2);
+    pl->info.n_rec_runs = nr;
+    pl->info.n_rec_chunks = pl->n_chunks;
+    pl->n_levels = nr ? *std::max_element(lvl.begin(), lvl.end()) + 1 : 0;
+    pl->h_level_off.assign(pl->n_levels + 1, 0);
+    for (int32_t l : lvl) pl->h_level_off[l + 1]++;
+    for (int32_t l = 0; l < pl->n_levels; l++) pl->h_level_off[l + 1] += pl->h_level_off[l];
+    lruns.resize(nr);
+    {
+      std::vector<int32_t> fill(pl->h_level_off.begin(), pl->h_level_off.end() - (pl->n_levels ? 1 : 0));
+      for (int32_t i = 0; i < nr; i++) lruns[fill[lvl[i]]++] = i;
+    }
+    coff.assign(nr + 1, 0);
+    for (int32_t i = 0; i < nr; i++)
+      if (runs[4 * i + 2] >= 0) coff[runs[4 * i + 2] + 1]++;
+    for (int32_t i = 0; i < nr; i++) coff[i + 1] += coff[i];
+    clist.resize(std::max(nr, 1));
+    {
+      std::vector<int32_t> fill(coff.begin(), coff.end() - 1);
+      for (int32_t i = 0; i < nr; i++)
+        if (runs[4 * i + 2] >= 0) clist[fill[runs[4 * i + 2]]++] = i;
+    }
+    OCTO_TRY(dalloc(pl, &pl->run_info, runs.size(), s));
+    OCTO_TRY(dalloc(pl, &pl->run_child_off, coff.size(), s));
+    OCTO_TRY(dalloc(pl, &pl->run_child, clist.size(), s));
+    OCTO_TRY(dalloc(pl, &pl->level_runs, lruns.size(), s));
+    OCTO_TRY(dalloc(pl, &pl->chunk_info, chunks.size(), s));
+    if (nr > 0) {
+      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->run_info, runs.data(), runs.size() * 4, cudaMemcpyHostToDevice, s)));
+      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->run_child_off, coff.data(), coff.size() * 4, cudaMemcpyHostToDevice, s)));
+      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->run_child, clist.data(), clist.size() * 4, cudaMemcpyHostToDevice, s)));
+      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->level_runs, lruns.data(), lruns.size() * 4, cudaMemcpyHostToDevice, s)));
+      OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->chunk_info, chunks.data(), chunks.size() * 4, cudaMemcpyHostToDevice, s)));
     }
   }
 
@@ -925,6 +1055,9 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
   pl->d_scratch = d_scratch;
   if (is_decode) {
     pl->cur_seg.assign(tile_segs_host, tile_segs_host + n_segs);
+    std::vector<int32_t> sorted_cur(pl->cur_seg);
+    std::sort(sorted_cur.begin(), sorted_cur.end());
+    pl->dup_cursors = std::adjacent_find(sorted_cur.begin(), sorted_cur.end()) != sorted_cur.end();
     pl->cur_len.resize(n_segs);
     for (int32_t i = 0; i < n_segs; i++) pl->cur_len[i] = pool->segs[tile_segs_host[i]].len;
   }
@@ -939,6 +1072,7 @@ extern "C" {
 
 int octo_pack_tree(octo_pool_t pool, const octo_cursor_t* roots, int32_t n_roots, int32_t bm, void* stream,
                    octo_plan_t* out) {
+  octo::NvtxRange nv("octo_pack_tree");
   if (!pool || !out || n_roots < 0 || (n_roots > 0 && !roots) || bm < 1 || bm > 128) return OCTO_EINVAL;
   const int32_t nseg = (int32_t)pool->segs.size();
   std::vector<int32_t> root_of(nseg, -1);
@@ -960,6 +1094,7 @@ int octo_pack_tree(octo_pool_t pool, const octo_cursor_t* roots, int32_t n_roots
 }
 
 int octo_decode_plan(octo_pool_t pool, const octo_cursor_t* cursors, int32_t n, void* stream, octo_plan_t* out) {
+  octo::NvtxRange nv("octo_decode_plan");
   if (!pool || !out || n < 0 || (n > 0 && !cursors)) return OCTO_EINVAL;
   for (int32_t i = 0; i < n; i++) {
     int32_t c = cursors[i];
@@ -971,16 +1106,21 @@ int octo_decode_plan(octo_pool_t pool, const octo_cursor_t* cursors, int32_t n, 
 
 int octo_decode_plan_advance(octo_plan_t pl, void* stream) {
   using namespace octo;
+  NvtxRange nv("octo_decode_plan_advance");
   if (!pl || !pl->info.is_decode) return OCTO_EINVAL;
   octo_pool_s* pool = pl->pool;
   const int32_t n = (int32_t)pl->info.n_tiles, P = pool->desc.page_size;
   cudaStream_t s = (cudaStream_t)stream;
-  if ((int32_t)pl->cur_seg.size() != n || (int32_t)pl->h_toff.size() != n + 1) return OCTO_ESTATE;
+  if ((int32_t)pl->cur_seg.size() != n || (int32_t)pl->h_toff.size() != n + 1 || pl->dup_cursors) return OCTO_ESTATE;
   if (n == 0) return OCTO_OK;
   // every cursor exactly one token longer, and nothing else in its context: no mount at or
   // after the point where the new token sits (a mount at that point becomes visible to it)
-  std::vector<int32_t> adv(2 * (size_t)n), off((size_t)n + 1, 0);
+  std::vector<int32_t>& stage = pl->h_stage;
+  stage.assign(3 * (size_t)n + 1, 0);
+  int32_t* adv = stage.data();             // [2 n] newest page, fresh flag
+  int32_t* off = stage.data() + 2 * n;     // [n + 1] new tile_off
   int32_t mx = 0;
+  std::vector<int32_t> fresh_pages;
   for (int32_t i = 0; i < n; i++) {
     const int32_t c = pl->cur_seg[i], L = pl->cur_len[i];
     if (c < 0 || c >= (int32_t)pool->segs.size()) return OCTO_ESTATE;
@@ -990,37 +1130,130 @@ int octo_decode_plan_advance(octo_plan_t pl, void* stream) {
       if (pool->mounts[mid].m >= L) return OCTO_ESTATE;
     adv[2 * i] = g.pages[L / P];
     adv[2 * i + 1] = (L % P == 0) ? 1 : 0;
+    if (adv[2 * i + 1]) fresh_pages.push_back(adv[2 * i]);
     const int32_t cnt = pl->h_toff[i + 1] - pl->h_toff[i] + adv[2 * i + 1];
     off[i + 1] = off[i] + cnt;
     mx = std::max(mx, cnt);
   }
-  // from here on the plan changes; an error leaves it unusable (destroy it)
+  // from here on the plan changes; an error leaves it unusable (destroy it).  The plan's
+  // arrays are rewritten and freed in order after the work already queued on the stream
+  // that last used them.
+  if (pl->last_stream != s) {
+    if (!pl->order_ev) OCTO_CUDA(cudaEventCreateWithFlags(&pl->order_ev, cudaEventDisableTiming));
+    OCTO_CUDA(cudaEventRecord(pl->order_ev, pl->last_stream));
+    OCTO_CUDA(cudaStreamWaitEvent(s, pl->order_ev, 0));
+  }
   pl->last_stream = s;
-  int32_t *d_adv = nullptr, *d_off = nullptr;
-  octo_entry* d_e = nullptr;
+  const int32_t m = (int32_t)fresh_pages.size();
+  if (m == 0) {
+    // no entry moves: the cursors' own-page entries widen in place
+    k_decode_widen<<<(n + 255) / 256, 256, 0, s>>>(pl->entries, pl->tile_off, n, pl->tile_t0, pl->row_pos);
+    count_launch();
+    OCTO_CUDA(cudaGetLastError());
+    for (int32_t i = 0; i < n; i++) pl->cur_len[i] += 1;
+    pl->info.pairs += n;
+    return OCTO_OK;
+  }
+  std::sort(fresh_pages.begin(), fresh_pages.end());
+  // split-KV runs of kSplitEntries entries per cursor: existing runs keep their first
+  // entry (entries are only added at the end of a cursor's list); a cursor whose list was
+  // a whole number of runs starts a new one on its fresh page
+  std::vector<int32_t> sp_tile, sp_e0, sp_e1, sp_first, cur0(n + 1, 0);
+  for (int32_t i = 0; i < n; i++) {
+    cur0[i] = (int32_t)sp_tile.size();
+    const int32_t old_runs = pl->h_cur0[i + 1] - pl->h_cur0[i];
+    for (int32_t e = off[i], j = 0; e < off[i + 1]; e += kSplitEntries, j++) {
+      sp_tile.push_back(i);
+      sp_e0.push_back(e);
+      sp_e1.push_back(std::min(e + kSplitEntries, off[i + 1]));
+      sp_first.push_back(j < old_runs ? pl->h_sp_first[pl->h_cur0[i] + j] : adv[2 * i]);
+    }
+  }
+  const int32_t ns = (int32_t)sp_tile.size();
+  cur0[n] = ns;
+  std::vector<int32_t> sp_order;
+  if (ns == pl->n_splits) {
+    sp_order = pl->h_sp_order;   // same runs, same first pages: same launch order
+  } else {
+    sp_order.resize(ns);
+    for (int32_t i = 0; i < ns; i++) sp_order[i] = i;
+    std::stable_sort(sp_order.begin(), sp_order.end(),
+                     [&](int32_t a, int32_t c) { return sp_first[a] < sp_first[c]; });
+  }
+  std::vector<int32_t> tord(n);
+  for (int32_t t = 0; t < n; t++) tord[t] = t;
+  std::stable_sort(tord.begin(), tord.end(),
+                   [&](int32_t a, int32_t b) { return off[a + 1] - off[a] > off[b + 1] - off[b]; });
+  // one upload: adv | tile_off | fresh pages | split cursor, first, end, order | first split
+  // per cursor | tile order
+  const size_t o_fp = 3 * (size_t)n + 1, o_st = o_fp + m, o_e0 = o_st + ns, o_e1 = o_e0 + ns,
+               o_so = o_e1 + ns, o_c0 = o_so + ns, o_to = o_c0 + n + 1, total = o_to + n;
+  stage.resize(total);
+  adv = stage.data();
+  off = stage.data() + 2 * n;
+  std::copy(fresh_pages.begin(), fresh_pages.end(), stage.begin() + o_fp);
+  std::copy(sp_tile.begin(), sp_tile.end(), stage.begin() + o_st);
+  std::copy(sp_e0.begin(), sp_e0.end(), stage.begin() + o_e0);
+  std::copy(sp_e1.begin(), sp_e1.end(), stage.begin() + o_e1);
+  std::copy(sp_order.begin(), sp_order.end(), stage.begin() + o_so);
+  std::copy(cur0.begin(), cur0.end(), stage.begin() + o_c0);
+  std::copy(tord.begin(), tord.end(), stage.begin() + o_to);
+  const int32_t e_old = (int32_t)pl->info.n_entries, e_new = off[n];
+  const int32_t t_old = pl->info.n_touched_pages;
+  int32_t *buf = nullptr, *csc = nullptr, *poff = nullptr, *touched = nullptr;
+  octo_entry* ent = nullptr;
   int st;
-  if ((st = dalloc(pl, &d_adv, adv.size(), s)) || (st = dalloc(pl, &d_off, off.size(), s)) ||
-      (st = dalloc(pl, &d_e, (size_t)off[n], s)))
+  if ((st = dalloc(pl, &buf, total, s)) || (st = dalloc(pl, &ent, (size_t)e_new, s)) ||
+      (st = dalloc(pl, &csc, (size_t)e_new, s)) || (st = dalloc(pl, &poff, (size_t)pl->num_pages + 1, s)) ||
+      (st = dalloc(pl, &touched, (size_t)t_old + m, s)))
     return st;
-  OCTO_CUDA(cudaMemcpyAsync(d_adv, adv.data(), adv.size() * 4, cudaMemcpyHostToDevice, s));
-  OCTO_CUDA(cudaMemcpyAsync(d_off, off.data(), off.size() * 4, cudaMemcpyHostToDevice, s));
+  // pageable source: staged by the runtime before the call returns
+  OCTO_CUDA(cudaMemcpyAsync(buf, stage.data(), total * 4, cudaMemcpyHostToDevice, s));
+  const int32_t* d_adv = buf;
+  int32_t* d_off = buf + 2 * n;
+  const int32_t* d_fp = buf + o_fp;
   k_decode_advance<<<(unsigned)(((int64_t)n * 32 + 255) / 256), 256, 0, s>>>(pl->entries, pl->tile_off, d_off, d_adv, n,
-                                                                           d_e, pl->tile_t0, pl->row_pos);
-  count_launch();
+                                                                           ent, pl->tile_t0, pl->row_pos);
+  k_csc_advance<<<(unsigned)((e_old + n + 255) / 256), 256, 0, s>>>(pl->csc_perm, pl->entries, e_old, pl->tile_off,
+                                                                   d_off, pl->page_off, d_fp, m, d_adv, n, csc);
+  k_pageoff_advance<<<(unsigned)((pl->num_pages + 1 + 255) / 256), 256, 0, s>>>(pl->page_off, pl->num_pages, d_fp, m,
+                                                                               poff);
+  k_touched_advance<<<(unsigned)((t_old + m + 255) / 256), 256, 0, s>>>(pl->touched, t_old, d_fp, m, touched);
+  count_launch(4);
   OCTO_CUDA(cudaGetLastError());
-  dfree(pl, pl->entries, s);
-  dfree(pl, pl->tile_off, s);
-  dfree(pl, d_adv, s);
-  pl->entries = d_e;
+  // the replaced arrays go back in stream order (arrays that lived in the previous
+  // advance's buffer are not allocations of their own: dfree skips them)
+  for (void* p : {(void*)pl->entries, (void*)pl->csc_perm, (void*)pl->page_off, (void*)pl->touched,
+                  (void*)pl->tile_off, (void*)pl->split_tile, (void*)pl->split_e0, (void*)pl->split_e1,
+                  (void*)pl->split_order, (void*)pl->cur_split0, (void*)pl->tile_order, pl->adv_buf})
+    if (p) dfree(pl, p, s);
+  pl->adv_buf = buf;
+  pl->entries = ent;
+  pl->csc_perm = csc;
+  pl->page_off = poff;
+  pl->touched = touched;
   pl->tile_off = d_off;
+  pl->split_tile = buf + o_st;
+  pl->split_e0 = buf + o_e0;
+  pl->split_e1 = buf + o_e1;
+  pl->split_order = buf + o_so;
+  pl->cur_split0 = buf + o_c0;
+  pl->tile_order = buf + o_to;
+  pl->n_splits = ns;
+  pl->h_toff.assign(off, off + n + 1);
+  pl->h_sp_tile = std::move(sp_tile);
+  pl->h_sp_e0 = std::move(sp_e0);
+  pl->h_sp_e1 = std::move(sp_e1);
+  pl->h_sp_first = std::move(sp_first);
+  pl->h_sp_order = std::move(sp_order);
+  pl->h_cur0 = std::move(cur0);
   for (int32_t i = 0; i < n; i++) pl->cur_len[i] += 1;
-  pl->info.n_entries = off[n];
+  pl->info.n_entries = e_new;
   pl->info.max_tile_entries = mx;
-  // the entry-derived part, rebuilt exactly as a fresh compile builds it
-  for (void* p : pl->b_allocs) dfree(pl, p, s);
-  pl->b_allocs.clear();
-  OCTO_CUDA(cudaMemsetAsync(pl->d_scratch, 0, 8 * sizeof(int32_t), s));
-  return finish_plan(pl, s);  // ends with a stream synchronisation: adv and off outlive their copies
+  pl->info.max_page_entries = std::max(pl->info.max_page_entries, 1);
+  pl->info.n_touched_pages = t_old + m;
+  pl->info.pairs += n;
+  return OCTO_OK;
 }
 
 int octo_plan_info(octo_plan_t plan, octo_plan_info_t* info) {
@@ -1057,6 +1290,7 @@ int octo_plan_destroy(octo_plan_t pl) {
   // stream-ordered: the arrays go back to the pool only after the work already enqueued
   // on the plan's last stream has finished with them
   for (void* p : pl->allocs) cudaFreeAsync(p, pl->last_stream);
+  if (pl->order_ev) cudaEventDestroy(pl->order_ev);
   delete pl;
   return OCTO_OK;
 }

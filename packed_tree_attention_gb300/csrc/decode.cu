@@ -34,6 +34,8 @@
 #include <cuda_bf16.h>
 
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "internal.h"
 #include "tc_common.cuh"
@@ -437,24 +439,56 @@ namespace {
 // One per device that loads the library, alive until the process exits.
 static __device__ __align__(256) unsigned char g_decode_scratch[OCTO_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
+// Scratch addresses already looked up, keyed by the unique id of the CUDA context that was
+// current (cuCtxGetId): a device address belongs to one context, and a context destroyed
+// and made again (cudaDeviceReset, or another context made current on the same device)
+// loads the module afresh, so an address cached per device ordinal could be stale.
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+std::vector<std::pair<unsigned long long, void*>> g_scratch_by_ctx;
 
-// Device address of the scratch array on the current device, looked up once per device
-// (cudaGetSymbolAddress with that device current).
-int scratch_for_current_device(void** out) {
-  int dev = 0;
-  OCTO_CUDA(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) return OCTO_ENOTSUP;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* ptr = nullptr;
-    OCTO_CUDA(cudaGetSymbolAddress(&ptr, g_decode_scratch));
-    if (!ptr) return OCTO_ECUDA;
-    g_scratch_ptr[dev] = ptr;
+int current_context_id(unsigned long long* id) {
+  using GetCur = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCur get_cur = nullptr;
+  static GetId get_id = nullptr;
+  if (!get_cur || !get_id) {
+    void *a = nullptr, *b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) != cudaSuccess ||
+        qa != cudaDriverEntryPointSuccess || qb != cudaDriverEntryPointSuccess || !a || !b)
+      return OCTO_ECUDA;
+    get_cur = reinterpret_cast<GetCur>(a);
+    get_id = reinterpret_cast<GetId>(b);
   }
-  *out = g_scratch_ptr[dev];
+  CUcontext ctx = nullptr;
+  if (get_cur(&ctx) != CUDA_SUCCESS) return OCTO_ECUDA;
+  if (!ctx) {
+    // no context current yet: cudaSetDevice makes the device's primary context current
+    int dev = 0;
+    OCTO_CUDA(cudaGetDevice(&dev));
+    OCTO_CUDA(cudaSetDevice(dev));
+    if (get_cur(&ctx) != CUDA_SUCCESS || !ctx) return OCTO_ECUDA;
+  }
+  return get_id(ctx, id) == CUDA_SUCCESS ? OCTO_OK : OCTO_ECUDA;
+}
+
+// Device address of the scratch array in the current context, looked up once per context
+// (cudaGetSymbolAddress with that context's device current).
+int scratch_for_current_device(void** out) {
+  unsigned long long id = 0;
+  if (int st = current_context_id(&id)) return st;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  for (const auto& e : g_scratch_by_ctx)
+    if (e.first == id) {
+      *out = e.second;
+      return OCTO_OK;
+    }
+  void* ptr = nullptr;
+  OCTO_CUDA(cudaGetSymbolAddress(&ptr, g_decode_scratch));
+  if (!ptr) return OCTO_ECUDA;
+  g_scratch_by_ctx.emplace_back(id, ptr);
+  *out = ptr;
   return OCTO_OK;
 }
 

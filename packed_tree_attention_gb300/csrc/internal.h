@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include <set>
@@ -98,6 +99,17 @@ struct octo_plan_s {
   int32_t* succ_pred = nullptr;      // [n_succ_extra] predecessor row, ascending
   int32_t* succ_row = nullptr;       // [n_succ_extra] first row of the continuing segment
   int32_t max_succ = 0;              // most successors of one row
+  // tree-packed recurrent layer: the packed rows cut into runs -- a new run at every
+  // segment start and after every row that other segments continue from -- so a run
+  // starts from the state after one row (its predecessor run's last row, or nothing) and
+  // no row inside a run feeds another run.  Runs are cut into chunks of kRecChunk rows.
+  int32_t n_runs = 0, n_chunks = 0, n_levels = 0;
+  int32_t* run_info = nullptr;       // [n_runs][4] first row, end row, predecessor run (-1 none), first chunk
+  int32_t* run_child_off = nullptr;  // [n_runs + 1] runs continuing from each run's last row
+  int32_t* run_child = nullptr;      // [n_runs] (ascending run ids per run)
+  int32_t* level_runs = nullptr;     // [n_runs] run ids by level (a run's level = its predecessor's + 1)
+  int32_t* chunk_info = nullptr;     // [n_chunks][2] first row, rows
+  std::vector<int32_t> h_level_off;  // [n_levels + 1] level slices of level_runs
   // decode plans: runs of up to kSplitEntries entries of one cursor (split-KV)
   int32_t n_splits = 0;
   int32_t* split_tile = nullptr;     // [n_splits] cursor (tile) of the split
@@ -106,13 +118,18 @@ struct octo_plan_s {
   int32_t* split_order = nullptr;    // [n_splits] launch order: first page read, then cursor, then split
   int32_t* cur_split0 = nullptr;     // [n_tiles+1] first split of each cursor
   std::vector<void*> allocs;
-  // allocations of the entry-derived part (CSC, orders, pairs, splits): rebuilt on advance
-  std::vector<void*> b_allocs;
   int32_t* d_cnt = nullptr;          // [max(n_tiles, num_pages)] compile scratch
   int32_t* d_scratch = nullptr;      // [8] compile scratch (status, maxima, counts, pairs)
   // decode plans: the cursors, their lengths when the plan was built or last advanced, and
-  // a host copy of tile_off
+  // host copies of tile_off and of the split-KV tables (split cursor, first / end entry,
+  // kv page of the first entry, launch order, first split per cursor), kept so that an
+  // advance by one token per cursor updates them without reading the device
   std::vector<int32_t> cur_seg, cur_len, h_toff;
+  std::vector<int32_t> h_sp_tile, h_sp_e0, h_sp_e1, h_sp_first, h_sp_order, h_cur0;
+  bool dup_cursors = false;          // a cursor listed twice (advance then refuses)
+  std::vector<int32_t> h_stage;      // staging of the small arrays an advance uploads
+  void* adv_buf = nullptr;           // device copy of the last advance's small arrays
+  cudaEvent_t order_ev = nullptr;    // orders an advance after work on another stream
   cudaStream_t last_stream = nullptr;  // stream of the last call that used the plan
 };
 
@@ -152,7 +169,16 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
                  bool is_decode, int32_t bm, cudaStream_t s, octo_plan_s** out);
 
 constexpr int32_t kSplitEntries = 32;
+constexpr int32_t kRecChunk = 64;   // rows per chunk of the tree-packed recurrent layer
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// An NVTX range over the scope (seen by nsys / ncu range filters; a no-op without a tool).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 }  // namespace octo

@@ -290,6 +290,65 @@ int octo_append_rope(octo_pool_t p, octo_cursor_t c, int32_t n, const void* k, c
   return append_impl(p, c, n, k, v, stream, pos_out, true, base);
 }
 
+int octo_append_step(octo_pool_t p, const octo_cursor_t* cursors, int32_t n, const void* k, const void* v,
+                     float rope_base, void* stream, int32_t* pos_out) {
+  octo::NvtxRange nv("octo_append_step");
+  if (!p || n < 0 || (n > 0 && !cursors)) return OCTO_EINVAL;
+  if ((k == nullptr) != (v == nullptr)) return OCTO_EINVAL;
+  const bool rope = rope_base != 0.f;
+  if (rope && octo::rope_validate(p->desc.head_dim, rope_base)) return OCTO_EINVAL;
+  const int32_t P = p->desc.page_size;
+  // checks first, so that a refused call changes nothing
+  std::vector<int32_t> sorted(cursors, cursors + n);
+  std::sort(sorted.begin(), sorted.end());
+  if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) return OCTO_EINVAL;
+  int64_t need = 0;
+  for (int32_t i = 0; i < n; i++) {
+    const int32_t c = cursors[i];
+    if (c < 0 || c >= (int32_t)p->segs.size()) return OCTO_EINVAL;
+    if (!writable(p, c)) return OCTO_ESTATE;
+    const Segment& g = p->segs[c];
+    if ((int64_t)g.len + 1 > INT32_MAX / 2) return OCTO_EINVAL;
+    if ((int64_t)g.len / P >= (int64_t)g.pages.size()) need++;
+  }
+  if (need > (int64_t)p->free_pages.size()) return OCTO_ENOMEM;
+  // host arrays for the device: fresh pages | destination slots | positions
+  std::vector<int32_t> host;
+  host.reserve((size_t)need + 2 * (size_t)n);
+  std::vector<int32_t> dst(n), pos(n);
+  for (int32_t i = 0; i < n; i++) {
+    Segment& g = p->segs[cursors[i]];
+    if (g.len / P >= (int32_t)g.pages.size()) {
+      auto it = p->free_pages.begin();
+      g.pages.push_back(*it);
+      host.push_back(*it);
+      p->free_pages.erase(it);
+    }
+    dst[i] = g.pages[g.len / P] * P + g.len % P;
+    pos[i] = g.p_next;
+    if (pos_out) pos_out[i] = g.p_next;
+    g.pos.push_back(g.p_next++);
+    g.len += 1;
+  }
+  p->seq++;
+  const int32_t n_fresh = (int32_t)host.size();
+  const bool zero = n_fresh > 0 && p->desc.k_pool && p->desc.v_pool;
+  if (!zero && !(k && n > 0)) return OCTO_OK;
+  host.insert(host.end(), dst.begin(), dst.end());
+  host.insert(host.end(), pos.begin(), pos.end());
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* d_buf = nullptr;
+  OCTO_CUDA(cudaMallocAsync((void**)&d_buf, sizeof(int32_t) * host.size(), s));
+  // pageable source: staged by the runtime before the call returns, so `host` may go
+  OCTO_CUDA(cudaMemcpyAsync(d_buf, host.data(), sizeof(int32_t) * host.size(), cudaMemcpyHostToDevice, s));
+  int st = zero ? octo::launch_zero_pages(p->desc, d_buf, n_fresh, s) : OCTO_OK;
+  if (st == OCTO_OK && k && n > 0)
+    st = rope ? octo::launch_append_rope(p->desc, d_buf + n_fresh, d_buf + n_fresh + n, n, k, v, rope_base, s)
+              : octo::launch_append_rows(p->desc, d_buf + n_fresh, n, k, v, s);
+  OCTO_CUDA(cudaFreeAsync(d_buf, s));
+  return st;
+}
+
 int octo_fork(octo_pool_t p, octo_cursor_t c, int32_t n, octo_cursor_t* out) {
   if (!p || !out || n < 1 || c < 0 || c >= (int32_t)p->segs.size()) return OCTO_EINVAL;
   if (!writable(p, c)) return OCTO_ESTATE;
@@ -391,6 +450,30 @@ int octo_pool_info(octo_pool_t p, int32_t* n_segments, int32_t* free_pages, int3
   if (n_segments) *n_segments = (int32_t)p->segs.size();
   if (free_pages) *free_pages = (int32_t)p->free_pages.size();
   if (n_mounts) *n_mounts = (int32_t)p->mounts.size();
+  return OCTO_OK;
+}
+
+int octo_pool_query(octo_pool_t p, octo_pool_state* st) {
+  if (!p || !st || st->seg_capacity < 0) return OCTO_EINVAL;
+  const int32_t ns = (int32_t)p->segs.size(), np = p->desc.num_pages;
+  if ((st->refcount || st->n_pages) && st->seg_capacity < ns) return OCTO_EINVAL;
+  for (int32_t s = 0; s < ns; s++) {
+    const Segment& g = p->segs[s];
+    if (st->refcount) st->refcount[s] = g.freed ? 0 : g.refcount;
+    if (st->n_pages) st->n_pages[s] = (int32_t)g.pages.size();
+  }
+  if (st->page_owner) {
+    std::fill(st->page_owner, st->page_owner + np, -1);
+    for (int32_t s = 0; s < ns; s++) {
+      const Segment& g = p->segs[s];
+      if (g.freed) continue;
+      for (int32_t pg : g.pages) st->page_owner[pg] = s;
+    }
+  }
+  st->n_segments = ns;
+  st->free_pages = (int32_t)p->free_pages.size();
+  st->n_mounts = (int32_t)p->mounts.size();
+  st->num_pages = np;
   return OCTO_OK;
 }
 

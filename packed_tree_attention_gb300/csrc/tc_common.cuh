@@ -60,13 +60,17 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Returns false (after writing
-// `code` into *status) if the wait gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status, int32_t code) {
-  for (uint32_t i = 0; i < kSpinLimit; i++)
+// Waits for the phase with the given parity to complete, polling at most `limit` times.
+// Returns false (after writing `code` into *status) if the wait gave up.
+__device__ __forceinline__ bool mbar_wait_n(uint64_t* bar, uint32_t parity, int32_t* status, int32_t code,
+                                            uint32_t limit) {
+  for (uint32_t i = 0; i < limit; i++)
     if (mbar_try(bar, parity)) return true;
   atomicExch(status, code);
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status, int32_t code) {
+  return mbar_wait_n(bar, parity, status, code, kSpinLimit);
 }
 
 // ---- TMA ----

@@ -93,8 +93,12 @@ class Episode:
             return False
         return not any((x, p) in self.mounted for x in lin)
 
-    def mount(self, r: int, p: int, a: int, b: int) -> None:
-        assert self.can_mount(r, p) and 0 <= a < b <= self.length[p]
+    def mount(self, r: int, p: int, a: int, b: int, checked: bool = True) -> None:
+        """checked=False records a mount that can_mount's conservative rule would refuse
+        (an ancestor's tokens past the fork point, a second span of a producer already
+        mounted on the lineage); the caller has made sure the pool accepts it."""
+        assert 0 <= a < b <= self.length[p] and self.appendable[r]
+        assert not checked or self.can_mount(r, p)
         self.ops.append(("mount", r, p, a, b))
         self.mounted.add((r, p))
 
@@ -115,6 +119,8 @@ CONFIGS = {
     "episode": dict(Hq=16, Hkv=4, d=128, P=64, dtype="bf16", scale=0.5),
     # bf16 training step over 8 trees, forward + backward
     "train_step": dict(Hq=16, Hkv=4, d=128, P=64, dtype="bf16", scale=0.5),
+    # the first tree of the training step alone (the small case of its ncu captures)
+    "train_tree": dict(Hq=16, Hkv=4, d=128, P=64, dtype="bf16", scale=0.5),
     # paged decode, 256 cursors
     "decode": dict(Hq=16, Hkv=4, d=128, P=64, dtype="bf16", scale=0.5),
     # the same cursor shape, 4 episodes x 8 cursors (about 1 GB of K/V: profiling runs)
@@ -212,7 +218,8 @@ def _episode(seed: int) -> Episode:
 
 def _train_step(seed: int, n_trees: int = 8, target: int = 140_000) -> Episode:
     """8 random trees: root prefix, fork fan-out 2-6 per level, depth <= 3, branch
-    growth <= 32K, 0-4 mounts per reader of 0.5-8K, each tree ~140K owned tokens."""
+    growth <= 32K, 0-4 mounts per reader of 0.5-8K, each tree 140K owned tokens (1.12M
+    in all)."""
     rng = np.random.default_rng(np.random.PCG64(seed))
     ep = Episode(64)
     for _ in range(n_trees):
@@ -249,16 +256,9 @@ def _random_tree(ep: Episode, rng, target: int) -> None:
                 frontier.append((kid, depth + 1))
             else:
                 leaves.append(kid)
-    # top up the leaves round-robin until the tree owns ~target tokens, with mounts
+    # 0-4 mounts per reader leaf, spans of 0.5-8K from non-lineage segments of this tree,
+    # each followed by a few of the reader's own tokens
     leaves = [c for c in leaves if ep.appendable[c]]
-    li = 0
-    while total < target and leaves:
-        c = leaves[li % len(leaves)]
-        n = min(int(rng.integers(512, 4097)), target - total)
-        ep.append(c, n)
-        total += n
-        li += 1
-    # 0-4 mounts per reader leaf, spans of 0.5-8K from non-lineage segments of this tree
     tree_segs = [s for s in range(r, ep.n_segments)]
     for c in leaves:
         nm = int(rng.integers(0, 5))
@@ -270,7 +270,17 @@ def _random_tree(ep: Episode, rng, target: int) -> None:
             span = min(int(rng.integers(512, 8193)), ep.length[p])
             a = int(rng.integers(0, ep.length[p] - span + 1))
             ep.mount(c, p, a, a + span)
-            ep.append(c, int(rng.integers(64, 1025)))
+            n = min(int(rng.integers(64, 1025)), max(0, target - total))
+            ep.append(c, n)
+            total += n
+    # then top the leaves up round-robin until the tree owns exactly `target` tokens
+    li = 0
+    while total < target and leaves:
+        c = leaves[li % len(leaves)]
+        n = min(int(rng.integers(512, 4097)), target - total)
+        ep.append(c, n)
+        total += n
+        li += 1
 
 
 def _decode(seed: int, n_episodes: int = 32, per_episode: int = 8) -> Episode:
@@ -355,6 +365,8 @@ def make_preset(name: str, seed: int = 0) -> Episode:
         return _episode(seed)
     if name == "train_step":
         return _train_step(seed)
+    if name == "train_tree":
+        return _train_step(seed, n_trees=1)
     if name == "decode":
         return _decode(seed)
     if name == "decode_small":
@@ -484,14 +496,15 @@ def hash_fill(stream: int, shape, dtype, device, scale: float = 1.0, row_start: 
     return out
 
 
-def hash_rows(stream: int, rows, row_size: int, dtype, scale: float = 1.0):
-    """CPU values of selected rows (numpy int array of row ids) of a hash_fill tensor:
-    float64 array [len(rows), row_size] holding the dtype-rounded values."""
+def hash_rows(stream: int, rows, row_size: int, dtype, scale: float = 1.0, device="cpu"):
+    """Values of selected rows (numpy int array of row ids) of a hash_fill tensor, as a
+    numpy float64 array [len(rows), row_size] holding the dtype-rounded values; computed
+    on `device` (identical bits on any device)."""
     import torch
-    r = torch.as_tensor(np.asarray(rows, dtype=np.int64))
-    idx = (r[:, None] * row_size + torch.arange(row_size, dtype=torch.int64)[None, :]).reshape(-1)
+    r = torch.as_tensor(np.asarray(rows, dtype=np.int64)).to(device)
+    idx = (r[:, None] * row_size + torch.arange(row_size, dtype=torch.int64, device=device)[None, :]).reshape(-1)
     x = hash_normal(stream, idx, scale).to(dtype).to(torch.float64)
-    return x.view(len(rows), row_size).numpy()
+    return x.view(len(rows), row_size).cpu().numpy()
 
 
 STREAM_K, STREAM_V, STREAM_Q, STREAM_DO, STREAM_DECODE_Q = 1, 2, 3, 4, 5

@@ -149,3 +149,125 @@ def packed(t, seg_order, arr):
 def pool_pages_needed(ep):
     P = ep.page_size
     return sum((L + P - 1) // P for L in ep.length) + 4
+
+
+def oracle_checked_dag(oracle_mod, seed, page_size=16, max_segments=12, max_len=80, n_roots=1, steps=160):
+    """Random episodes whose mounts are drawn from every segment and span, kept only when
+    the oracle's own pool accepts them: besides sibling spans this gives spans of an
+    ancestor's tokens past the fork point, second and third disjoint spans of a producer
+    the lineage already mounted, and spans of segments the reader's parent mounted.  Forks,
+    rewinds and appends as in synth.random_dag."""
+    rng = np.random.default_rng(np.random.PCG64(seed))
+    ep = synth.Episode(page_size)
+    orc = oracle_mod.Oracle(page_size, 1 << 16, 1, 8)
+    fork_of = {}
+    for _ in range(n_roots):
+        r = ep.root()
+        orc.root()
+        n = int(rng.integers(1, max_len))
+        ep.append(r, n)
+        orc.append(r, n)
+
+    def lineage(c):
+        out = []
+        while c >= 0:
+            out.append(c)
+            c = ep.parent[c]
+        return out
+
+    def try_mount(c, p, a, b):
+        if orc.mount(c, p, a, b, check=False) == oracle_mod.OK:
+            ep.mount(c, p, a, b, checked=False)
+            return True
+        return False
+
+    for _ in range(steps):
+        if ep.n_segments >= max_segments * n_roots:
+            break
+        live = [c for c in range(ep.n_segments) if ep.appendable[c]]
+        if not live:
+            break
+        c = live[int(rng.integers(0, len(live)))]
+        u = rng.random()
+        if u < 0.3:
+            n = int(rng.integers(1, max_len))
+            ep.append(c, n)
+            orc.append(c, n)
+        elif u < 0.45:
+            k = int(rng.integers(1, 4))
+            kids = ep.fork(c, k)
+            orc.fork(c, k)
+            for kid in kids:
+                fork_of[kid] = ep.length[c]
+                n = int(rng.integers(0, max_len))
+                ep.append(kid, n)
+                orc.append(kid, n)
+        elif u < 0.85:
+            lin = lineage(c)
+            kind = rng.random()
+            if kind < 0.35 and len(lin) > 1:
+                # an ancestor's own tokens past the point its lineage child forked at
+                j = int(rng.integers(1, len(lin)))
+                x, f = lin[j], fork_of.get(lin[j - 1], 0)
+                if ep.length[x] > f:
+                    a = int(rng.integers(f, ep.length[x]))
+                    b = int(rng.integers(a + 1, ep.length[x] + 1))
+                    try_mount(c, x, a, b)
+            else:
+                # any other segment: a producer mounted before on the lineage half the time
+                prev = [p for (rr, p) in ep.mounted if rr in lin]
+                if prev and kind < 0.65:
+                    p = prev[int(rng.integers(0, len(prev)))]
+                else:
+                    p = int(rng.integers(0, ep.n_segments))
+                if ep.length[p] > 0:
+                    a = int(rng.integers(0, ep.length[p]))
+                    b = int(rng.integers(a + 1, min(ep.length[p], a + max_len) + 1))
+                    try_mount(c, p, a, b)
+            n = int(rng.integers(0, max_len // 2 + 1))
+            ep.append(c, n)
+            orc.append(c, n)
+        elif u < 0.95:
+            if ep.length[c] > 0:
+                k = int(rng.integers(0, ep.length[c] + 1))
+                nid = ep.rewind(c, k)
+                orc.rewind(c, k)
+                fork_of[nid] = k
+                n = int(rng.integers(0, max_len))
+                ep.append(nid, n)
+                orc.append(nid, n)
+        else:
+            ep.done(c)
+            orc.done(c)
+    return ep
+
+
+def mount_kinds(ep):
+    """Counts of the mount kinds in an op log: (ancestor spans, repeated producers)."""
+    parent, anc, rep = {}, 0, 0
+    seen = set()
+    nseg = 0
+    for op in ep.ops:
+        if op[0] == "root":
+            parent[nseg] = -1
+            nseg += 1
+        elif op[0] == "fork":
+            for _ in range(op[2]):
+                parent[nseg] = op[1]
+                nseg += 1
+        elif op[0] == "rewind":
+            parent[nseg] = op[1]
+            nseg += 1
+        elif op[0] == "mount":
+            r, p = op[1], op[2]
+            lin = []
+            x = r
+            while x >= 0:
+                lin.append(x)
+                x = parent[x]
+            if p in lin:
+                anc += 1
+            if any((y, p) in seen for y in lin):
+                rep += 1
+            seen.add((r, p))
+    return anc, rep

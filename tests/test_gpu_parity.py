@@ -278,3 +278,151 @@ def test_decode_group_sizes(lib, oracle_mod, Hq, Hkv):
     want, wl = r.orc.decode(curs, q.astype(np.float64), r.scale)
     assert_close(out.float().cpu().numpy(), want, "bf16", "decode out")
     assert_close(lse.cpu().numpy(), wl, "bf16", "decode lse")
+
+
+# ------------------------------------------------------------------ mounts the episode generators never make
+def _checked_dag(oracle_mod, seed, **kw):
+    from helpers import mount_kinds, oracle_checked_dag
+    ep = oracle_checked_dag(oracle_mod, seed, **kw)
+    return ep, mount_kinds(ep)
+
+
+@pytest.mark.parametrize("seed", range(600, 612))
+def test_plan_checked_mounts(lib, oracle_mod, seed):
+    """Plans bit-exact with the oracle on episodes with every kind of legal mount."""
+    P = [4, 8, 16, 64][seed % 4]
+    ep, _ = _checked_dag(oracle_mod, seed, page_size=P, max_segments=12, max_len=[40, 80, 150][seed % 3])
+    r = Run(lib, oracle_mod, ep, 2, 1, 64, "f32", seed)
+    compare_pools(r.pool, r.orc)
+    plan, opl = r.pack([16, 32, 128, 1][seed % 4])
+    compare_plans(plan.copy_out(), opl)
+    assert plan.info["pairs"] == opl.total_pairs()
+
+
+@pytest.mark.parametrize("seed", [602, 603, 605, 606, 607, 609])
+def test_values_checked_mounts(lib, oracle_mod, seed):
+    """fp32 (CUDA-core kernels) and bf16 (tensor-core kernels, 16 q / 4 kv heads, d 128,
+    page 64) forward and backward against the oracle on those episodes."""
+    ep, _ = _checked_dag(oracle_mod, seed, page_size=16, max_segments=12, max_len=80)
+    r = Run(lib, oracle_mod, ep, 4, 2, 64, "f32", seed)
+    r.pack(32)
+    _check_fwd_bwd(r)
+    ep, _ = _checked_dag(oracle_mod, seed, page_size=64, max_segments=12, max_len=300)
+    r = Run(lib, oracle_mod, ep, 16, 4, 128, "bf16", seed)
+    r.pack(128)
+    assert r.plan.kernel_path(16, 0) == 1 and r.plan.kernel_path(16, 1) == 1
+    _check_fwd_bwd(r)
+
+
+def test_decode_checked_mounts(lib, oracle_mod):
+    ep, _ = _checked_dag(oracle_mod, 607, page_size=64, max_segments=12, max_len=300)
+    r = Run(lib, oracle_mod, ep, 16, 4, 128, "bf16", 2)
+    curs = [s for s in range(r.orc.n_segments) if r.orc.seg_info(s)["len"] > 0]
+    q = synth.make_decode_q(len(curs), 16, 128, "bf16", 0.5, 3)
+    dp = r.pool.decode_plan(curs)
+    out = torch.empty((len(curs), 16, 128), dtype=r.tdt, device="cuda")
+    lse = torch.empty((len(curs), 16), dtype=torch.float32, device="cuda")
+    ws_n = dp.decode_workspace_size(16)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device="cuda")
+    dp.decode(16, r.dev(q), out, lse, r.scale, ws, ws_n)
+    dp.sync()
+    want, wl = r.orc.decode(curs, q.astype(np.float64), r.scale)
+    assert_close(out.float().cpu().numpy(), want, "bf16", "decode out")
+    assert_close(lse.cpu().numpy(), wl, "bf16", "decode lse")
+
+
+# ------------------------------------------------------------------ heavily shared prefix pages
+def _shared_prefix_episode(seed, prefix=1024, branches=7):
+    """A prefix forked into 7 branches of 1.5-2K tokens that mount spans of each other:
+    the prefix pages are read by every query tile of every branch (over 100 reader tiles
+    each), the mounted pages by their owner's tiles and the readers'."""
+    rng = np.random.default_rng(seed)
+    ep = synth.Episode(64)
+    r = ep.root()
+    ep.append(r, prefix)
+    kids = ep.fork(r, branches)
+    want = {k: int(rng.integers(1536, 2049)) for k in kids}
+    for rnd in range(8):
+        for k in kids:
+            ep.append(k, want[k] // 8)
+        if rnd in (3, 5):
+            for k in kids[:4]:
+                p = kids[(kids.index(k) + 1 + rnd) % branches]
+                if ep.can_mount(k, p) and ep.length[p] >= 256:
+                    a = int(rng.integers(0, ep.length[p] - 192))
+                    ep.mount(k, p, a, a + int(rng.integers(64, min(640, ep.length[p] - a) + 1)))
+    return ep
+
+
+def test_shared_prefix_every_dk_dv(lib, oracle_mod):
+    """Tensor-core path, 2 query heads over 1 kv head, d 128, page 64, q-tile 128: every
+    element of O, LSE, dQ, dK and dV against the oracle, where each prefix page's dK/dV is
+    an ordered sum over more than 100 reader tiles."""
+    ep = _shared_prefix_episode(5)
+    r = Run(lib, oracle_mod, ep, 2, 1, 128, "bf16", 6)
+    plan, _ = r.pack(128)
+    assert plan.kernel_path(2, 0) == 1 and plan.kernel_path(2, 1) == 1
+    gp = plan.copy_out()
+    readers = np.diff(gp["page_off"])
+    prefix_pages = r.orc.seg_pages(0)
+    assert readers[prefix_pages].min() >= 100, readers[prefix_pages]
+    assert any(e[7] >= 0 for e in product_entries(gp["entries"]))   # mounted spans are read
+    _check_fwd_bwd(r)
+
+
+def test_decode_cursors_one_call(lib, oracle_mod):
+    """octo_decode_cursors (plan, decode and release in one call; with and without a caller
+    workspace) equals the plan-based decode bit for bit and the oracle within tolerance."""
+    ep = synth.random_dag(93, page_size=64, max_segments=14, max_len=300)
+    r = Run(lib, oracle_mod, ep, 16, 4, 128, "bf16", 3)
+    curs = [s for s in range(r.orc.n_segments) if r.orc.seg_info(s)["len"] > 0]
+    q = r.dev(synth.make_decode_q(len(curs), 16, 128, "bf16", 0.5, 12))
+    dp = r.pool.decode_plan(curs)
+    ref = torch.empty_like(q)
+    ref_lse = torch.empty((len(curs), 16), dtype=torch.float32, device="cuda")
+    ws_n = dp.decode_workspace_size(16)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device="cuda")
+    dp.decode(16, q, ref, ref_lse, r.scale, ws, ws_n)
+    for w in (ws, None):
+        out = torch.full_like(q, float("nan"))
+        lse = torch.full((len(curs), 16), float("nan"), dtype=torch.float32, device="cuda")
+        r.pool.decode_cursors(curs, 16, q, out, lse, r.scale, w, ws_n if w is not None else 0)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
+    want, wl = r.orc.decode(curs, q.float().cpu().numpy().astype(np.float64), r.scale)
+    assert_close(out.float().cpu().numpy(), want, "bf16", "decode out")
+    assert_close(lse.cpu().numpy(), wl, "bf16", "decode lse")
+
+
+@pytest.mark.parametrize("rope", [0.0, 10000.0])
+def test_append_step_writes_like_single_appends(lib, oracle_mod, rope):
+    """octo_append_step with K/V rows (bf16, plain and rotated) writes the pool arrays bit
+    for bit as one-token octo_append / octo_append_rope calls on a twin pool do."""
+    ep = synth.random_dag(33, page_size=16, max_segments=10, max_len=60)
+    Hkv, d, P = 2, 64, 16
+    npages = pool_pages_needed(ep) + 40
+    pools = []
+    for _ in range(2):
+        kp = torch.zeros((npages, Hkv, P, d), dtype=torch.bfloat16, device="cuda")
+        vp = torch.zeros_like(kp)
+        pool = lib.Pool(npages, P, Hkv, d, lib.DTYPE_BF16, kp, vp)
+        from helpers import replay_host
+        replay_host(pool, ep)
+        pools.append((pool, kp, vp))
+    curs = [s for s in range(ep.n_segments) if ep.appendable[s]]
+    rng = np.random.default_rng(4)
+    for step in range(20):
+        k = torch.from_numpy(rng.normal(0, 1, (len(curs), Hkv, d)).astype(np.float32)).cuda().bfloat16()
+        v = torch.from_numpy(rng.normal(0, 1, (len(curs), Hkv, d)).astype(np.float32)).cuda().bfloat16()
+        a = pools[0][0].append_step(curs, k, v, rope_base=rope)
+        b = []
+        for i, c in enumerate(curs):
+            if rope:
+                b.append(int(pools[1][0].append_rope(c, 1, k[i:i + 1], v[i:i + 1], rope)[0]))
+            else:
+                b.append(int(pools[1][0].append(c, 1, k[i:i + 1], v[i:i + 1])[0]))
+        assert a.tolist() == b
+    torch.cuda.synchronize()
+    assert torch.equal(pools[0][1], pools[1][1]) and torch.equal(pools[0][2], pools[1][2])
+    for s in range(ep.n_segments):
+        assert np.array_equal(pools[0][0].seg_pages(s), pools[1][0].seg_pages(s))

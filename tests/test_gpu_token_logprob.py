@@ -191,14 +191,20 @@ def test_episode_chunk_full_vocabulary(lib):
     logp, lse, loss, g = _run(lib, plan, xt, V, ids, w, row0=row0, n=n)
     sample = sorted(set(rng.integers(0, n, 40).tolist()) | {fork_row - row0, 0, n - 1})
     xs = xt[sample].float().cpu().numpy().astype(np.float64)
-    for k, rl in enumerate(sample):
-        r = row0 + rl
-        kids = np.nonzero(pred == r)[0]
-        row_lse = np.log(np.exp(xs[k] - xs[k].max()).sum()) + xs[k].max()
-        assert_close([lse[rl]], [row_lse], "bf16", "lse row %d" % r)
-        want = np.exp(xs[k] - row_lse) * w[kids].sum()
-        for t in kids:
-            assert_close([logp[t]], [xs[k][ids[t]] - row_lse], "bf16", "logp %d" % t)
-            want[ids[t]] -= w[t]
-        assert_close(g[rl], want, "bf16", "dlogits row %d" % r)
+    # the oracle on a sub-problem: the sampled rows as logits rows, followed by the tokens
+    # they predict (as rows of their own whose logits feed nothing here)
+    rows = [row0 + rl for rl in sample]
+    kids = [np.nonzero(pred == r)[0] for r in rows]
+    toks = np.concatenate(kids)
+    k = len(rows)
+    x_sub = np.zeros((k + len(toks), V))
+    x_sub[:k] = xs
+    pred_sub = np.full(k + len(toks), -1)
+    pred_sub[k:] = np.repeat(np.arange(k), [len(c) for c in kids])
+    ids_sub = np.concatenate([np.zeros(k, dtype=np.int64), ids[toks]])
+    w_sub = np.concatenate([np.zeros(k), w[toks].astype(np.float64)])
+    rlogp, rlse, _, rdx = token_logprob(x_sub, ids_sub, w_sub, pred_sub)
+    assert_close(lse[sample], rlse[:k], "bf16", "row lse")
+    assert_close(logp[toks], rlogp[k:], "bf16", "logp")
+    assert_close(g[sample], rdx[:k], "bf16", "dlogits")
     assert np.bincount(pred[pred >= 0]).max() >= 7

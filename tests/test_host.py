@@ -164,3 +164,107 @@ def test_exp2_polynomial_error_bound():
     ref = np.exp2(x.astype(np.float64))
     ok = x > -120          # near the clamp the result is a denormal-range zero for a probability
     assert np.max(np.abs(r[ok] / ref[ok] - 1)) < 1e-4
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_pool_query_matches_oracle(lib, oracle_mod, seed):
+    """octo_pool_query: every segment's refcount and page count and every page's owner
+    against the oracle's allocator model, on episodes with releases and pins."""
+    from helpers import oracle_checked_dag
+    ep = oracle_checked_dag(oracle_mod, 700 + seed, page_size=8, max_segments=12, max_len=50)
+    # release a few cursors at the end (their segments free once nothing reaches them)
+    for c in range(ep.n_segments):
+        if seed % 2 and c % 3 == 1:
+            ep.ops.append(("release", c))
+    npages = sum((L + 7) // 8 for L in ep.length) + 5
+    pool = lib.Pool(npages, 8, 1, 64, lib.DTYPE_F32)
+    orc = oracle_mod.Oracle(8, npages, 1, 64)
+    for op in ep.ops:
+        st_l = _apply(pool, op)
+        st_o = _apply_oracle(orc, op)
+        assert st_l == st_o, op
+    q = pool.query()
+    assert q["n_segments"] == orc.n_segments and q["free_pages"] == orc.free_pages()
+    assert q["n_mounts"] == orc.n_mounts and q["num_pages"] == npages
+    owner = np.full(npages, -1)
+    for s in range(orc.n_segments):
+        info = orc.seg_info(s)
+        assert q["refcount"][s] == info["refcount"], s
+        assert q["n_pages"][s] == info["n_pages"], s
+        if not info["flags"] & 16:
+            owner[orc.seg_pages(s)] = s
+    assert np.array_equal(q["page_owner"], owner)
+    assert int((owner < 0).sum()) == q["free_pages"]
+
+
+def _apply(pool, op):
+    k = op[0]
+    if k == "root":
+        pool.root()
+        return 0
+    if k == "append":
+        return pool.append(op[1], op[2], check=False)
+    if k == "fork":
+        return pool.fork(op[1], op[2], check=False)
+    if k == "mount":
+        return pool.mount(*op[1:], check=False)
+    if k == "rewind":
+        return pool.rewind(op[1], op[2], check=False)
+    if k == "done":
+        return pool.done(op[1], check=False)
+    if k == "release":
+        return pool.release(op[1], check=False)
+    raise ValueError(k)
+
+
+def _apply_oracle(orc, op):
+    k = op[0]
+    if k == "root":
+        orc.root()
+        return 0
+    if k == "append":
+        return orc.append(op[1], op[2], check=False)
+    if k == "fork":
+        return orc.fork(op[1], op[2], check=False)
+    if k == "mount":
+        return orc.mount(*op[1:], check=False)
+    if k == "rewind":
+        return orc.rewind(op[1], op[2], check=False)
+    if k == "done":
+        return orc.done(op[1], check=False)
+    if k == "release":
+        return orc.release(op[1], check=False)
+    raise ValueError(k)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_append_step_matches_oracle(lib, oracle_mod, seed):
+    """octo_append_step (one token for each of several cursors) leaves the pool as the
+    oracle's one-token appends do, step after step, cursors opening pages included; refused
+    calls (a cursor twice, a frozen cursor, too few pages) change nothing."""
+    ep = synth.random_dag(900 + seed, page_size=4, max_segments=10, max_len=30)
+    npages = sum((L + 3) // 4 for L in ep.length) + 40
+    pool = lib.Pool(npages, 4, 1, 64, lib.DTYPE_F32)
+    orc = oracle_mod.Oracle(4, npages, 1, 64)
+    replay_host(pool, ep)
+    orc.replay(ep)
+    curs = [s for s in range(ep.n_segments) if ep.appendable[s]]
+    assert curs
+    for step in range(9):
+        pos = pool.append_step(curs)
+        want = [int(orc.append(c, 1)[0]) for c in curs]
+        assert pos.tolist() == want
+        compare_pools(pool, orc)
+    before = pool.query()
+    assert pool.append_step(curs + curs[:1], check=False) == lib.EINVAL
+    if len(ep.roots) and not ep.appendable[ep.roots[0]]:
+        assert pool.append_step([ep.roots[0]] + curs, check=False) == lib.ESTATE
+    big = lib.Pool(3, 4, 1, 64, lib.DTYPE_F32)
+    r = big.root()
+    kids = big.fork(r, 4)
+    assert big.append_step(kids, check=False) == lib.ENOMEM      # 4 pages needed, 3 free
+    assert big.info()["free_pages"] == 3 and all(big.seg_info(k)["len"] == 0 for k in kids)
+    after = pool.query()
+    for key in ("n_segments", "free_pages", "n_mounts"):
+        assert before[key] == after[key]
+    assert np.array_equal(before["page_owner"], after["page_owner"])
