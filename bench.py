@@ -1,15 +1,17 @@
 """Benchmark: packed DAG attention forward + backward (useful TFLOP/s) and paged decode
 (HBM GB/s) on one GB300, through the C ABI.
 
-One step = one pass of the training hot path over the full episode (16K prefix, 7
-branches x 32K owned tokens, 3 rewinds, 6 mounts; 16 q / 4 kv heads, d 128, page 64,
-bf16): the GPU plan compile (positions + tile list + CSC), the forward, and the backward.
-The decode leg times the decode plan and the paged decode of 256 cursors (32 episodes x 8,
-mean context ~26K tokens) the same way.
+One step = one pass of the training hot path over the training-step workload (8 random
+trees of 140K owned tokens each, 1.12M packed rows; fork fan-out 2-6, depth <= 3, 0-4
+mounted spans per reader; 16 q / 4 kv heads, d 128, page 64, bf16): the GPU plan compile
+(positions + tile list + CSC), the forward, and the backward.  The same step over the
+episode workload (16K prefix, 7 branches x 32K owned tokens, 3 rewinds, 6 mounts) is a
+second object on the line.  The decode leg times the decode plan and the paged decode of
+256 cursors (32 episodes x 8, mean context ~26K tokens) the same way.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
-Under torchrun each rank runs its own episode (a different seed): weak scaling, no
+Under torchrun each rank runs its own workload (a different seed): weak scaling, no
 collective on the data path; rank 0 prints the JSON line with the max time over ranks.
 --impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
 """
@@ -127,25 +129,48 @@ def unique_tokens(entries, num_pages, P):
 L2_BYTES = 129 * 2**20   # GB300 L2
 
 
-def profiled_traffic(workload, call, profile="dram_traffic_episode.md", profiled_workload="episode"):
-    """DRAM bytes per call of `call` from a committed ncu summary of the full-size workload,
-    or None when the workload differs or a kernel source's code changed since the counters."""
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", profile)
-    if workload != profiled_workload or not os.path.exists(path):
-        return None
-    want, got = {}, None
-    for line in open(path):
-        line = line.strip()
-        if " sha256/16: " in line:
-            name, h = line.split(" sha256/16: ")
-            want[name] = h
-        elif line.startswith(call + " bytes per call: "):
-            got = int(line.split(": ")[1])
-    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "packed_tree_attention_gb300", "csrc")
-    for name, h in want.items():
-        if code_fingerprint(os.path.join(src, name)) != h:
-            return None
-    return got if want else None
+# ncu traffic may be taken on a smaller case of the same kernels: one tree of the training
+# step, 32 of the 256 decode cursors; bench scales it to the workload by its units of work
+TRAFFIC_CASES = {"train_step": ("train_tree", "train_step"), "episode": ("episode",),
+                 "decode": ("decode_small", "decode"), "decode_small": ("decode_small",)}
+
+
+def profiled_traffic(workload, call, units):
+    """(DRAM bytes per call, note) of `call` on `workload` from the committed ncu summaries
+    under profiles/.  A line 'traffic: <call> <case> <bytes> bytes per call, <units> units'
+    gives the bytes measured on <case> with <units> units of work (visible pairs for the
+    attention calls, algorithmic bytes for the decode); a case in TRAFFIC_CASES[workload]
+    is scaled to `units`.  (None, reason) when no summary has it or when a kernel source
+    named by a fingerprint line of that summary has changed since the counters."""
+    here = os.path.dirname(os.path.abspath(__file__))
+    src = os.path.join(here, "packed_tree_attention_gb300", "csrc")
+    cases = TRAFFIC_CASES.get(workload, (workload,))
+    best = None
+    for fname in sorted(os.listdir(os.path.join(here, "profiles"))):
+        if not fname.endswith(".md"):
+            continue
+        want, found = {}, []
+        for line in open(os.path.join(here, "profiles", fname)):
+            line = line.strip()
+            if " sha256/16: " in line:
+                name, h = line.split(" sha256/16: ")
+                want[name] = h
+            elif line.startswith("traffic: "):
+                f = line[len("traffic: "):].replace(",", "").split()
+                if len(f) >= 7 and f[0] == call and f[1] in cases:
+                    found.append((cases.index(f[1]), f[1], int(f[2]), int(f[6])))
+        if not found:
+            continue
+        if any(code_fingerprint(os.path.join(src, n)) != h for n, h in want.items()):
+            best = best or (None, "%s: kernel sources changed since the counters" % fname)
+            continue
+        rank, case, b, u = min(found)
+        if best is None or best[0] is None:
+            scaled = int(round(b * units / u))
+            note = ("profiles/%s, measured on %s" % (fname, case) +
+                    ("" if case == workload else ", scaled by units of work %d/%d" % (units, u)))
+            best = (scaled, note)
+    return best if best else (None, "no ncu summary for this workload")
 
 
 def code_fingerprint(path):
@@ -163,7 +188,8 @@ def code_fingerprint(path):
 WORKLOAD_DESC = {
     "episode": "episode: 16K prefix, 7 branches x 32K owned tokens, 3 rewinds, 6 mounts",
     "tree_fwd": "tree: 4K prefix, 4 x 8K branches, 2 mounts",
-    "train_step": "train step: 8 trees of ~140K owned tokens, fan-out 2-6, depth <= 3, mounts",
+    "train_step": "train step: 8 trees of 140K owned tokens (1.12M), fan-out 2-6, depth <= 3, 0-4 mounts per reader",
+    "train_tree": "one tree of the train step: 140K owned tokens, fan-out 2-6, depth <= 3, 0-4 mounts per reader",
     "tiny": "tiny: 64-token prefix, 2 x 32 branches, 1 mount",
     "decode": "paged decode: 32 episodes x 8 cursors, shared prefix 2-8K, paths 8-32K, 0-3 sibling mounts of 0.5-8K",
     "decode_small": "paged decode: 4 episodes x 8 cursors, shared prefix 2-8K, paths 8-32K, 0-3 sibling mounts",
@@ -214,48 +240,80 @@ def build_episode(pta, torch, name, seed, dev):
 # --------------------------------------------------------------------------------------
 # CPU baseline: the oracle on a bounded sample of the same workload
 # --------------------------------------------------------------------------------------
-def oracle_sample(name, seed, budget_s=15.0, n_rows_max=256):
-    """Times the fp64 oracle's forward + backward on a seeded sample of packed rows of the
-    workload (all 16 heads of each row; the backward's dK/dV from those rows only).
-    Returns (TFLOP/s, threads, description)."""
-    import torch
-    import oracle
-    cfg = synth.CONFIGS[name]
-    Hq, Hkv, d, P = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["P"]
-    ep = synth.make_preset(name, seed=seed)
-    T = ep.n_tokens
-    npages = sum((L + P - 1) // P for L in ep.length) + 8 + 4 * len(ep.cursors)   # room for decode steps
-    orc = oracle.Oracle(P, npages, Hkv, d)
-    K = synth.hash_rows(synth.STREAM_K + 16 * seed, np.arange(T), Hkv * d, torch.bfloat16, 0.5).reshape(T, Hkv, d)
-    V = synth.hash_rows(synth.STREAM_V + 16 * seed, np.arange(T), Hkv * d, torch.bfloat16, 0.5).reshape(T, Hkv, d)
-    orc.replay(ep, K, V)
-    del K, V
-    opl = orc.pack(ep.roots, 128, tile_stride=1 << 30)
-    N = opl.n_rows
-    rng = np.random.default_rng(seed)
-    threads = os.cpu_count() or 1
-    scale = 1.0 / math.sqrt(d)
-    done_rows, flops, elapsed = 0, 0.0, 0.0
-    batch = 8
-    while elapsed < budget_s and done_rows < n_rows_max:
-        rows = np.sort(rng.choice(N, size=batch, replace=False)).astype(np.int32)
-        Q = np.zeros((N, Hq, d))
-        dO = np.zeros((N, Hq, d))
-        Q[rows] = synth.hash_rows(synth.STREAM_Q + 16 * seed, rows, Hq * d, torch.bfloat16, 0.5).reshape(-1, Hq, d)
-        dO[rows] = synth.hash_rows(synth.STREAM_DO + 16 * seed, rows, Hq * d, torch.bfloat16, 1.0).reshape(-1, Hq, d)
-        need = np.zeros(N, dtype=np.uint8)
+class OracleSampler:
+    """The fp64 oracle's forward + backward on seeded samples of packed rows of a workload
+    (all 16 heads of each row; the backward's dK/dV from those rows only).  The oracle
+    replays the op log without values and gets K/V rows only for the tokens in the sampled
+    rows' contexts, generated on `kv_device` before the timed calls.  The training step's
+    trees are independent units of the same statistics, so its rows are sampled from its
+    first tree, replayed alone."""
+
+    def __init__(self, name, seed, kv_device="cpu"):
+        import oracle
+        self.name, self.seed, self.kv_device = name, seed, kv_device
+        cfg = synth.CONFIGS[name]
+        self.Hq, self.Hkv, self.d, P = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["P"]
+        self.unit = "train_tree" if name == "train_step" else name
+        ep = synth.make_preset(self.unit, seed=seed)
+        self.T = ep.n_tokens
+        npages = sum((L + P - 1) // P for L in ep.length) + 8 + 4 * len(ep.cursors)
+        self.orc = oracle.Oracle(P, npages, self.Hkv, self.d)
+        self.orc.replay(ep)
+        self.opl = self.orc.pack(ep.roots, 128, tile_stride=1 << 30)
+        self.N = self.opl.n_rows
+        self.rng = np.random.default_rng(seed)
+        self.threads = os.cpu_count() or 1
+        self.kv_set = np.zeros(self.T, dtype=bool)
+        self.rows_done = 0
+
+    def batch(self, n_rows):
+        """One timed batch of n_rows sampled rows: returns (useful FLOPs, seconds)."""
+        import torch
+        Hq, Hkv, d, seed = self.Hq, self.Hkv, self.d, self.seed
+        rows = np.sort(self.rng.choice(self.N, size=n_rows, replace=False)).astype(np.int32)
+        ctx = [self.opl.row_context(int(r))[0] for r in rows]
+        toks = np.unique(np.concatenate(ctx))
+        toks = toks[~self.kv_set[toks]]
+        if len(toks):
+            K = synth.hash_rows(synth.STREAM_K + 16 * seed, toks, Hkv * d, torch.bfloat16, 0.5, self.kv_device)
+            V = synth.hash_rows(synth.STREAM_V + 16 * seed, toks, Hkv * d, torch.bfloat16, 0.5, self.kv_device)
+            self.orc.set_kv(toks, K.reshape(-1, Hkv, d), V.reshape(-1, Hkv, d))
+            self.kv_set[toks] = True
+        Q = np.zeros((self.N, Hq, d))
+        dO = np.zeros((self.N, Hq, d))
+        Q[rows] = synth.hash_rows(synth.STREAM_Q + 16 * seed, rows, Hq * d, torch.bfloat16, 0.5,
+                                  self.kv_device).reshape(-1, Hq, d)
+        dO[rows] = synth.hash_rows(synth.STREAM_DO + 16 * seed, rows, Hq * d, torch.bfloat16, 1.0,
+                                   self.kv_device).reshape(-1, Hq, d)
+        need = np.zeros(self.N, dtype=np.uint8)
         need[rows] = 1
-        pairs = sum(len(opl.row_context(int(r))[0]) for r in rows)
+        pairs = sum(len(c) for c in ctx)
+        scale = 1.0 / math.sqrt(d)
         t0 = time.perf_counter()
-        opl.fwd(Q, scale, rows=rows, nthreads=threads)
-        opl.bwd(Q, dO, scale, need_dq=need, need_dkdv=np.zeros(T, dtype=np.uint8), nthreads=threads,
-                partial=True)
-        elapsed += time.perf_counter() - t0
-        flops += 14.0 * d * Hq * pairs
-        done_rows += batch
-    desc = ("fp64 oracle fwd+bwd of %d sampled rows x %d heads of the %s workload (%.3g of its %d rows); "
-            "useful FLOPs 14*d*Hq*pairs of the sample" % (done_rows, Hq, name, done_rows / N, N))
-    return flops / elapsed / 1e12, threads, desc, elapsed
+        self.opl.fwd(Q, scale, rows=rows, nthreads=self.threads)
+        self.opl.bwd(Q, dO, scale, need_dq=need, need_dkdv=np.zeros(self.T, dtype=np.uint8), nthreads=self.threads,
+                     partial=True)
+        el = time.perf_counter() - t0
+        self.rows_done += n_rows
+        return 14.0 * d * Hq * pairs, el
+
+    def describe(self):
+        where = ("its first tree (%d of its rows; the 8 trees are independent)" % self.N
+                 if self.unit != self.name else "its %d rows" % self.N)
+        return ("fp64 oracle fwd+bwd of %d rows x %d heads sampled from %s of the %s workload; useful FLOPs "
+                "14*d*Hq*pairs of the sample" % (self.rows_done, self.Hq, where, self.name))
+
+
+def oracle_sample(name, seed, budget_s=15.0, n_rows_max=256, kv_device="cpu"):
+    """(TFLOP/s, threads, description, seconds) of the oracle on row batches of 8 until
+    about budget_s seconds of timed oracle work."""
+    smp = OracleSampler(name, seed, kv_device)
+    flops, elapsed = 0.0, 0.0
+    while elapsed < budget_s and smp.rows_done < n_rows_max:
+        f, el = smp.batch(8)
+        flops += f
+        elapsed += el
+    return flops / elapsed / 1e12, smp.threads, smp.describe(), elapsed
 
 
 # --------------------------------------------------------------------------------------
@@ -284,8 +342,9 @@ def timed(torch, stream, fn, steps, warmup, dist=None):
 
 def decode_leg(pta, torch, name, seed, dev, stream, steps, warmup, world, dist, hbm, peak_src):
     """Paged decode of the cursors of decode workload `name`: kernel-only GB/s of the
-    algorithmic bytes (unique visible K/V tokens + queries, outputs, plan), then plan +
-    decode."""
+    algorithmic bytes (unique visible K/V tokens + queries, outputs, plan); then a fresh
+    plan + decode, and serving steps of one new token per cursor with the plan advanced in
+    place + decode."""
     ev = lambda: torch.cuda.Event(enable_timing=True)
     cfg = synth.CONFIGS[name]
     Hq, Hkv, d, P = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["P"]
@@ -298,7 +357,7 @@ def decode_leg(pta, torch, name, seed, dev, stream, steps, warmup, world, dist, 
     ld = torch.empty((n, Hq), dtype=torch.float32, device=dev)
     dplan = dpool.decode_plan(curs)
     wsn = dplan.decode_workspace_size(Hq)
-    wsd = torch.empty(max(1, wsn), dtype=torch.uint8, device=dev)
+    wsd = torch.empty(max(1, 2 * wsn), dtype=torch.uint8, device=dev)   # room for runs added by advances
     ent = dplan.copy_out()["entries"]
     uniq = unique_tokens(ent, dpool.num_pages, P)
     logical = int((ent["kv_hi"].astype(np.int64) - ent["kv_lo"]).sum())
@@ -332,38 +391,40 @@ def decode_leg(pta, torch, name, seed, dev, stream, steps, warmup, world, dist, 
         plan_ms_list.append((a, b, p2))
 
     timed(torch, stream, pstep, 3, 1, dist)
-    full_ms = statistics.mean([a.elapsed_time(b) for a, b, _ in plan_ms_list[1:]])
-    # plan upkeep per decoded token: every cursor one token longer (layout only), then the
-    # plan advanced in place vs compiled afresh (both synchronous: wall time)
+    fresh_ms = statistics.mean([a.elapsed_time(b) for a, b, _ in plan_ms_list[1:]])
+    # serving steps with plan upkeep: every cursor gets one token (octo_append_step, layout
+    # only: the new slots keep their zeroed K/V), the plan is advanced in place and the
+    # cursors decoded;
+    # CUDA-event time per step over the whole run (host work between launches included
+    # where the GPU waits for it), and the advance's wall time on the host
     upkeep = None
-    if all(dpool.append(c, 1, check=False) == pta.OK for c in curs):
-        adv_t, fresh_t = [], []
-        for it in range(4):
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            if dplan.advance(stream, check=False) != pta.OK:
-                break
-            t1 = time.perf_counter()
-            p3 = dpool.decode_plan(curs, stream)
-            t2 = time.perf_counter()
-            adv_t.append(t1 - t0)
-            fresh_t.append(t2 - t1)
-            del p3
-            if it < 3 and not all(dpool.append(c, 1, check=False) == pta.OK for c in curs):
-                break
-        if adv_t:
-            upkeep = {"advance_ms": 1e3 * statistics.median(adv_t),
-                      "fresh_plan_ms": 1e3 * statistics.median(fresh_t)}
+    adv_wall = []
+
+    def ustep():
+        if dpool.append_step(curs, stream=stream, check=False) != pta.OK:
+            raise RuntimeError("decode pool full")
+        t0 = time.perf_counter()
+        dplan.advance(stream)
+        adv_wall.append(time.perf_counter() - t0)
+        wsz = dplan.decode_workspace_size(Hq)
+        assert wsz <= 2 * wsn
+        dplan.decode(Hq, qd, od, ld, scale, wsd, wsz, stream=stream)
+
+    u_steps = 20
+    u_ms, _ = timed(torch, stream, ustep, u_steps, 3, dist)
+    upkeep = {"ms_per_step_advance_and_decode": u_ms / u_steps, "advance_wall_ms": 1e3 * statistics.median(adv_wall),
+              "steps": u_steps, "fresh_plan_and_decode_ms": fresh_ms}
     world_bytes = world * alg_bytes
+    dec_traffic, dec_note = profiled_traffic(name, "octo_decode", alg_bytes)
     dec = {"metric": "paged decode HBM GB/s", "value": world_bytes / (kern_ms * 1e-3) / 1e9, "unit": "GB/s",
            "workload": WORKLOAD_DESC[name] + "; 16q/4kv heads, d=128, page 64, bf16",
-           "ms_per_step": kern_ms, "ms_per_step_with_plan": full_ms, "plan_upkeep": upkeep,
+           "ms_per_step": kern_ms, "plan_upkeep": upkeep,
            "cursors": n, "unique_kv_tokens": uniq, "logical_kv_tokens": logical,
            "algorithmic_bytes": alg_bytes, "logical_bytes": logical * tok_bytes,
            "roofline": {"bound": "hbm", "achieved": alg_bytes / (kern_ms * 1e-3) / 1e9, "peak": hbm,
                         "unit": "GB/s", "frac": alg_bytes / (kern_ms * 1e-3) / 1e9 / hbm,
                         "peak_source": peak_src,
-                        "traffic": profiled_traffic(name, "octo_decode", "ncu_decode.md", "decode"),
+                        "traffic": dec_traffic, "traffic_note": dec_note,
                         "traffic_unit": "bytes per call (ncu dram__bytes_read + write)"},
            "gpu_launches": dlaunch, "clocks": dclocks, "kernel_path": dplan.kernel_path(Hq, 2)}
     del dpool, dkp, dvp
@@ -371,31 +432,12 @@ def decode_leg(pta, torch, name, seed, dev, stream, steps, warmup, world, dist, 
     return dec
 
 
-def run_ours(args, rank, world, dist):
-    import torch
-    import packed_tree_attention_gb300 as pta
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    pta.load()
-    stream = torch.cuda.current_stream()
-    hbm, bf16, bf16s, peak_src = peaks()
-    seed = rank_seed(args.seed, rank)
-
-    if args.decode_only:
-        dec = decode_leg(pta, torch, args.decode_workload, seed, dev, stream, args.decode_steps, args.warmup,
-                         world, dist, hbm, peak_src)
-        if rank == 0:
-            print(json.dumps({"metric": dec["metric"], "value": dec["value"], "unit": dec["unit"], "n_gpus": world,
-                              "steps": args.decode_steps, "warmup": args.warmup, "ms_per_step": dec["ms_per_step"],
-                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-                              "data": "synthetic (counter-based generator, seed %d + rank)" % args.seed,
-                              "config": {"workload": dec["workload"],
-                                         "l2": "K/V read larger than L2 (%d MB unique)" % (dec["algorithmic_bytes"] // 10**6)},
-                              "decode": dec}))
-        return
-
-    # ---------------- training leg: episode fwd + bwd ----------------
-    ep, pool, kp, vp, cfg = build_episode(pta, torch, args.workload, seed, dev)
+def train_leg(pta, torch, name, seed, dev, stream, steps, warmup, world, dist, bf16s, peak_src, with_e2e):
+    """One step = plan compile + forward + backward of training workload `name`; useful
+    TFLOP/s over the step, per-call times, the backward's roofline and (with_e2e) the same
+    step through host buffers.  Returns a dict; its "_state", "_q" and "_dq" entries hand
+    the workload on to the legs that reuse it."""
+    ep, pool, kp, vp, cfg = build_episode(pta, torch, name, seed, dev)
     Hq, Hkv, d, P = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["P"]
     scale = 1.0 / math.sqrt(d)
     plan = pool.pack_tree(ep.roots, 128)
@@ -427,15 +469,14 @@ def run_ours(args, rank, world, dist):
         e3.record(stream)
         return (e0, e1, e2, e3, pl)
 
-    launches0 = pta.launch_count()
     clk = ClockSampler(dev.index)
-    # warm-up, then the timed steps (inputs > L2: 1 GB of Q alone)
-    for _ in range(args.warmup):
+    # warm-up, then the timed steps (inputs > L2: Q alone is hundreds of MB)
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     launches0 = pta.launch_count()
     clk.start()
-    total_ms, recs = timed(torch, stream, step, args.steps, 0, dist)
+    total_ms, recs = timed(torch, stream, step, steps, 0, dist)
     clocks = clk.stop()
     launches = pta.launch_count() - launches0
     for e0, e1, e2, e3, pl in recs:
@@ -445,7 +486,7 @@ def run_ours(args, rank, world, dist):
     path_fwd = recs[0][4].kernel_path(Hq, 0)
     path_bwd = recs[0][4].kernel_path(Hq, 1)
     del recs
-    ms_step = max_over_ranks(total_ms / args.steps, dist)
+    ms_step = max_over_ranks(total_ms / steps, dist)
     value = world * (fwd_flops + bwd_flops) / (ms_step * 1e-3) / 1e12
     fwd_ms = statistics.mean(per["fwd"])
     bwd_ms = statistics.mean(per["bwd"])
@@ -454,9 +495,9 @@ def run_ours(args, rank, world, dist):
     dom_ms = max(bwd_ms, fwd_ms)
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
 
-    # ---------------- e2e leg: host buffers through the public API ----------------
+    # e2e: host buffers through the public API, copies inside the timed region
     e2e = None
-    if not args.no_e2e:
+    if with_e2e:
         hq = q.cpu().pin_memory()
         hdo = do.cpu().pin_memory()
         hk = kp.cpu().pin_memory()
@@ -479,7 +520,7 @@ def run_ours(args, rank, world, dist):
             hdv.copy_(dv, non_blocking=True)
             return pl
 
-        e2e_steps = max(1, min(args.steps, 3))
+        e2e_steps = max(1, min(steps, 3))
         e_ms, _ = timed(torch, stream, e2e_step, e2e_steps, 1, dist)
         e_ms = max_over_ranks(e_ms / e2e_steps, dist)
         h2d = sum(x.numel() * x.element_size() for x in (hq, hdo, hk, hv))
@@ -487,8 +528,146 @@ def run_ours(args, rank, world, dist):
         e2e = {"value": world * (fwd_flops + bwd_flops) / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
         del hq, hdo, hk, hv, hdq, hdk, hdv, q2, do2
+    traffic, traffic_note = profiled_traffic(name, "octo_attn_" + dom, pairs)
+    out = {
+        "value": value, "ms_per_step": ms_step,
+        "config": {"workload": workload_desc(name, cfg),
+                   "packed_tokens": N, "visible_pairs": pairs, "useful_tflop_per_step": (fwd_flops + bwd_flops) / 1e12,
+                   "step": "plan compile + fwd + bwd",
+                   "l2": ("inputs larger than L2 (Q alone %.0f MB)" if q_bytes > L2_BYTES else
+                          "inputs fit in L2 (Q %.0f MB): timings include L2 reuse") % (q_bytes / 1e6),
+                   "parallelism": "replicas: one workload per GPU, no collective"},
+        "breakdown_ms": {k: statistics.mean(v) for k, v in per.items()},
+        "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,
+        "bwd_tflops": bwd_flops / (bwd_ms * 1e-3) / 1e12,
+        "roofline": {"bound": "tensor", "kernel": "octo_attn_" + dom, "achieved": achieved, "peak": bf16s,
+                     "unit": "TFLOP/s", "frac": achieved / bf16s, "peak_source": peak_src + " (sustained bf16)",
+                     "traffic": traffic, "traffic_note": traffic_note,
+                     "traffic_unit": "bytes per call (ncu dram__bytes_read + write)"},
+        "kernel_path": {"fwd": path_fwd, "bwd": path_bwd},
+        "clocks": clocks,
+        "gpu_launches": launches,
+        "e2e": e2e,
+    }
+    del o, lse, do, dk, dv, ws
+    out["_state"] = (ep, pool, kp, vp, cfg)
+    out["_q"], out["_dq"] = q, dq
+    return out
 
-    # ---------------- rotary embedding leg (rows of the episode plan) ----------------
+
+# FP32 fused multiply-add peak of GB300 from its unit counts: 152 SMs x 128 FP32 lanes x
+# 2 FLOP per FMA x the 2070 MHz maximum SM clock
+FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def recurrent_flops(n_chunks, H, D, C=64):
+    """Executed FLOPs of the chunked gated delta rule (every chunk computed at full size):
+    forward 3 C D^2 + 5 C^2 D + C^3 / 6 multiply-adds per (chunk, head), backward
+    9 C D^2 + 15 C^2 D."""
+    fwd = 2.0 * (3 * C * D * D + 5 * C * C * D + C ** 3 / 6) * n_chunks * H
+    bwd = 2.0 * (9 * C * D * D + 15 * C * C * D) * n_chunks * H
+    return fwd, bwd
+
+
+def recurrent_leg(pta, torch, name, seed, dev, stream, steps, warmup, dist, H=16, D=128):
+    """Tree-packed recurrent layer (gated delta rule) over the rows of training workload
+    `name`: forward and backward, fp32, H heads of head_dim D."""
+    ep = synth.make_preset(name, seed=seed)
+    P = synth.CONFIGS[name]["P"]
+    pool = pta.Pool(sum((L + P - 1) // P for L in ep.length) + 8, P, 1, 64, pta.DTYPE_F32)   # layout only
+    for op in ep.ops:
+        kind = op[0]
+        if kind == "root":
+            pool.root()
+        elif kind == "append":
+            pool.append(op[1], op[2])
+        elif kind == "fork":
+            pool.fork(op[1], op[2])
+        elif kind == "mount":
+            pool.mount(*op[1:])
+        elif kind == "rewind":
+            pool.rewind(op[1], op[2])
+        elif kind == "done":
+            pool.done(op[1])
+    plan = pool.pack_tree(ep.roots, 128)
+    N = plan.info["n_rows"]
+    gen = lambda s, shape: synth.hash_fill(s, shape, torch.float32, dev, 1.0)
+    q = gen(synth.STREAM_Q + 200 + 16 * seed, (N, H, D))
+    k = gen(synth.STREAM_K + 200 + 16 * seed, (N, H, D))
+    k /= k.norm(dim=2, keepdim=True)
+    v = gen(synth.STREAM_V + 200 + 16 * seed, (N, H, D))
+    do = gen(synth.STREAM_DO + 200 + 16 * seed, (N, H, D))
+    g = torch.Generator(device=dev).manual_seed(seed)
+    a = 0.6 + 0.4 * torch.rand((N, H), generator=g, device=dev)
+    b = torch.rand((N, H), generator=g, device=dev)
+    o = torch.empty_like(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    da, db = torch.empty_like(a), torch.empty_like(a)
+    ws = torch.empty(plan.recurrent_workspace_size(H, D), dtype=torch.uint8, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    rec = []
+
+    def step():
+        e0, e1, e2 = ev(), ev(), ev()
+        e0.record(stream)
+        plan.recurrent_fwd(H, D, q, k, v, a, b, o, ws, stream=stream)
+        e1.record(stream)
+        plan.recurrent_bwd(H, D, q, k, v, a, b, do, dq, dk, dv, da, db, ws, stream=stream)
+        e2.record(stream)
+        rec.append((e0, e1, e2))
+
+    l0 = pta.launch_count()
+    timed(torch, stream, step, steps, warmup, dist)
+    launches = (pta.launch_count() - l0) // (steps + warmup)
+    fwd_ms = statistics.mean(x.elapsed_time(y) for x, y, _ in rec[warmup:])
+    bwd_ms = statistics.mean(y.elapsed_time(z) for _, y, z in rec[warmup:])
+    fwd_f, bwd_f = recurrent_flops(plan.info["n_rec_chunks"], H, D)
+    out = {"metric": "tree-packed recurrent layer (gated delta rule) fwd + bwd, executed TFLOP/s",
+           "workload": "%s DAG rows (%d packed rows), %d heads, head_dim %d, fp32, chunks of 64" % (name, N, H, D),
+           "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+           "fwd_tflops": fwd_f / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_f / (bwd_ms * 1e-3) / 1e12,
+           "launches_per_step": launches,
+           "roofline": {"bound": "alu", "achieved": (fwd_f + bwd_f) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12,
+                        "peak": FFMA_PEAK_TFLOPS, "unit": "TFLOP/s",
+                        "frac": (fwd_f + bwd_f) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12 / FFMA_PEAK_TFLOPS,
+                        "peak_source": "derived: FP32 FMA lanes x 2 x max SM clock", "traffic": None}}
+    del q, k, v, do, a, b, o, dq, dk, dv, da, db, ws, plan, pool
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    import packed_tree_attention_gb300 as pta
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    pta.load()
+    stream = torch.cuda.current_stream()
+    hbm, bf16, bf16s, peak_src = peaks()
+    seed = rank_seed(args.seed, rank)
+
+    if args.decode_only:
+        dec = decode_leg(pta, torch, args.decode_workload, seed, dev, stream, args.decode_steps, args.warmup,
+                         world, dist, hbm, peak_src)
+        if rank == 0:
+            print(json.dumps({"metric": dec["metric"], "value": dec["value"], "unit": dec["unit"], "n_gpus": world,
+                              "steps": args.decode_steps, "warmup": args.warmup, "ms_per_step": dec["ms_per_step"],
+                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                              "data": "synthetic (counter-based generator, seed %d + rank)" % args.seed,
+                              "config": {"workload": dec["workload"],
+                                         "l2": "K/V read larger than L2 (%d MB unique)" % (dec["algorithmic_bytes"] // 10**6)},
+                              "decode": dec}))
+        return
+
+    # ---------------- training leg: fwd + bwd of the headline workload ----------------
+    tr = train_leg(pta, torch, args.workload, seed, dev, stream, args.steps, args.warmup, world, dist, bf16s,
+                   peak_src, with_e2e=not args.no_e2e)
+    ep, pool, kp, vp, cfg = tr.pop("_state")
+    Hq, Hkv, d, P = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["P"]
+    q, dq, N = tr.pop("_q"), tr.pop("_dq"), tr["config"]["packed_tokens"]
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    # ---------------- rotary embedding leg (rows of the headline workload's plan) ----------------
     rope = None
     if not args.no_rope:
         rplan = pool.pack_tree(ep.roots, 128)
@@ -516,7 +695,7 @@ def run_ours(args, rank, world, dist):
                 "peak": hbm, "peak_source": peak_src}
         del rplan
 
-    # ---------------- per-token log-probability / loss leg (rows of the episode plan) ----
+    # ---------------- per-token log-probability / loss leg (rows of the same plan) ----
     logprob = None
     if not args.no_logprob:
         lplan = pool.pack_tree(ep.roots, 128)
@@ -547,7 +726,8 @@ def run_ours(args, rank, world, dist):
         fb = lx.numel() * 2 + small                      # one read of the logits
         gb = 2 * lx.numel() * 2 + small                  # + one write of the gradient
         logprob = {"metric": "per-token log-prob / loss over packed rows, HBM GB/s",
-                   "workload": "%d episode rows x vocabulary %d, bf16 logits (%.1f GB)" % (R, V, lx.numel() * 2 / 1e9),
+                   "workload": "%d packed rows of the %s workload x vocabulary %d, bf16 logits (%.1f GB)" % (
+                       R, args.workload, V, lx.numel() * 2 / 1e9),
                    "terms": {"value": fb / (f_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": f_ms,
                              "frac": fb / (f_ms * 1e-3) / 1e9 / hbm},
                    "terms_and_gradient": {"value": gb / (g_ms * 1e-3) / 1e9, "unit": "GB/s", "ms": g_ms,
@@ -555,9 +735,21 @@ def run_ours(args, rank, world, dist):
                    "peak": hbm, "peak_source": peak_src}
         del lplan, lx, lg, lids, lw, llogp, lloss, lws
 
-    # free the training leg before the decode leg
-    del pool, kp, vp, q, do, o, lse, dq, dk, dv, ws
+    # free the headline workload, then the second training workload (same step, fewer steps)
+    del pool, kp, vp, q, dq, ep
     torch.cuda.empty_cache()
+    second = None
+    if args.second_workload and args.second_workload != args.workload:
+        second = train_leg(pta, torch, args.second_workload, seed, dev, stream, max(3, min(args.steps, 10)),
+                           args.warmup, world, dist, bf16s, peak_src, with_e2e=False)
+        for k in ("_state", "_q", "_dq"):
+            second.pop(k)
+        torch.cuda.empty_cache()
+
+    # ---------------- tree-packed recurrent layer (episode DAG rows) ----------------
+    rec = None
+    if not args.no_recurrent:
+        rec = recurrent_leg(pta, torch, "episode", seed, dev, stream, 3, 2, dist)
 
     # ---------------- decode leg ----------------
     dec = None
@@ -593,39 +785,33 @@ def run_ours(args, rank, world, dist):
     # ---------------- CPU baseline (rank 0, N = 1) ----------------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        v, thr, desc, el = oracle_sample(args.workload, seed, budget_s=args.cpu_budget)
+        v, thr, desc, el = oracle_sample(args.workload, seed, budget_s=args.cpu_budget, kv_device="cuda")
         cpu = {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": desc, "seconds": el}
 
     out = {
         "metric": METRIC,
-        "value": value,
+        "value": tr["value"],
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": ms_step,
+        "ms_per_step": tr["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (counter-based generator, seed %d + rank)" % args.seed,
-        "config": {"workload": workload_desc(args.workload, cfg),
-                   "packed_tokens": N, "visible_pairs": pairs, "useful_tflop_per_step": (fwd_flops + bwd_flops) / 1e12,
-                   "step": "plan compile + fwd + bwd",
-                   "l2": ("inputs larger than L2 (Q alone %.0f MB)" if q_bytes > L2_BYTES else
-                          "inputs fit in L2 (Q %.0f MB): timings include L2 reuse") % (q_bytes / 1e6),
-                   "parallelism": "replicas: one episode per GPU, no collective"},
-        "breakdown_ms": {k: statistics.mean(v) for k, v in per.items()},
-        "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,
-        "bwd_tflops": bwd_flops / (bwd_ms * 1e-3) / 1e12,
-        "roofline": {"bound": "tensor", "kernel": "octo_attn_" + dom, "achieved": achieved, "peak": bf16s,
-                     "unit": "TFLOP/s", "frac": achieved / bf16s, "peak_source": peak_src + " (sustained bf16)",
-                     "traffic": profiled_traffic(args.workload, "octo_attn_" + dom),
-                     "traffic_unit": "bytes per call (ncu dram__bytes_read + write)"},
-        "kernel_path": {"fwd": path_fwd, "bwd": path_bwd},
-        "clocks": clocks,
-        "gpu_launches": launches,
-        "e2e": e2e,
+        "config": tr["config"],
+        "breakdown_ms": tr["breakdown_ms"],
+        "fwd_tflops": tr["fwd_tflops"],
+        "bwd_tflops": tr["bwd_tflops"],
+        "roofline": tr["roofline"],
+        "kernel_path": tr["kernel_path"],
+        "clocks": tr["clocks"],
+        "gpu_launches": tr["gpu_launches"],
+        "e2e": tr["e2e"],
+        "second_workload": second,
+        "recurrent": rec,
         "decode": dec,
         "rope": rope,
         "token_logprob": logprob,
@@ -637,23 +823,27 @@ def run_ours(args, rank, world, dist):
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores; each step one
+    batch of sampled rows of the same workload (the oracle state built once, untimed)."""
     if rank != 0:
         return
+    smp = OracleSampler(args.workload, args.seed)
     per = []
-    thr = None
-    desc = None
     for i in range(args.warmup + args.steps):
-        v, thr, desc, el = oracle_sample(args.workload, args.seed, budget_s=args.ref_budget, n_rows_max=64)
+        f, el = smp.batch(args.ref_rows)
         if i >= args.warmup:
-            per.append((v, el))
-    value = statistics.mean(v for v, _ in per)
+            per.append((f, el))
+    flops = sum(f for f, _ in per)
+    secs = sum(e for _, e in per)
+    value = flops / secs / 1e12
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(e for _, e in per),
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / len(per),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (counter-based generator, seed %d)" % args.seed,
            "config": {"workload": workload_desc(args.workload, synth.CONFIGS[args.workload]) +
-                                  "; each step a bounded row sample"},
-           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": desc},
+                                  "; each step a batch of %d sampled rows" % args.ref_rows},
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": smp.threads, "kind": "oracle",
+                            "sample": smp.describe()},
            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
 
@@ -665,9 +855,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--decode-steps", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="episode")
+    ap.add_argument("--workload", default="train_step")
+    ap.add_argument("--second-workload", default="episode", help="a second training workload on the same line ('' = none)")
     ap.add_argument("--no-rope", action="store_true")
     ap.add_argument("--no-logprob", action="store_true")
+    ap.add_argument("--no-recurrent", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
@@ -675,7 +867,7 @@ def main():
     ap.add_argument("--decode-workload", default="decode", help="decode or decode_small (32 cursors)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--ref-budget", type=float, default=8.0)
+    ap.add_argument("--ref-rows", type=int, default=2, help="sampled rows per step of the reference arm")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))
