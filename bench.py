@@ -646,6 +646,17 @@ def run_ours(args, rank, world, dist):
     hbm, bf16, bf16s, peak_src = peaks()
     seed = rank_seed(args.seed, rank)
 
+    if args.recurrent_only:
+        rec = recurrent_leg(pta, torch, args.recurrent_workload, seed, dev, stream, args.steps, args.warmup, dist)
+        if rank == 0:
+            print(json.dumps({"metric": rec["metric"], "value": rec["roofline"]["achieved"], "unit": "TFLOP/s",
+                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": rec["fwd_ms"] + rec["bwd_ms"], "higher_is_better": True,
+                              "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                              "data": "synthetic (counter-based generator, seed %d + rank)" % args.seed,
+                              "config": {"workload": rec["workload"]}, "recurrent": rec}))
+        return
+
     if args.decode_only:
         dec = decode_leg(pta, torch, args.decode_workload, seed, dev, stream, args.decode_steps, args.warmup,
                          world, dist, hbm, peak_src)
@@ -860,6 +871,8 @@ def main():
     ap.add_argument("--no-rope", action="store_true")
     ap.add_argument("--no-logprob", action="store_true")
     ap.add_argument("--no-recurrent", action="store_true")
+    ap.add_argument("--recurrent-only", action="store_true", help="only the recurrent-layer leg (profiling runs)")
+    ap.add_argument("--recurrent-workload", default="episode", help="DAG whose rows the recurrent leg runs over")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")

@@ -690,7 +690,9 @@ int finish_plan(octo_plan_s* pl, cudaStream_t s) {
     count_launch();
   }
   OCTO_RET(cuda_status(cudaGetLastError()));
-  // ---- launch orders: heaviest tiles / page pairs first (longest-processing-time first) ----
+  // ---- launch orders: tree by tree (concurrent CTAs then read the same tree's rows and
+  // pages, which keeps their shared tiles in L2), heaviest tiles / page pairs first within
+  // a tree (longest-processing-time first) ----
   {
     std::vector<int32_t> toff(n_tiles + 1), poff((size_t)pl->num_pages + 1);
     OCTO_RET(cuda_status(cudaMemcpyAsync(toff.data(), pl->tile_off, (n_tiles + 1) * 4, cudaMemcpyDeviceToHost, s)));
@@ -700,21 +702,26 @@ int finish_plan(octo_plan_s* pl, cudaStream_t s) {
     if (is_decode) pl->h_toff = toff;
     std::vector<int32_t> tord(n_tiles);
     for (int64_t t = 0; t < n_tiles; t++) tord[t] = (int32_t)t;
-    std::stable_sort(tord.begin(), tord.end(),
-                     [&](int32_t a, int32_t b) { return toff[a + 1] - toff[a] > toff[b + 1] - toff[b]; });
+    const std::vector<int32_t>& ttree = pl->h_tile_tree;
+    std::stable_sort(tord.begin(), tord.end(), [&](int32_t a, int32_t b) {
+      if (!ttree.empty() && ttree[a] != ttree[b]) return ttree[a] < ttree[b];
+      return toff[a + 1] - toff[a] > toff[b + 1] - toff[b];
+    });
     const bool any_touched = pl->info.n_touched_pages > 0;
     // dK/dV work units: consecutive own pages of each segment, two at a time, among the
     // touched pages; a touched page without a touched partner runs alone
     if (!is_decode && any_touched) {
-      std::vector<int32_t> pp;
+      std::vector<int32_t> pp, ptree;   // page pairs, and the tree of each
       std::vector<char> seen((size_t)pl->num_pages, 0);
       auto cnt = [&](int32_t pg) { return pg < 0 ? 0 : poff[pg + 1] - poff[pg]; };
-      for (const Segment& g : pool->segs) {
+      for (size_t gi = 0; gi < pool->segs.size(); gi++) {
+        const Segment& g = pool->segs[gi];
         if (g.freed) continue;
+        const int32_t tr = gi < pl->h_seg_tree.size() ? pl->h_seg_tree[gi] : INT32_MAX;
         int32_t pend = -1;
         for (int32_t pg : g.pages) {
           if (pg < 0 || pg >= pl->num_pages || cnt(pg) == 0 || seen[pg]) {
-            if (pend >= 0) { pp.push_back(pend); pp.push_back(-1); pend = -1; }
+            if (pend >= 0) { pp.push_back(pend); pp.push_back(-1); ptree.push_back(tr); pend = -1; }
             continue;
           }
           seen[pg] = 1;
@@ -723,13 +730,14 @@ int finish_plan(octo_plan_s* pl, cudaStream_t s) {
           } else {
             pp.push_back(pend);
             pp.push_back(pg);
+            ptree.push_back(tr);
             pend = -1;
           }
         }
-        if (pend >= 0) { pp.push_back(pend); pp.push_back(-1); }
+        if (pend >= 0) { pp.push_back(pend); pp.push_back(-1); ptree.push_back(tr); }
       }
       for (int32_t pg = 0; pg < pl->num_pages; pg++)
-        if (cnt(pg) > 0 && !seen[pg]) { pp.push_back(pg); pp.push_back(-1); }
+        if (cnt(pg) > 0 && !seen[pg]) { pp.push_back(pg); pp.push_back(-1); ptree.push_back(INT32_MAX); }
       const int32_t np = (int32_t)(pp.size() / 2);
       std::vector<int32_t> poff2(np + 1, 0), pord2(np);
       for (int32_t i = 0; i < np; i++) {
@@ -737,6 +745,7 @@ int finish_plan(octo_plan_s* pl, cudaStream_t s) {
         pord2[i] = i;
       }
       std::stable_sort(pord2.begin(), pord2.end(), [&](int32_t a, int32_t b) {
+        if (ptree[a] != ptree[b]) return ptree[a] < ptree[b];
         return poff2[a + 1] - poff2[a] > poff2[b + 1] - poff2[b];
       });
       pl->n_pairs = np;
@@ -898,6 +907,20 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
   const int32_t* order_src = is_decode ? tile_segs_host : seg_order_host;
   if (n_segs > 0)
     OCTO_TRY(cuda_status(cudaMemcpyAsync(pl->seg_order, order_src, n_segs * 4, cudaMemcpyHostToDevice, s)));
+
+  // ---- tree of every packed segment and tile (training plans: tree-major launch orders) ----
+  if (!is_decode) {
+    pl->h_seg_tree.assign(nseg_all, INT32_MAX);
+    int32_t rank = -1, prev_root = -1;
+    for (int32_t k = 0; k < n_segs; k++) {
+      int32_t r = seg_order_host[k];
+      while (pool->segs[r].parent >= 0) r = pool->segs[r].parent;
+      if (r != prev_root) rank++, prev_root = r;
+      pl->h_seg_tree[seg_order_host[k]] = rank;
+      const int32_t nt = (pool->segs[seg_order_host[k]].len + bm - 1) / bm;
+      pl->h_tile_tree.insert(pl->h_tile_tree.end(), nt, rank);
+    }
+  }
 
   // ---- path predecessors of the packed rows (training plans) ----
   std::vector<int32_t> spred, ep, er;  // pageable sources of async copies: kept to the end

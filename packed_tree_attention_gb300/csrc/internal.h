@@ -110,6 +110,9 @@ struct octo_plan_s {
   int32_t* level_runs = nullptr;     // [n_runs] run ids by level (a run's level = its predecessor's + 1)
   int32_t* chunk_info = nullptr;     // [n_chunks][2] first row, rows
   std::vector<int32_t> h_level_off;  // [n_levels + 1] level slices of level_runs
+  // pack plans: the tree (rank of its root among the packed roots) of every pool segment
+  // (INT32_MAX if not packed) and of every tile, for tree-major launch orders
+  std::vector<int32_t> h_seg_tree, h_tile_tree;
   // decode plans: runs of up to kSplitEntries entries of one cursor (split-KV)
   int32_t n_splits = 0;
   int32_t* split_tile = nullptr;     // [n_splits] cursor (tile) of the split

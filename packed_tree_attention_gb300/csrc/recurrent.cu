@@ -41,7 +41,8 @@ namespace {
 
 constexpr int kC = kRecChunk;     // 64 rows per chunk
 constexpr int kT = 256;           // threads per CTA
-constexpr int kLC = kC + 1;       // padded row length of C x C matrices in shared memory
+constexpr int kLC = kC + 4;       // row length of C x C matrices in shared memory
+constexpr int kL32 = 36;          // row length of C x 32 column blocks in shared memory
 
 struct RecParams {
   const float *q, *k, *v, *alpha, *beta, *dout;
@@ -67,23 +68,134 @@ struct RecParams {
   float* run_grad; // [run][h][D][D] gradient with respect to the run's start state
 };
 
+// Shared-memory tiles keep rows 16-byte aligned with a length of 4 mod 32 floats: 16-byte
+// reads along a row are then free of bank conflicts both when every lane reads the same
+// row (a broadcast) and when the lanes read 32 different rows at the same column.
 template <int D>
 struct Lay {
-  static constexpr int LD = D + 1;   // padded row length of C x D and 32 x D tiles
-  static constexpr int NC = D / 32;  // columns per thread of a C x D tile
+  static constexpr int LD = D + 4;   // row length of C x D and 32 x D tiles
+  static constexpr int NC = D / 32;  // columns per thread of a C x D result
 };
 
-// acc[r][c] += sum_k A[(i0 + r) sai + k sak] * B[k sbk + (j0 + 32 c) sbj], k < K
+__device__ __forceinline__ uint32_t saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// 16-byte global -> shared copy without the registers (zero-filled when !valid)
+__device__ __forceinline__ void cp16(float* dst, const float* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr(dst)), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+}
+// closes the group of this thread's copies issued since the last commit
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// waits until at most N of this thread's committed groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// rows [row0, row0 + rows) of x [N][H][D] at head h into dst [C][LD]; zeros past `rows`
+template <int D>
+__device__ __forceinline__ void cp_rows(float* dst, const float* __restrict__ x, int64_t row0, int rows, int H, int h) {
+  constexpr int Q = D / 4;
+  for (int i = threadIdx.x; i < kC * Q; i += kT) {
+    const int t = i / Q, c = (i % Q) * 4;
+    const bool ok = t < rows;
+    cp16(dst + t * Lay<D>::LD + c, ok ? x + ((row0 + t) * H + h) * D + c : x, ok);
+  }
+}
+// columns [j0, j0 + 32) of the same rows into dst [C][kL32]
+template <int D>
+__device__ __forceinline__ void cp_rows32(float* dst, const float* __restrict__ x, int64_t row0, int rows, int H,
+                                          int h, int j0) {
+  for (int i = threadIdx.x; i < kC * 8; i += kT) {
+    const int t = i >> 3, c = (i & 7) * 4;
+    const bool ok = t < rows;
+    cp16(dst + t * kL32 + c, ok ? x + ((row0 + t) * H + h) * D + j0 + c : x, ok);
+  }
+}
+// a dense [R][D] block into dst [R][LD] (R = C, or 32 rows j0.. of a [D][D] state)
+template <int D, int R = kC>
+__device__ __forceinline__ void cp_blk(float* dst, const float* __restrict__ src) {
+  constexpr int Q = D / 4;
+  for (int i = threadIdx.x; i < R * Q; i += kT) cp16(dst + (i / Q) * Lay<D>::LD + (i % Q) * 4, src + i * 4, true);
+}
+// columns [j0, j0 + 32) of a dense [C][D] block into dst [C][kL32]
+template <int D>
+__device__ __forceinline__ void cp_blk32(float* dst, const float* __restrict__ src, int j0) {
+  for (int i = threadIdx.x; i < kC * 8; i += kT) cp16(dst + (i >> 3) * kL32 + (i & 7) * 4, src + (i >> 3) * D + j0 + (i & 7) * 4, true);
+}
+// a dense [C][C] block into dst [C][kLC]
+__device__ __forceinline__ void cp_cc(float* dst, const float* __restrict__ src) {
+  for (int i = threadIdx.x; i < kC * kC / 4; i += kT) cp16(dst + (i / 16) * kLC + (i % 16) * 4, src + i * 4, true);
+}
+
+// acc[r][c] += sum_k A[i0 + r][k] B[k][j0 + 32 c]      (A, B row-major; K % 4 == 0)
 template <int R, int NC>
-__device__ __forceinline__ void mm(float (&acc)[R][NC], const float* A, int sai, int sak, const float* B, int sbk,
-                                   int sbj, int K, int i0, int j0) {
+__device__ __forceinline__ void mm_nn(float (&acc)[R][NC], const float* A, int lda, const float* B, int ldb, int K,
+                                      int i0, int j0) {
+#pragma unroll 2
+  for (int k = 0; k < K; k += 4) {
+    float4 a[R];
+#pragma unroll
+    for (int r = 0; r < R; r++) a[r] = *reinterpret_cast<const float4*>(A + (i0 + r) * lda + k);
+#pragma unroll
+    for (int kk = 0; kk < 4; kk++) {
+      float b[NC];
+#pragma unroll
+      for (int c = 0; c < NC; c++) b[c] = B[(k + kk) * ldb + j0 + 32 * c];
+#pragma unroll
+      for (int r = 0; r < R; r++) {
+        const float av = kk == 0 ? a[r].x : kk == 1 ? a[r].y : kk == 2 ? a[r].z : a[r].w;
+#pragma unroll
+        for (int c = 0; c < NC; c++) acc[r][c] = fmaf(av, b[c], acc[r][c]);
+      }
+    }
+  }
+}
+
+// acc[r][c] += sum_k A[i0 + r][k] B[j0 + 32 c][k]      (B read by rows: a product with B^T)
+template <int R, int NC>
+__device__ __forceinline__ void mm_nt(float (&acc)[R][NC], const float* A, int lda, const float* B, int ldb, int K,
+                                      int i0, int j0) {
+#pragma unroll 2
+  for (int k = 0; k < K; k += 4) {
+    float4 a[R], b[NC];
+#pragma unroll
+    for (int r = 0; r < R; r++) a[r] = *reinterpret_cast<const float4*>(A + (i0 + r) * lda + k);
+#pragma unroll
+    for (int c = 0; c < NC; c++) b[c] = *reinterpret_cast<const float4*>(B + (j0 + 32 * c) * ldb + k);
+#pragma unroll
+    for (int r = 0; r < R; r++)
+#pragma unroll
+      for (int c = 0; c < NC; c++) {
+        acc[r][c] = fmaf(a[r].x, b[c].x, acc[r][c]);
+        acc[r][c] = fmaf(a[r].y, b[c].y, acc[r][c]);
+        acc[r][c] = fmaf(a[r].z, b[c].z, acc[r][c]);
+        acc[r][c] = fmaf(a[r].w, b[c].w, acc[r][c]);
+      }
+  }
+}
+
+// acc[r][c] += sum_k A[k][i0 + r] B[k][j0 + 32 c]      (A read by columns: a product with A^T;
+// i0 % 4 == 0)
+template <int R, int NC>
+__device__ __forceinline__ void mm_tn(float (&acc)[R][NC], const float* A, int lda, const float* B, int ldb, int K,
+                                      int i0, int j0) {
 #pragma unroll 4
   for (int k = 0; k < K; k++) {
     float a[R], b[NC];
 #pragma unroll
-    for (int r = 0; r < R; r++) a[r] = A[(i0 + r) * sai + k * sak];
+    for (int r = 0; r < R; r += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(A + k * lda + i0 + r);
+      a[r] = x.x;
+      a[r + 1] = x.y;
+      a[r + 2] = x.z;
+      a[r + 3] = x.w;
+    }
 #pragma unroll
-    for (int c = 0; c < NC; c++) b[c] = B[k * sbk + (j0 + 32 * c) * sbj];
+    for (int c = 0; c < NC; c++) b[c] = B[k * ldb + j0 + 32 * c];
 #pragma unroll
     for (int r = 0; r < R; r++)
 #pragma unroll
@@ -99,43 +211,28 @@ __device__ __forceinline__ void zero(float (&acc)[R][NC]) {
     for (int c = 0; c < NC; c++) acc[r][c] = 0.f;
 }
 
-// rows [row0, row0 + rows) of x [N][H][D] at head h into dst [C][LD]; zeros past `rows`
-template <int D>
-__device__ __forceinline__ void load_rows(float* dst, const float* __restrict__ x, int64_t row0, int rows, int H,
-                                          int h) {
-  for (int i = threadIdx.x; i < kC * D; i += kT) {
-    const int t = i / D, c = i % D;
-    dst[t * Lay<D>::LD + c] = t < rows ? x[((row0 + t) * H + h) * D + c] : 0.f;
-  }
-}
-// a dense [C][D] block of the workspace into dst [C][LD]
-template <int D>
-__device__ __forceinline__ void load_blk(float* dst, const float* __restrict__ src) {
-  for (int i = threadIdx.x; i < kC * D; i += kT) dst[(i / D) * Lay<D>::LD + i % D] = src[i];
-}
-// rows [j0, j0 + 32) of a dense [D][D] state into dst [32][LD]
-template <int D>
-__device__ __forceinline__ void load_state_rows(float* dst, const float* __restrict__ src, int j0) {
-  for (int i = threadIdx.x; i < 32 * D; i += kT) dst[(i / D) * Lay<D>::LD + i % D] = src[(j0 + i / D) * D + i % D];
-}
-
 // per-row gate values of one chunk: lg (running sum of log alpha), beta, rows past the end
-// get alpha = 1, beta = 0 (no effect)
+// get alpha = 1, beta = 0 (no effect).  Ends with a block barrier.
 __device__ __forceinline__ void load_gates(float* lg, float* be, float* al, const float* __restrict__ alpha,
                                            const float* __restrict__ beta, int64_t row0, int rows, int H, int h) {
-  if (threadIdx.x < kC) {
-    const int t = threadIdx.x;
-    al[t] = t < rows ? alpha[(row0 + t) * H + h] : 1.f;
+  __shared__ float warp_tot;
+  const int t = threadIdx.x;
+  float x = 0.f;
+  if (t < kC) {
+    const float a = t < rows ? alpha[(row0 + t) * H + h] : 1.f;
+    al[t] = a;
     be[t] = t < rows ? beta[(row0 + t) * H + h] : 0.f;
+    x = logf(a);
+    // inclusive running sum within the warp (rows 0-31, 32-63)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if ((t & 31) >= o) x += y;
+    }
+    if (t == 31) warp_tot = x;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float s = 0.f;
-    for (int t = 0; t < kC; t++) {
-      s += logf(al[t]);
-      lg[t] = s;
-    }
-  }
+  if (t < kC) lg[t] = t >= 32 ? x + warp_tot : x;
   __syncthreads();
 }
 
@@ -143,8 +240,7 @@ __device__ __forceinline__ void load_gates(float* lg, float* be, float* al, cons
 template <int D>
 __device__ __forceinline__ void gram(float (&acc)[8][2], const float* X, const float* Y) {
   zero(acc);
-  const int i0 = (threadIdx.x >> 5) * 8, j0 = threadIdx.x & 31;
-  mm(acc, X, Lay<D>::LD, 1, Y, 1, Lay<D>::LD, D, i0, j0);
+  mm_nt(acc, X, Lay<D>::LD, Y, Lay<D>::LD, D, (threadIdx.x >> 5) * 8, threadIdx.x & 31);
 }
 
 // =====================================================================================
@@ -155,8 +251,8 @@ __device__ __forceinline__ void gram(float (&acc)[8][2], const float* X, const f
 // U = Minv diag(beta) V.
 template <int D>
 __global__ void __launch_bounds__(kT) k_rec_prep(RecParams p) {
-  constexpr int LD = Lay<D>::LD;
-  extern __shared__ float sm[];
+  constexpr int LD = Lay<D>::LD, NC = Lay<D>::NC;
+  extern __shared__ __align__(16) float sm[];
   float* sK = sm;
   float* sV = sK + kC * LD;
   float* sA = sV + kC * LD;
@@ -168,10 +264,13 @@ __global__ void __launch_bounds__(kT) k_rec_prep(RecParams p) {
   const int64_t row0 = p.chunk_info[2 * ch];
   const int rows = p.chunk_info[2 * ch + 1];
   const size_t blk = (size_t)ch * p.H + h;
-  load_rows<D>(sK, p.k, row0, rows, p.H, h);
-  load_rows<D>(sV, p.v, row0, rows, p.H, h);
-  load_gates(lg, be, al, p.alpha, p.beta, row0, rows, p.H, h);
   const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
+  cp_rows<D>(sK, p.k, row0, rows, p.H, h);
+  cp_rows<D>(sV, p.v, row0, rows, p.H, h);
+  for (int i = threadIdx.x; i < kC * kLC; i += kT) sMi[i] = 0.f;
+  load_gates(lg, be, al, p.alpha, p.beta, row0, rows, p.H, h);
+  cp_wait();
+  __syncthreads();
   {
     float acc[8][2];
     gram<D>(acc, sK, sK);
@@ -183,19 +282,27 @@ __global__ void __launch_bounds__(kT) k_rec_prep(RecParams p) {
         sA[t * kLC + s] = s < t ? expf(lg[t] - lg[s]) * acc[r][c] : 0.f;
       }
   }
-  // forward substitution, one row of Minv at a time: Minv[t][s] = [t == s]
-  //   - beta_t sum_{s <= u < t} A[t][u] Minv[u][s]
-  for (int i = threadIdx.x; i < kC * kLC; i += kT) sMi[i] = 0.f;
   __syncthreads();
-  for (int t = 0; t < kC; t++) {
-    if (threadIdx.x <= t) {
-      const int s = threadIdx.x;
-      float x = 0.f;
-      for (int u = s; u < t; u++) x = fmaf(sA[t * kLC + u], sMi[u * kLC + s], x);
-      sMi[t * kLC + s] = (s == t ? 1.f : 0.f) - be[t] * x;
+  // forward substitution, a column of Minv per thread (columns are independent):
+  //   Minv[t][s] = [t == s] - beta_t sum_{u < t} A[t][u] Minv[u][s], Minv[u][s] = 0 for u < s;
+  // every lane walks the same t and u, so the reads of A are broadcasts
+  if (threadIdx.x < kC) {
+    const int s = threadIdx.x;
+    for (int t = 0; t < kC; t++) {
+      float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;   // four chains for the FMA latency
+      int u = 0;
+      for (; u + 4 <= t; u += 4) {
+        x0 = fmaf(sA[t * kLC + u], sMi[u * kLC + s], x0);
+        x1 = fmaf(sA[t * kLC + u + 1], sMi[(u + 1) * kLC + s], x1);
+        x2 = fmaf(sA[t * kLC + u + 2], sMi[(u + 2) * kLC + s], x2);
+        x3 = fmaf(sA[t * kLC + u + 3], sMi[(u + 3) * kLC + s], x3);
+      }
+      for (; u < t; u++) x0 = fmaf(sA[t * kLC + u], sMi[u * kLC + s], x0);
+      const float x = (x0 + x1) + (x2 + x3);
+      sMi[t * kLC + s] = (s == t ? 1.f : 0.f) - (t > s ? be[t] * x : 0.f);
     }
-    __syncthreads();
   }
+  __syncthreads();
   // rows of K scaled by beta g, of V by beta
   for (int i = threadIdx.x; i < kC * D; i += kT) {
     const int t = i / D, c = i % D;
@@ -203,12 +310,11 @@ __global__ void __launch_bounds__(kT) k_rec_prep(RecParams p) {
     sV[t * LD + c] *= be[t];
   }
   __syncthreads();
-  constexpr int NC = Lay<D>::NC;
   float w[8][NC], u[8][NC];
   zero(w);
   zero(u);
-  mm(w, sMi, kLC, 1, sK, LD, 1, kC, ty * 8, tx);
-  mm(u, sMi, kLC, 1, sV, LD, 1, kC, ty * 8, tx);
+  mm_nn(w, sMi, kLC, sK, LD, kC, ty * 8, tx);
+  mm_nn(u, sMi, kLC, sV, LD, kC, ty * 8, tx);
   float* Wg = p.Wb + blk * kC * D;
   float* Ug = p.Ub + blk * kC * D;
 #pragma unroll
@@ -229,13 +335,15 @@ __global__ void __launch_bounds__(kT) k_rec_prep(RecParams p) {
 // continue from it.
 template <int D>
 __global__ void __launch_bounds__(kT) k_rec_scan_fwd(RecParams p, int32_t lvl0) {
+  // single-buffered on purpose: at 94 KB of shared memory two CTAs share an SM, and a
+  // level's chains finish in one round of CTAs instead of two
   constexpr int LD = Lay<D>::LD, NC = Lay<D>::NC, NB = D / 32;
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* sW = sm;
   float* sK = sW + kC * LD;
   float* sS = sK + kC * LD;          // [32][LD]
-  float* sU = sS + 32 * LD;          // [C][33]: U, then Delta (scaled by g_C / g)
-  float* lg = sU + kC * 33;
+  float* sU = sS + 32 * LD;          // [C][kL32]: U, then Delta (scaled by g_C / g)
+  float* lg = sU + kC * kL32;
   const int li = blockIdx.x / (p.H * NB), h = (blockIdx.x / NB) % p.H, jb = blockIdx.x % NB;
   const int run = p.level_runs[lvl0 + li];
   const int32_t r0 = p.run_info[4 * run], r1 = p.run_info[4 * run + 1];
@@ -244,43 +352,45 @@ __global__ void __launch_bounds__(kT) k_rec_scan_fwd(RecParams p, int32_t lvl0) 
   const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
   const int j0 = jb * 32;
   if (pr >= 0)
-    load_state_rows<D>(sS, p.run_end + ((size_t)pr * p.H + h) * D * D, j0);
+    cp_blk<D, 32>(sS, p.run_end + ((size_t)pr * p.H + h) * D * D + (size_t)j0 * D);
   else
     for (int i = threadIdx.x; i < 32 * LD; i += kT) sS[i] = 0.f;
-  __syncthreads();
   for (int ci = 0; ci < nch; ci++) {
     const int ch = c0 + ci;
     const size_t blk = (size_t)ch * p.H + h;
-    float* S0g = p.S0 + blk * D * D;
-    for (int i = threadIdx.x; i < 32 * D; i += kT) S0g[(j0 + i / D) * D + i % D] = sS[(i / D) * LD + i % D];
     const int64_t row0 = p.chunk_info[2 * ch];
     const int rows = p.chunk_info[2 * ch + 1];
-    load_blk<D>(sW, p.Wb + blk * kC * D);
-    load_rows<D>(sK, p.k, row0, rows, p.H, h);
-    const float* Ug = p.Ub + blk * kC * D;
-    for (int i = threadIdx.x; i < kC * 32; i += kT) sU[(i >> 5) * 33 + (i & 31)] = Ug[(i >> 5) * D + j0 + (i & 31)];
-    if (threadIdx.x < kC) lg[threadIdx.x] = p.Lb[blk * kC + threadIdx.x];
+    cp_blk<D>(sW, p.Wb + blk * kC * D);
+    cp_blk32<D>(sU, p.Ub + blk * kC * D, j0);
+    if (threadIdx.x < kC / 4) cp16(lg + threadIdx.x * 4, p.Lb + blk * kC + threadIdx.x * 4, true);
+    cp_commit();
+    cp_rows<D>(sK, p.k, row0, rows, p.H, h);   // needed only after Delta: a group of its own
+    cp_commit();
+    cp_wait_group<1>();
     __syncthreads();
+    float* S0g = p.S0 + blk * D * D + (size_t)j0 * D;
+    for (int i = threadIdx.x; i < 32 * D / 4; i += kT)
+      *reinterpret_cast<float4*>(S0g + i * 4) = *reinterpret_cast<const float4*>(sS + (i / (D / 4)) * LD + (i % (D / 4)) * 4);
     {
       float acc[8][1];
       zero(acc);
-      mm(acc, sW, LD, 1, sS, 1, LD, D, ty * 8, tx);   // (W S0^T)[t][j]
+      mm_nt(acc, sW, LD, sS, LD, D, ty * 8, tx);   // (W S0^T)[t][j]
       const float gC = lg[kC - 1];
       float* Dg = p.Db + blk * kC * D;
-      __syncthreads();
 #pragma unroll
       for (int r = 0; r < 8; r++) {
         const int t = ty * 8 + r;
-        const float dl = sU[t * 33 + tx] - acc[r][0];
+        const float dl = sU[t * kL32 + tx] - acc[r][0];
         Dg[t * D + j0 + tx] = dl;
-        sU[t * 33 + tx] = dl * expf(gC - lg[t]);
+        sU[t * kL32 + tx] = dl * expf(gC - lg[t]);
       }
     }
+    cp_wait_group<0>();
     __syncthreads();
     {
       float acc[4][NC];
       zero(acc);
-      mm(acc, sU, 1, 33, sK, LD, 1, kC, ty * 4, tx);   // (Delta^T diag(g_C/g) K)[j][k]
+      mm_tn(acc, sU, kL32, sK, LD, kC, ty * 4, tx);   // (Delta^T diag(g_C/g) K)[j][k]
       const float gC = expf(lg[kC - 1]);
 #pragma unroll
       for (int r = 0; r < 4; r++)
@@ -292,19 +402,20 @@ __global__ void __launch_bounds__(kT) k_rec_scan_fwd(RecParams p, int32_t lvl0) 
     }
     __syncthreads();
   }
-  float* Eg = p.run_end + ((size_t)run * p.H + h) * D * D;
-  for (int i = threadIdx.x; i < 32 * D; i += kT) Eg[(j0 + i / D) * D + i % D] = sS[(i / D) * LD + i % D];
+  float* Eg = p.run_end + ((size_t)run * p.H + h) * D * D + (size_t)j0 * D;
+  for (int i = threadIdx.x; i < 32 * D / 4; i += kT)
+    *reinterpret_cast<float4*>(Eg + i * 4) = *reinterpret_cast<const float4*>(sS + (i / (D / 4)) * LD + (i % (D / 4)) * 4);
 }
 
-// Outputs per chunk and head: O = diag(g) Q S0^T + tril(G o Q K^T) Delta.
+// Outputs per chunk and head: O = diag(g) Q S0^T + tril(G o Q K^T) Delta.  K's buffer takes
+// Delta once the Q K^T block is formed.
 template <int D>
 __global__ void __launch_bounds__(kT) k_rec_out(RecParams p) {
   constexpr int LD = Lay<D>::LD, NC = Lay<D>::NC;
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* sQ = sm;
-  float* sK = sQ + kC * LD;
-  float* sD = sK + kC * LD;
-  float* sS = sD + kC * LD;    // [32][LD] slice of S0
+  float* sKD = sQ + kC * LD;   // K, then Delta
+  float* sS = sKD + kC * LD;   // [32][LD] rows of S0
   float* sB = sS + 32 * LD;    // [C][kLC]
   float* lg = sB + kC * kLC;
   const int ch = blockIdx.x / p.H, h = blockIdx.x % p.H;
@@ -312,14 +423,14 @@ __global__ void __launch_bounds__(kT) k_rec_out(RecParams p) {
   const int rows = p.chunk_info[2 * ch + 1];
   const size_t blk = (size_t)ch * p.H + h;
   const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
-  load_rows<D>(sQ, p.q, row0, rows, p.H, h);
-  load_rows<D>(sK, p.k, row0, rows, p.H, h);
-  load_blk<D>(sD, p.Db + blk * kC * D);
+  cp_rows<D>(sQ, p.q, row0, rows, p.H, h);
+  cp_rows<D>(sKD, p.k, row0, rows, p.H, h);
   if (threadIdx.x < kC) lg[threadIdx.x] = p.Lb[blk * kC + threadIdx.x];
+  cp_wait();
   __syncthreads();
   {
     float acc[8][2];
-    gram<D>(acc, sQ, sK);
+    gram<D>(acc, sQ, sKD);
 #pragma unroll
     for (int r = 0; r < 8; r++)
 #pragma unroll
@@ -328,21 +439,23 @@ __global__ void __launch_bounds__(kT) k_rec_out(RecParams p) {
         sB[t * kLC + s] = s <= t ? expf(lg[t] - lg[s]) * acc[r][c] : 0.f;
       }
   }
+  __syncthreads();
+  cp_blk<D>(sKD, p.Db + blk * kC * D);
   float out[8][NC];
-  zero(out);
   const float* S0g = p.S0 + blk * D * D;
 #pragma unroll
   for (int js = 0; js < NC; js++) {
-    __syncthreads();
-    load_state_rows<D>(sS, S0g, 32 * js);
+    if (js) __syncthreads();
+    cp_blk<D, 32>(sS, S0g + (size_t)32 * js * D);
+    cp_wait();
     __syncthreads();
     float acc[8][1];
     zero(acc);
-    mm(acc, sQ, LD, 1, sS, 1, LD, D, ty * 8, tx);
+    mm_nt(acc, sQ, LD, sS, LD, D, ty * 8, tx);
 #pragma unroll
     for (int r = 0; r < 8; r++) out[r][js] = acc[r][0] * expf(lg[ty * 8 + r]);
   }
-  mm(out, sB, kLC, 1, sD, LD, 1, kC, ty * 8, tx);
+  mm_nn(out, sB, kLC, sKD, LD, kC, ty * 8, tx);
 #pragma unroll
   for (int r = 0; r < 8; r++) {
     const int t = ty * 8 + r;
@@ -356,29 +469,28 @@ __global__ void __launch_bounds__(kT) k_rec_out(RecParams p) {
 // backward
 // =====================================================================================
 
-// E = diag(g) Q - tril(G o Q K^T) W per chunk and head.
+// E = diag(g) Q - tril(G o Q K^T) W per chunk and head (K's buffer then holds W).
 template <int D>
 __global__ void __launch_bounds__(kT) k_rec_prep_bwd(RecParams p) {
   constexpr int LD = Lay<D>::LD, NC = Lay<D>::NC;
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* sQ = sm;
-  float* sK = sQ + kC * LD;
-  float* sW = sK + kC * LD;
-  float* sB = sW + kC * LD;
+  float* sKW = sQ + kC * LD;
+  float* sB = sKW + kC * LD;
   float* lg = sB + kC * kLC;
   const int ch = blockIdx.x / p.H, h = blockIdx.x % p.H;
   const int64_t row0 = p.chunk_info[2 * ch];
   const int rows = p.chunk_info[2 * ch + 1];
   const size_t blk = (size_t)ch * p.H + h;
   const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
-  load_rows<D>(sQ, p.q, row0, rows, p.H, h);
-  load_rows<D>(sK, p.k, row0, rows, p.H, h);
-  load_blk<D>(sW, p.Wb + blk * kC * D);
+  cp_rows<D>(sQ, p.q, row0, rows, p.H, h);
+  cp_rows<D>(sKW, p.k, row0, rows, p.H, h);
   if (threadIdx.x < kC) lg[threadIdx.x] = p.Lb[blk * kC + threadIdx.x];
+  cp_wait();
   __syncthreads();
   {
     float acc[8][2];
-    gram<D>(acc, sQ, sK);
+    gram<D>(acc, sQ, sKW);
 #pragma unroll
     for (int r = 0; r < 8; r++)
 #pragma unroll
@@ -388,6 +500,9 @@ __global__ void __launch_bounds__(kT) k_rec_prep_bwd(RecParams p) {
       }
   }
   __syncthreads();
+  cp_blk<D>(sKW, p.Wb + blk * kC * D);
+  cp_wait();
+  __syncthreads();
   float e[8][NC];
 #pragma unroll
   for (int r = 0; r < 8; r++) {
@@ -395,7 +510,7 @@ __global__ void __launch_bounds__(kT) k_rec_prep_bwd(RecParams p) {
 #pragma unroll
     for (int c = 0; c < NC; c++) e[r][c] = g * sQ[(ty * 8 + r) * LD + tx + 32 * c];
   }
-  mm(e, sB, kLC, 1, sW, LD, 1, kC, ty * 8, tx);
+  mm_nn(e, sB, kLC, sKW, LD, kC, ty * 8, tx);
   float* Eg = p.Ub + blk * kC * D;
 #pragma unroll
   for (int r = 0; r < 8; r++)
@@ -411,47 +526,55 @@ __global__ void __launch_bounds__(kT) k_rec_prep_bwd(RecParams p) {
 template <int D>
 __global__ void __launch_bounds__(kT) k_rec_scan_bwd(RecParams p, int32_t lvl0) {
   constexpr int LD = Lay<D>::LD, NC = Lay<D>::NC, NB = D / 32;
-  extern __shared__ float sm[];
-  float* sK = sm;
-  float* sW = sK + kC * LD;
+  extern __shared__ __align__(16) float sm[];
+  float* sKb = sm;                   // 2 x ([C][LD] K, [C] lg)
+  constexpr int kSetK = kC * LD + kC;
+  float* sW = sKb + 2 * kSetK;
   float* sE = sW + kC * LD;
   float* sG = sE + kC * LD;          // [32][LD]
   float* sX = sG + 32 * LD;          // [32][kLC]
-  float* sO = sX + 32 * kLC;         // [C][33] rows of dO, this block's columns
-  float* lg = sO + kC * 33;
+  float* sO = sX + 32 * kLC;         // [C][kL32] rows of dO, this block's columns
   const int li = blockIdx.x / (p.H * NB), h = (blockIdx.x / NB) % p.H, jb = blockIdx.x % NB;
   const int run = p.level_runs[lvl0 + li];
   const int32_t r0 = p.run_info[4 * run], r1 = p.run_info[4 * run + 1], c0 = p.run_info[4 * run + 3];
   const int nch = (r1 - r0 + kC - 1) / kC;
   const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
   const int j0 = jb * 32;
+  auto issue_k = [&](int ci, int b) {
+    const int ch = c0 + ci;
+    const size_t blk = (size_t)ch * p.H + h;
+    float* set = sKb + b * kSetK;
+    cp_rows<D>(set, p.k, p.chunk_info[2 * ch], p.chunk_info[2 * ch + 1], p.H, h);
+    if (threadIdx.x < kC / 4) cp16(set + kC * LD + threadIdx.x * 4, p.Lb + blk * kC + threadIdx.x * 4, true);
+    cp_commit();
+  };
+  issue_k(nch - 1, (nch - 1) & 1);
   for (int i = threadIdx.x; i < 32 * D; i += kT) {
     float x = 0.f;
     for (int c = p.child_off[run]; c < p.child_off[run + 1]; c++)
       x += p.run_grad[((size_t)p.child[c] * p.H + h) * D * D + (j0 + i / D) * D + i % D];
     sG[(i / D) * LD + i % D] = x;
   }
-  __syncthreads();
   for (int ci = nch - 1; ci >= 0; ci--) {
     const int ch = c0 + ci;
     const size_t blk = (size_t)ch * p.H + h;
-    float* Gg = p.Gb + blk * D * D;
-    for (int i = threadIdx.x; i < 32 * D; i += kT) Gg[(j0 + i / D) * D + i % D] = sG[(i / D) * LD + i % D];
     const int64_t row0 = p.chunk_info[2 * ch];
     const int rows = p.chunk_info[2 * ch + 1];
-    load_rows<D>(sK, p.k, row0, rows, p.H, h);
-    load_blk<D>(sW, p.Wb + blk * kC * D);
-    load_blk<D>(sE, p.Ub + blk * kC * D);
-    for (int i = threadIdx.x; i < kC * 32; i += kT) {
-      const int t = i >> 5;
-      sO[t * 33 + (i & 31)] = t < rows ? p.dout[((row0 + t) * p.H + h) * D + j0 + (i & 31)] : 0.f;
-    }
-    if (threadIdx.x < kC) lg[threadIdx.x] = p.Lb[blk * kC + threadIdx.x];
+    float* sK = sKb + (ci & 1) * kSetK;
+    float* lg = sK + kC * LD;
+    cp_blk<D>(sW, p.Wb + blk * kC * D);
+    cp_blk<D>(sE, p.Ub + blk * kC * D);
+    cp_rows32<D>(sO, p.dout, row0, rows, p.H, h, j0);
+    cp_commit();
+    cp_wait_group<1>();   // this chunk's K and lg
     __syncthreads();
+    float* Gg = p.Gb + blk * D * D + (size_t)j0 * D;
+    for (int i = threadIdx.x; i < 32 * D / 4; i += kT)
+      *reinterpret_cast<float4*>(Gg + i * 4) = *reinterpret_cast<const float4*>(sG + (i / (D / 4)) * LD + (i % (D / 4)) * 4);
     {
       float acc[4][2];
       zero(acc);
-      mm(acc, sG, LD, 1, sK, 1, LD, D, ty * 4, tx);   // (G K^T)[j][t]
+      mm_nt(acc, sG, LD, sK, LD, D, ty * 4, tx);   // (G K^T)[j][t]
       const float gC = lg[kC - 1];
 #pragma unroll
       for (int r = 0; r < 4; r++)
@@ -461,13 +584,19 @@ __global__ void __launch_bounds__(kT) k_rec_scan_bwd(RecParams p, int32_t lvl0) 
           sX[(ty * 4 + r) * kLC + t] = acc[r][c] * expf(gC - lg[t]);
         }
     }
+    if (ci > 0) {
+      issue_k(ci - 1, (ci - 1) & 1);   // the other buffer: its last reader finished a chunk ago
+      cp_wait_group<1>();              // this chunk's W, E, dO
+    } else {
+      cp_wait_group<0>();
+    }
     __syncthreads();
     {
       float acc[4][NC], acc2[4][NC];
       zero(acc);
       zero(acc2);
-      mm(acc, sX, kLC, 1, sW, LD, 1, kC, ty * 4, tx);
-      mm(acc2, sO, 1, 33, sE, LD, 1, kC, ty * 4, tx);
+      mm_nn(acc, sX, kLC, sW, LD, kC, ty * 4, tx);
+      mm_tn(acc2, sO, kL32, sE, LD, kC, ty * 4, tx);
       const float gC = expf(lg[kC - 1]);
 #pragma unroll
       for (int r = 0; r < 4; r++)
@@ -479,8 +608,9 @@ __global__ void __launch_bounds__(kT) k_rec_scan_bwd(RecParams p, int32_t lvl0) 
     }
     __syncthreads();
   }
-  float* Rg = p.run_grad + ((size_t)run * p.H + h) * D * D;
-  for (int i = threadIdx.x; i < 32 * D; i += kT) Rg[(j0 + i / D) * D + i % D] = sG[(i / D) * LD + i % D];
+  float* Rg = p.run_grad + ((size_t)run * p.H + h) * D * D + (size_t)j0 * D;
+  for (int i = threadIdx.x; i < 32 * D / 4; i += kT)
+    *reinterpret_cast<float4*>(Rg + i * 4) = *reinterpret_cast<const float4*>(sG + (i / (D / 4)) * LD + (i % (D / 4)) * 4);
 }
 
 // sum over the 32 lanes of a warp
@@ -494,18 +624,19 @@ __device__ __forceinline__ float warp_sum(float x) {
 // Gbar = diag(g_C / g) K G_C^T + tril(G o Q K^T)^T dO (gradient of Delta);
 // Y = Minv^T Gbar; dv = diag(beta) Y; dbeta_t = Y_t . (X_t - (A Delta)_t); and the row
 // parts of the gate gradient: g_t dg_t = -dv_t . (g_t K S0^T)_t + g_t dO_t . (Q S0^T)_t and
-// r_t = (g_C / g_t) Delta_t . (K G_C^T)_t.  Y goes to the workspace for part b.
+// r_t = (g_C / g_t) Delta_t . (K G_C^T)_t, and <G_C, S0>.  Y goes to the workspace for part b.
 template <int D>
 __global__ void __launch_bounds__(kT) k_rec_grad_a(RecParams p) {
   constexpr int LD = Lay<D>::LD, NC = Lay<D>::NC;
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* sK = sm;
   float* sQ = sK + kC * LD;      // Q, later Delta
   float* sO = sQ + kC * LD;      // dO
   float* sX = sO + kC * LD;      // V, then X
   float* sY = sX + kC * LD;      // Gbar, then Y
-  float* sS = sY + kC * LD;      // [32][LD] slice of S0 or G_C
-  float* sB = sS + 32 * LD;      // [C][kLC]: tril(G o Q K^T), then Minv, then A
+  float* sS = sY + kC * LD;      // [32][LD] rows of S0
+  float* sT = sS + 32 * LD;      // [32][LD] the same rows of G_C
+  float* sB = sT + 32 * LD;      // [C][kLC]: tril(G o Q K^T), then Minv, then A
   float* lg = sB + kC * kLC;
   float* be = lg + kC;
   float* al = be + kC;
@@ -514,11 +645,20 @@ __global__ void __launch_bounds__(kT) k_rec_grad_a(RecParams p) {
   const int rows = p.chunk_info[2 * ch + 1];
   const size_t blk = (size_t)ch * p.H + h;
   const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
-  load_rows<D>(sK, p.k, row0, rows, p.H, h);
-  load_rows<D>(sQ, p.q, row0, rows, p.H, h);
-  load_rows<D>(sO, p.dout, row0, rows, p.H, h);
-  load_rows<D>(sX, p.v, row0, rows, p.H, h);
+  const float* S0g = p.S0 + blk * D * D;
+  const float* GCg = p.Gb + blk * D * D;
+  cp_rows<D>(sK, p.k, row0, rows, p.H, h);
+  cp_rows<D>(sQ, p.q, row0, rows, p.H, h);
+  cp_rows<D>(sO, p.dout, row0, rows, p.H, h);
+  cp_rows<D>(sX, p.v, row0, rows, p.H, h);
+  cp_commit();
+  cp_blk<D, 32>(sS, S0g);
+  cp_commit();
+  cp_blk<D, 32>(sT, GCg);
+  cp_commit();
   load_gates(lg, be, al, p.alpha, p.beta, row0, rows, p.H, h);
+  cp_wait_group<2>();
+  __syncthreads();
   {
     float acc[8][2];
     gram<D>(acc, sQ, sK);
@@ -533,21 +673,20 @@ __global__ void __launch_bounds__(kT) k_rec_grad_a(RecParams p) {
   float pq[8], pr[8], pdb[8], gsum = 0.f;
 #pragma unroll
   for (int r = 0; r < 8; r++) pq[r] = pr[r] = pdb[r] = 0.f;
-  const float* S0g = p.S0 + blk * D * D;
-  const float* GCg = p.Gb + blk * D * D;
   const float* Dg = p.Db + blk * kC * D;
   const float lgC = lg[kC - 1];
+  // row block js of S0 in sS and of G_C in sT; block js + 1 of S0 is fetched while G_C's
+  // block js is used, and of G_C while S0's block js + 1 is used
 #pragma unroll
   for (int js = 0; js < NC; js++) {
     const int j = 32 * js + tx;
-    __syncthreads();
-    load_state_rows<D>(sS, S0g, 32 * js);
+    cp_wait_group<1>();   // S0 rows of block js
     __syncthreads();
     float ks[8][1], qs[8][1];
     zero(ks);
     zero(qs);
-    mm(ks, sK, LD, 1, sS, 1, LD, D, ty * 8, tx);
-    mm(qs, sQ, LD, 1, sS, 1, LD, D, ty * 8, tx);
+    mm_nt(ks, sK, LD, sS, LD, D, ty * 8, tx);
+    mm_nt(qs, sQ, LD, sS, LD, D, ty * 8, tx);
 #pragma unroll
     for (int r = 0; r < 8; r++) {
       const int t = ty * 8 + r;
@@ -555,14 +694,16 @@ __global__ void __launch_bounds__(kT) k_rec_grad_a(RecParams p) {
       sX[t * LD + j] -= g * ks[r][0];
       pq[r] = fmaf(sO[t * LD + j], g * qs[r][0], pq[r]);
     }
-    __syncthreads();
-    load_state_rows<D>(sS, GCg, 32 * js);
+    cp_wait_group<0>();   // G_C rows of block js
     __syncthreads();
     for (int i = threadIdx.x; i < 32 * D; i += kT)   // <G_C, S0> over these rows
-      gsum = fmaf(sS[(i / D) * LD + i % D], S0g[(32 * js + i / D) * D + i % D], gsum);
+      gsum = fmaf(sS[(i / D) * LD + i % D], sT[(i / D) * LD + i % D], gsum);
+    __syncthreads();
+    if (js + 1 < NC) cp_blk<D, 32>(sS, S0g + (size_t)32 * (js + 1) * D);
+    cp_commit();
     float kg[8][1];
     zero(kg);
-    mm(kg, sK, LD, 1, sS, 1, LD, D, ty * 8, tx);
+    mm_nt(kg, sK, LD, sT, LD, D, ty * 8, tx);
 #pragma unroll
     for (int r = 0; r < 8; r++) {
       const int t = ty * 8 + r;
@@ -570,24 +711,28 @@ __global__ void __launch_bounds__(kT) k_rec_grad_a(RecParams p) {
       sY[t * LD + j] = rc;
       pr[r] = fmaf(Dg[t * D + j], rc, pr[r]);
     }
+    __syncthreads();
+    if (js + 1 < NC) cp_blk<D, 32>(sT, GCg + (size_t)32 * (js + 1) * D);
+    cp_commit();
   }
+  cp_wait_group<0>();
   __syncthreads();
   {
     float acc[8][NC];
     zero(acc);
-    mm(acc, sB, 1, kLC, sO, LD, 1, kC, ty * 8, tx);   // tril(G o Q K^T)^T dO
+    mm_tn(acc, sB, kLC, sO, LD, kC, ty * 8, tx);   // tril(G o Q K^T)^T dO
 #pragma unroll
     for (int r = 0; r < 8; r++)
 #pragma unroll
       for (int c = 0; c < NC; c++) sY[(ty * 8 + r) * LD + tx + 32 * c] += acc[r][c];
   }
   __syncthreads();
-  const float* Mg = p.Mb + blk * kC * kC;
-  for (int i = threadIdx.x; i < kC * kC; i += kT) sB[(i / kC) * kLC + i % kC] = Mg[i];
+  cp_cc(sB, p.Mb + blk * kC * kC);
+  cp_wait();
   __syncthreads();
   float y[8][NC];
   zero(y);
-  mm(y, sB, 1, kLC, sY, LD, 1, kC, ty * 8, tx);     // Minv^T Gbar
+  mm_tn(y, sB, kLC, sY, LD, kC, ty * 8, tx);     // Minv^T Gbar
   __syncthreads();
   float* Yg = p.Yb + blk * kC * D;
 #pragma unroll
@@ -618,13 +763,14 @@ __global__ void __launch_bounds__(kT) k_rec_grad_a(RecParams p) {
         const int t = ty * 8 + r, s = tx + 32 * c;
         sB[t * kLC + s] = s < t ? expf(lg[t] - lg[s]) * acc[r][c] : 0.f;
       }
-    load_blk<D>(sQ, Dg);
+    cp_blk<D>(sQ, Dg);
+    cp_wait();
   }
   __syncthreads();
   {
     float ad[8][NC];
     zero(ad);
-    mm(ad, sB, kLC, 1, sQ, LD, 1, kC, ty * 8, tx);
+    mm_nn(ad, sB, kLC, sQ, LD, kC, ty * 8, tx);
 #pragma unroll
     for (int r = 0; r < 8; r++) {
       const int t = ty * 8 + r;
@@ -668,32 +814,80 @@ __global__ void __launch_bounds__(kT) k_rec_grad_a(RecParams p) {
 template <int D>
 __global__ void __launch_bounds__(kT) k_rec_grad_b(RecParams p) {
   constexpr int LD = Lay<D>::LD, NC = Lay<D>::NC;
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   float* sK = sm;
   float* sQ = sK + kC * LD;
   float* sO = sQ + kC * LD;
   float* sD = sO + kC * LD;      // Delta
   float* sY = sD + kC * LD;
-  float* sS = sY + kC * LD;      // [32][LD] slice of S0 or G_C
-  float* sL = sS + 32 * LD;      // [C][kLC]: DoD, then L
-  float* sA = sL + kC * kLC;     // [C][kLC]: dA, then DA
+  float* sL = sY + kC * LD;      // [C][kLC]: L; before that, with sA, two [32][LD] row blocks of S0 / G_C
+  float* sA = sL + kC * kLC;     // [C][kLC]: DA
   float* lg = sA + kC * kLC;
   float* be = lg + kC;
   float* al = be + kC;
   float* dlg = al + kC;          // [C]
   float* cs = dlg + kC;          // [8][C] column sums of Z per warp
+  static_assert(2 * 32 * Lay<D>::LD <= 2 * kC * kLC, "row blocks fit the C x C buffers");
   const int ch = blockIdx.x / p.H, h = blockIdx.x % p.H;
   const int64_t row0 = p.chunk_info[2 * ch];
   const int rows = p.chunk_info[2 * ch + 1];
   const size_t blk = (size_t)ch * p.H + h;
   const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
-  load_rows<D>(sK, p.k, row0, rows, p.H, h);
-  load_rows<D>(sQ, p.q, row0, rows, p.H, h);
-  load_rows<D>(sO, p.dout, row0, rows, p.H, h);
-  load_blk<D>(sD, p.Db + blk * kC * D);
-  load_blk<D>(sY, p.Yb + blk * kC * D);
+  const float* S0g = p.S0 + blk * D * D;
+  const float* GCg = p.Gb + blk * D * D;
+  float* slot[2] = {sL, sL + 32 * LD};
+  // row blocks 0 .. NC-1 of S0, then of G_C; block i in slot i % 2
+  auto issue = [&](int i) {
+    if (i < 2 * NC) cp_blk<D, 32>(slot[i & 1], (i < NC ? S0g : GCg) + (size_t)32 * (i % NC) * D);
+    cp_commit();
+  };
+  cp_rows<D>(sK, p.k, row0, rows, p.H, h);
+  cp_rows<D>(sQ, p.q, row0, rows, p.H, h);
+  cp_rows<D>(sO, p.dout, row0, rows, p.H, h);
+  cp_blk<D>(sD, p.Db + blk * kC * D);
+  cp_blk<D>(sY, p.Yb + blk * kC * D);
+  cp_commit();
+  issue(0);
   load_gates(lg, be, al, p.alpha, p.beta, row0, rows, p.H, h);
   const float lgC = lg[kC - 1];
+  // dq = diag(g) dO S0 + L K;  dk = diag(g_C/g) Delta G_C - diag(g beta) Y S0 + L^T Q + (DA + DA^T) K
+  float gq[8][NC], gk[8][NC], t1[8][NC];
+  zero(gq);
+  zero(t1);
+#pragma unroll 1
+  for (int i = 0; i < 2 * NC; i++) {
+    issue(i + 1);
+    cp_wait_group<1>();
+    __syncthreads();
+    const float* blkp = slot[i & 1];
+    const int js = i % NC;
+    if (i < NC) {
+      mm_nn(gq, sO + 32 * js, LD, blkp, LD, 32, ty * 8, tx);
+      mm_nn(t1, sY + 32 * js, LD, blkp, LD, 32, ty * 8, tx);
+    } else {
+      mm_nn(t1, sD + 32 * js, LD, blkp, LD, 32, ty * 8, tx);
+    }
+    if (i == NC - 1) {   // Y S0 complete: fold it in, then collect Delta G_C in t1
+#pragma unroll
+      for (int r = 0; r < 8; r++) {
+        const int t = ty * 8 + r;
+        const float g = expf(lg[t]);
+#pragma unroll
+        for (int c = 0; c < NC; c++) {
+          gq[r][c] *= g;
+          gk[r][c] = -g * be[t] * t1[r][c];
+          t1[r][c] = 0.f;
+        }
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 8; r++) {
+    const float rc = expf(lgC - lg[ty * 8 + r]);
+#pragma unroll
+    for (int c = 0; c < NC; c++) gk[r][c] = fmaf(rc, t1[r][c], gk[r][c]);
+  }
   {
     float dod[8][2], yd[8][2], qk[8][2], kk[8][2];
     gram<D>(dod, sO, sD);
@@ -728,55 +922,10 @@ __global__ void __launch_bounds__(kT) k_rec_grad_b(RecParams p) {
     for (int w = 0; w < kT / 32; w++) c += cs[w * kC + threadIdx.x];
     dlg[threadIdx.x] -= c;
   }
-  // dq = diag(g) dO S0 + L K;  dk = diag(g_C/g) Delta G_C - diag(g beta) Y S0 + L^T Q + (DA + DA^T) K
-  float gq[8][NC], gk[8][NC];
-  zero(gq);
-  zero(gk);
-  const float* S0g = p.S0 + blk * D * D;
-  const float* GCg = p.Gb + blk * D * D;
-  {
-    float ys[8][NC];
-    zero(ys);
-#pragma unroll 1
-    for (int js = 0; js < NC; js++) {
-      __syncthreads();
-      load_state_rows<D>(sS, S0g, 32 * js);
-      __syncthreads();
-      mm(gq, sO + 32 * js, LD, 1, sS, LD, 1, 32, ty * 8, tx);
-      mm(ys, sY + 32 * js, LD, 1, sS, LD, 1, 32, ty * 8, tx);
-    }
-#pragma unroll
-    for (int r = 0; r < 8; r++) {
-      const int t = ty * 8 + r;
-      const float g = expf(lg[t]);
-#pragma unroll
-      for (int c = 0; c < NC; c++) {
-        gq[r][c] *= g;
-        gk[r][c] = -g * be[t] * ys[r][c];
-      }
-    }
-  }
-  {
-    float dg[8][NC];
-    zero(dg);
-#pragma unroll 1
-    for (int js = 0; js < NC; js++) {
-      __syncthreads();
-      load_state_rows<D>(sS, GCg, 32 * js);
-      __syncthreads();
-      mm(dg, sD + 32 * js, LD, 1, sS, LD, 1, 32, ty * 8, tx);
-    }
-#pragma unroll
-    for (int r = 0; r < 8; r++) {
-      const float rc = expf(lgC - lg[ty * 8 + r]);
-#pragma unroll
-      for (int c = 0; c < NC; c++) gk[r][c] = fmaf(rc, dg[r][c], gk[r][c]);
-    }
-  }
-  mm(gq, sL, kLC, 1, sK, LD, 1, kC, ty * 8, tx);
-  mm(gk, sL, 1, kLC, sQ, LD, 1, kC, ty * 8, tx);
-  mm(gk, sA, kLC, 1, sK, LD, 1, kC, ty * 8, tx);
-  mm(gk, sA, 1, kLC, sK, LD, 1, kC, ty * 8, tx);
+  mm_nn(gq, sL, kLC, sK, LD, kC, ty * 8, tx);
+  mm_tn(gk, sL, kLC, sQ, LD, kC, ty * 8, tx);
+  mm_nn(gk, sA, kLC, sK, LD, kC, ty * 8, tx);
+  mm_tn(gk, sA, kLC, sK, LD, kC, ty * 8, tx);
 #pragma unroll
   for (int r = 0; r < 8; r++) {
     const int t = ty * 8 + r;
@@ -787,41 +936,53 @@ __global__ void __launch_bounds__(kT) k_rec_grad_b(RecParams p) {
         p.dk[((row0 + t) * p.H + h) * D + tx + 32 * c] = gk[r][c];
       }
   }
+  // dalpha_j = (sum_{t >= j} dlg_t) / alpha_j: two warps, suffix sums by shuffles
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < kC) {
+    const int t = threadIdx.x;
     const float* Sg = p.Sc + blk * 3 * kC;
-    float rsum = 0.f;
-    for (int t = 0; t < kC; t++) {
-      dlg[t] += Sg[t] - Sg[kC + t];
-      rsum += Sg[kC + t];
+    const float r = Sg[kC + t];
+    float x = dlg[t] + Sg[t] - r;
+    const float rsum = warp_sum(r);
+    cs[t] = rsum;   // the column-sum scratch is free: per-warp totals of r
+    // suffix sum within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, x, o);
+      if ((t & 31) + o < 32) x += y;
     }
-    dlg[kC - 1] += rsum + expf(lgC) * Sg[2 * kC];
-    float acc = 0.f;
-    for (int t = kC - 1; t >= 0; t--) {
-      acc += dlg[t];
-      if (t < rows) p.dalpha[(row0 + t) * p.H + h] = acc / al[t];
-    }
+    dlg[t] = x;
+  }
+  __syncthreads();
+  if (threadIdx.x < kC) {
+    const int t = threadIdx.x;
+    // the last row's extra terms (all r, and g_C <G_C, S0>) reach every row's suffix sum,
+    // and rows of the first warp also take the second warp's total
+    const float extra = cs[0] + cs[32] + expf(lgC) * p.Sc[blk * 3 * kC + 2 * kC];
+    const float x = dlg[t] + extra + (t < 32 ? dlg[32] : 0.f);
+    if (t < rows) p.dalpha[(row0 + t) * p.H + h] = x / al[t];
   }
 }
 
 template <int D>
 constexpr size_t smem_prep() { return (size_t)(2 * kC * Lay<D>::LD + 2 * kC * kLC + 3 * kC) * 4; }
 template <int D>
-constexpr size_t smem_scan_fwd() { return (size_t)(2 * kC * Lay<D>::LD + 32 * Lay<D>::LD + kC * 33 + kC) * 4; }
+constexpr size_t smem_scan_fwd() { return (size_t)(2 * kC * Lay<D>::LD + 32 * Lay<D>::LD + kC * kL32 + kC) * 4; }
 template <int D>
-constexpr size_t smem_out() { return (size_t)(3 * kC * Lay<D>::LD + 32 * Lay<D>::LD + kC * kLC + kC) * 4; }
+constexpr size_t smem_out() { return (size_t)(2 * kC * Lay<D>::LD + 32 * Lay<D>::LD + kC * kLC + kC) * 4; }
 template <int D>
-constexpr size_t smem_prep_bwd() { return (size_t)(3 * kC * Lay<D>::LD + kC * kLC + kC) * 4; }
+constexpr size_t smem_prep_bwd() { return (size_t)(2 * kC * Lay<D>::LD + kC * kLC + kC) * 4; }
 template <int D>
 constexpr size_t smem_scan_bwd() {
-  return (size_t)(3 * kC * Lay<D>::LD + 32 * Lay<D>::LD + 32 * kLC + kC * 33 + kC) * 4;
+  return (size_t)(2 * (kC * Lay<D>::LD + kC) + 2 * kC * Lay<D>::LD + 32 * Lay<D>::LD + 32 * kLC + kC * kL32) * 4;
 }
 template <int D>
-constexpr size_t smem_grad_a() { return (size_t)(5 * kC * Lay<D>::LD + 32 * Lay<D>::LD + kC * kLC + 3 * kC) * 4; }
+constexpr size_t smem_grad_a() { return (size_t)(5 * kC * Lay<D>::LD + 64 * Lay<D>::LD + kC * kLC + 3 * kC) * 4; }
 template <int D>
 constexpr size_t smem_grad_b() {
-  return (size_t)(5 * kC * Lay<D>::LD + 32 * Lay<D>::LD + 2 * kC * kLC + 4 * kC + (kT / 32) * kC) * 4;
+  return (size_t)(5 * kC * Lay<D>::LD + 2 * kC * kLC + 4 * kC + (kT / 32) * kC) * 4;
 }
+static_assert(smem_grad_b<128>() <= 232448 && smem_grad_a<128>() <= 232448, "shared memory per CTA");
 
 }  // namespace
 }  // namespace octo
