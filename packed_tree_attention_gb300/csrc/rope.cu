@@ -55,69 +55,89 @@ __device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162
 __device__ __forceinline__ void st(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
-// One block per row: the row's d/2 (cos, sin) pairs once, then every head.  sgn = -1 turns
-// the other way (the inverse rotation, for gradients).  Each thread takes 4 consecutive
-// pairs (8- or 16-byte loads from both halves) when d/2 is a multiple of 4 and x is
-// 16-byte aligned.
+// Four rows per block: the rows' d/2 (cos, sin) pairs once (one thread per pair), then
+// every head of the rows.  sgn = -1 turns the other way (the inverse rotation, for
+// gradients).  When d/2 is a multiple of the 16-byte vector width and x is 16-byte aligned,
+// each thread takes a 16-byte vector from both halves (8 bf16 or 4 fp32 pairs).
+constexpr int kRopeRows = 4;
+
 template <typename T>
-struct Vec4;
+struct Vec16;
 template <>
-struct Vec4<float> {
-  using type = float4;
-  __device__ static void unpack(const float4& v, float (&f)[4]) { f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w; }
-  __device__ static float4 pack(const float (&f)[4]) { return make_float4(f[0], f[1], f[2], f[3]); }
+struct Vec16<float> {
+  static constexpr int W = 4;
+  __device__ static void unpack(const uint4& v, float (&f)[4]) {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y); f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+  __device__ static uint4 pack(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
 };
 template <>
-struct Vec4<__nv_bfloat16> {
-  using type = uint2;
-  __device__ static void unpack(const uint2& v, float (&f)[4]) {
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+struct Vec16<__nv_bfloat16> {
+  static constexpr int W = 8;
+  __device__ static void unpack(const uint4& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      f[2 * i] = a.x;
+      f[2 * i + 1] = a.y;
+    }
   }
-  __device__ static uint2 pack(const float (&f)[4]) {
-    const __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]), b = __floats2bfloat162_rn(f[2], f[3]);
-    return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  __device__ static uint4 pack(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const __nv_bfloat162 a = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&a);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
   }
 };
 
 template <typename T>
-__global__ void k_rope_rows(T* __restrict__ x, const int32_t* __restrict__ row_pos, int32_t H, RopeFreq f,
-                            float sgn, bool vec) {
-  __shared__ float cs[64][2];
-  const int64_t row = blockIdx.x;
+__global__ void __launch_bounds__(256) k_rope_rows(T* __restrict__ x, const int32_t* __restrict__ row_pos,
+                                                   int64_t n_rows, int32_t H, RopeFreq f, float sgn, bool vec) {
+  __shared__ float cs[kRopeRows][64][2];
+  const int64_t row0 = (int64_t)blockIdx.x * kRopeRows;
   const int32_t half = f.half, d = 2 * half;
-  if (threadIdx.x < half) rope_cs(row_pos[row], f.inv[threadIdx.x], cs[threadIdx.x][0], cs[threadIdx.x][1]);
+  const int nr = (int)min((int64_t)kRopeRows, n_rows - row0);
+  {
+    const int r = threadIdx.x / 64, i = threadIdx.x % 64;
+    if (r < nr && i < half) rope_cs(row_pos[row0 + r], f.inv[i], cs[r][i][0], cs[r][i][1]);
+  }
   __syncthreads();
-  T* xr = x + row * H * d;
   if (vec) {
-    using V = typename Vec4<T>::type;
-    const int32_t q4 = half / 4;
-    for (int32_t e = threadIdx.x; e < H * q4; e += blockDim.x) {
-      const int32_t h = e / q4, i0 = (e % q4) * 4;
-      V* pa = reinterpret_cast<V*>(xr + (size_t)h * d + i0);
-      V* pb = reinterpret_cast<V*>(xr + (size_t)h * d + i0 + half);
-      float a[4], b[4], ya[4], yb[4];
-      Vec4<T>::unpack(*pa, a);
-      Vec4<T>::unpack(*pb, b);
+    constexpr int W = Vec16<T>::W;
+    const int32_t qv = half / W;        // vectors per half head
+    const int32_t per_row = H * qv;
+    for (int32_t e = threadIdx.x; e < nr * per_row; e += blockDim.x) {
+      const int r = e / per_row, h = (e % per_row) / qv, i0 = (e % qv) * W;
+      T* xr = x + (row0 + r) * H * d + (size_t)h * d;
+      uint4* pa = reinterpret_cast<uint4*>(xr + i0);
+      uint4* pb = reinterpret_cast<uint4*>(xr + i0 + half);
+      float a[W], b[W], ya[W], yb[W];
+      Vec16<T>::unpack(*pa, a);
+      Vec16<T>::unpack(*pb, b);
 #pragma unroll
-      for (int t = 0; t < 4; t++) {
-        const float c = cs[i0 + t][0], s = sgn * cs[i0 + t][1];
-        ya[t] = a[t] * c - b[t] * s;
-        yb[t] = b[t] * c + a[t] * s;
+      for (int t = 0; t < W; t++) {
+        const float c = cs[r][i0 + t][0], sn = sgn * cs[r][i0 + t][1];
+        ya[t] = a[t] * c - b[t] * sn;
+        yb[t] = b[t] * c + a[t] * sn;
       }
-      *pa = Vec4<T>::pack(ya);
-      *pb = Vec4<T>::pack(yb);
+      *pa = Vec16<T>::pack(ya);
+      *pb = Vec16<T>::pack(yb);
     }
     return;
   }
-  for (int32_t e = threadIdx.x; e < H * half; e += blockDim.x) {
-    const int32_t h = e / half, i = e % half;
-    T* p = xr + (size_t)h * d + i;
+  for (int32_t e = threadIdx.x; e < nr * H * half; e += blockDim.x) {
+    const int r = e / (H * half), h = (e % (H * half)) / half, i = e % half;
+    T* p = x + (row0 + r) * H * d + (size_t)h * d + i;
     const float a = ld(p), b = ld(p + half);
-    const float c = cs[i][0], s = sgn * cs[i][1];
-    st(p, a * c - b * s);
-    st(p + half, b * c + a * s);
+    const float c = cs[r][i][0], sn = sgn * cs[r][i][1];
+    st(p, a * c - b * sn);
+    st(p + half, b * c + a * sn);
   }
 }
 
@@ -198,12 +218,15 @@ int octo_rope_rows(octo_plan_t plan, int32_t n_heads, void* x, int32_t dtype, fl
   cudaStream_t s = (cudaStream_t)stream;
   plan->last_stream = s;
   const float sgn = inverse ? -1.f : 1.f;
-  const bool vec = (f.half % 4) == 0 && ((uintptr_t)x % 16) == 0;
-  if (dtype == OCTO_DTYPE_F32)
-    octo::k_rope_rows<float><<<(unsigned)N, 256, 0, s>>>((float*)x, plan->row_pos, n_heads, f, sgn, vec);
-  else
-    octo::k_rope_rows<__nv_bfloat16><<<(unsigned)N, 256, 0, s>>>((__nv_bfloat16*)x, plan->row_pos, n_heads, f, sgn,
-                                                                 vec);
+  const unsigned grid = (unsigned)((N + octo::kRopeRows - 1) / octo::kRopeRows);
+  if (dtype == OCTO_DTYPE_F32) {
+    const bool vec = (f.half % 4) == 0 && ((uintptr_t)x % 16) == 0;
+    octo::k_rope_rows<float><<<grid, 256, 0, s>>>((float*)x, plan->row_pos, N, n_heads, f, sgn, vec);
+  } else {
+    const bool vec = (f.half % 8) == 0 && ((uintptr_t)x % 16) == 0;
+    octo::k_rope_rows<__nv_bfloat16><<<grid, 256, 0, s>>>((__nv_bfloat16*)x, plan->row_pos, N, n_heads, f, sgn,
+                                                          vec);
+  }
   octo::count_launch();
   return octo::cuda_status(cudaGetLastError());
 }
