@@ -383,14 +383,10 @@ __global__ void __launch_bounds__(kDkThreads, 1)
           // S'^T already holds S - LSE / scale
           mul2(a0, a1, __uint_as_float(xs[ii]), __uint_as_float(xs[ii + 1]), p.scale_log2, p.scale_log2);
           mul2(a2, a3, __uint_as_float(xs[ii + 2]), __uint_as_float(xs[ii + 3]), p.scale_log2, p.scale_log2);
-          // MUFU for 3 of every 4 pairs, the FMA-pipe polynomial for the 4th
-          if ((i & 7) == 4) {
-            a2 = ex2_poly(a2);
-            a3 = ex2_poly(a3);
-          } else {
-            a2 = ex2(a2);
-            a3 = ex2(a3);
-          }
+          // every exponential on MUFU: here the softmax warps' issue slots, shared with the
+          // MMA issuers, are scarcer than MUFU throughput (unlike the forward)
+          a2 = ex2(a2);
+          a3 = ex2(a3);
           a0 = ex2(a0);
           a1 = ex2(a1);
           if constexpr (decltype(masked)::value) {
@@ -750,14 +746,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           float a0, a1, a2, a3;
           fma2(a0, a1, __uint_as_float(xs[ii]), __uint_as_float(xs[ii + 1]), p.scale_log2, -lse2);
           fma2(a2, a3, __uint_as_float(xs[ii + 2]), __uint_as_float(xs[ii + 3]), p.scale_log2, -lse2);
-          // MUFU for 3 of every 4 pairs, the FMA-pipe polynomial for the 4th
-          if ((i & 7) == 4) {
-            a2 = ex2_poly(a2);
-            a3 = ex2_poly(a3);
-          } else {
-            a2 = ex2(a2);
-            a3 = ex2(a3);
-          }
+          // every exponential on MUFU: here the softmax warps' issue slots, shared with the
+          // MMA issuers, are scarcer than MUFU throughput (unlike the forward)
+          a2 = ex2(a2);
+          a3 = ex2(a3);
           a0 = ex2(a0);
           a1 = ex2(a1);
           if constexpr (decltype(masked)::value) {

@@ -282,21 +282,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         need = true;
       }
       const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-      // p = 2^(s * scale_log2 - msub): MUFU for 3 of every 4 pairs, the FMA-pipe
-      // polynomial for the 4th; eight running partial sums
+      // p = 2^(s * scale_log2 - msub), every exponential on MUFU (its throughput has room
+      // here; the issue slots the softmax warps share with the MMA issuers do not);
+      // eight running partial sums
       uint32_t pk[32];
       float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < 32; i++) {
         float a, c;
         fma2(a, c, x[2 * i], x[2 * i + 1], p.scale_log2, -msub);
-        if ((i & 3) == 3) {
-          a = ex2_poly(a);
-          c = ex2_poly(c);
-        } else {
-          a = ex2(a);
-          c = ex2(c);
-        }
+        a = ex2(a);
+        c = ex2(c);
         add2(ps[2 * (i & 3)], ps[2 * (i & 3) + 1], ps[2 * (i & 3)], ps[2 * (i & 3) + 1], a, c);
         pk[i] = pack_bf16(a, c);
       }

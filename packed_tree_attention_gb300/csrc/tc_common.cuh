@@ -215,21 +215,6 @@ __device__ __forceinline__ float ex2(float x) {
 
 // 2^x on the FMA and integer pipes, to take part of the exponentials off the MUFU pipe.
 // x = j + f with j = round(x) found by adding and subtracting 1.5 * 2^23, f in [-1/2, 1/2];
-// 2^f from a degree-3 polynomial whose coefficients were fitted for least maximum relative
-// error on [-1/2, 1/2] (7.6e-5, far below the 2^-8 of the bf16 probabilities it feeds);
-// j is added to the exponent field.  x is clamped below at -126 (the result is then ~1e-38,
-// i.e. zero for a probability); valid up to x = +127.
-__device__ __forceinline__ float ex2_poly(float x) {
-  x = fmaxf(x, -126.f);
-  const float t = x + 12582912.f;
-  const int j = __float_as_int(t) - 0x4B400000;
-  const float f = x - (t - 12582912.f);
-  float p = fmaf(f, 0.055170797f, 0.24260911f);
-  p = fmaf(f, p, 0.69326097f);
-  p = fmaf(f, p, 0.9999282f);
-  return __int_as_float(__float_as_int(p) + (j << 23));
-}
-
 // packed pairs of fp32 (sm_100 f32x2 instructions)
 __device__ __forceinline__ uint64_t f2pack(float a, float b) {
   uint64_t r;

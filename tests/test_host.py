@@ -137,35 +137,6 @@ def test_append_all_or_nothing(lib, oracle_mod):
 
 
 
-def test_exp2_polynomial_error_bound():
-    """The kernels take part of their exponentials off the MUFU pipe with a polynomial:
-    round-to-nearest split x = j + f (|f| <= 1/2) by the 1.5 * 2^23 trick, degree-3
-    polynomial for 2^f, j added to the exponent field.  This replays those fp32 steps
-    (constants read from the source) and checks the relative error against 2^x, which
-    must stay far below the 2^-8 resolution of the bf16 probabilities it feeds."""
-    import os
-    import re
-    src = open(os.path.join(os.path.dirname(__file__), "..", "packed_tree_attention_gb300", "csrc",
-                            "tc_common.cuh")).read()
-    body = src[src.index("float ex2_poly"):]
-    body = body[:body.index("}")]
-    c = [float(v) for v in re.findall(r"([0-9]\.[0-9]+)f", body)]
-    c3, c2, c1, c0 = c[-4:]
-    x = np.linspace(-126, 8, 400001).astype(np.float32)
-    x = np.concatenate([x, np.float32([-0.5, 0.5, 0.0, 7.999, -125.9])])
-    t = x + np.float32(12582912.0)
-    j = t.view(np.int32) - np.int32(0x4B400000)
-    f = x - (t - np.float32(12582912.0))
-    assert np.all(np.abs(f) <= 0.5)
-    p = np.float32(c3) * f + np.float32(c2)
-    p = p * f + np.float32(c1)
-    p = p * f + np.float32(c0)
-    r = (p.view(np.int32) + (j << 23)).view(np.float32).astype(np.float64)
-    ref = np.exp2(x.astype(np.float64))
-    ok = x > -120          # near the clamp the result is a denormal-range zero for a probability
-    assert np.max(np.abs(r[ok] / ref[ok] - 1)) < 1e-4
-
-
 @pytest.mark.parametrize("seed", range(8))
 def test_pool_query_matches_oracle(lib, oracle_mod, seed):
     """octo_pool_query: every segment's refcount and page count and every page's owner
