@@ -213,8 +213,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 2^x on the FMA and integer pipes, to take part of the exponentials off the MUFU pipe.
-// x = j + f with j = round(x) found by adding and subtracting 1.5 * 2^23, f in [-1/2, 1/2];
 // packed pairs of fp32 (sm_100 f32x2 instructions)
 __device__ __forceinline__ uint64_t f2pack(float a, float b) {
   uint64_t r;
