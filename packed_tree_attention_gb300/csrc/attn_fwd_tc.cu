@@ -17,8 +17,9 @@
 //   warp 2      TMEM allocator (512 columns: O_0, O_1, and two S buffers per head)
 //   warps 4-7   softmax of head 0, warps 8-11 softmax of head 1: one row per thread,
 //               S read with tcgen05.ld, mask from the entry rectangle, online softmax
-//               in the log2 domain with lazy rescaling (O is rescaled in TMEM only when
-//               the running max grows by more than 2^8), P written back to TMEM as bf16
+//               in the log2 domain with lazy rescaling (no maximum per entry: O is
+//               rescaled in TMEM only when an entry's probabilities relative to the
+//               running max sum past 2^16), P written back to TMEM as bf16
 //               over the S it came from; P V takes its A operand from TMEM
 // S (and the P that replaces it) is double-buffered per head: the MMA issuer runs S two
 // entries ahead, so a softmax warpgroup starts entry j+1 while the tensor core still runs
@@ -270,33 +271,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 64; i++)
           if (i < lo || i >= hi) x[i] = -INFINITY;
       }
-      const float mc = max64(x) * p.scale_log2;
       bool need = false;
       float factor = 1.f;
-      if (j == 0) {
-        m_used = mc;
-      } else if (mc > m_used + 8.f) {
-        factor = ex2(m_used - mc);
-        l *= factor;
-        m_used = mc;
-        need = true;
-      }
-      const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-      // p = 2^(s * scale_log2 - msub), every exponential on MUFU (its throughput has room
-      // here; the issue slots the softmax warps share with the MMA issuers do not);
-      // eight running partial sums
+      // nothing visible to this row yet: start from the entry's exact maximum
+      if (m_used == -INFINITY) m_used = max64(x) * p.scale_log2;
+      float msub = (m_used == -INFINITY) ? 0.f : m_used;
+      // p = 2^(s * scale_log2 - msub), every exponential on MUFU; eight running partial sums
       uint32_t pk[32];
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      auto pass = [&]() -> float {
+        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 32; i++) {
-        float a, c;
-        fma2(a, c, x[2 * i], x[2 * i + 1], p.scale_log2, -msub);
-        a = ex2(a);
-        c = ex2(c);
-        add2(ps[2 * (i & 3)], ps[2 * (i & 3) + 1], ps[2 * (i & 3)], ps[2 * (i & 3) + 1], a, c);
-        pk[i] = pack_bf16(a, c);
+        for (int i = 0; i < 32; i++) {
+          float a, c;
+          fma2(a, c, x[2 * i], x[2 * i + 1], p.scale_log2, -msub);
+          a = ex2(a);
+          c = ex2(c);
+          add2(ps[2 * (i & 3)], ps[2 * (i & 3) + 1], ps[2 * (i & 3)], ps[2 * (i & 3) + 1], a, c);
+          pk[i] = pack_bf16(a, c);
+        }
+        return ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      };
+      // Lazy rescaling without a maximum per entry: the running maximum stays while every
+      // p of the entry is at most 2^16, which holds whenever their sum is; an entry whose
+      // sum is larger (or not finite) is redone from its exact maximum.
+      float le = pass();
+      const bool over = !(le <= 65536.f);
+      if (__any_sync(0xffffffffu, over)) {
+        if (over) {
+          const float mc = max64(x) * p.scale_log2;
+          factor = ex2(m_used - mc);
+          l *= factor;
+          m_used = mc;
+          msub = mc;
+          need = true;
+        }
+        le = pass();
       }
-      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      l += le;
       if (__any_sync(0xffffffffu, need)) {
         // O must hold every P V so far before it is rescaled
         if (!(ok = warp_wait(&B->o_done[hh][(j - 1) & 1], ((j - 1) >> 1) & 1, B, p.status))) break;
