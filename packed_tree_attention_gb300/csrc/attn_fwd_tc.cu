@@ -11,9 +11,10 @@
 //               entry's page through a 5-stage ring (a page load takes ~1.3 us, several
 //               entries' worth of tensor work, so it has to start well ahead)
 //   warps 1, 3  MMA issuers, one thread each, one per head: S_h = Q_h K^T (M128 N64
-//               K16 x8) and O_h += P_h V (M128 N128 K16 x4), accumulators in TMEM.  With
-//               64-key pages the MMAs are small, and issuing them (not executing them)
-//               is what a single issuer is limited by; two issue streams double that rate
+//               K16 x8) and O_h += P_h V (M128 N128 K16 x4), accumulators in TMEM.  Each
+//               head's chain S -> softmax -> P V waits on its own warpgroup; one thread
+//               issuing both heads' MMAs in turn made each wait behind the other (45%
+//               slower, measured)
 //   warp 2      TMEM allocator (512 columns: O_0, O_1, and two S buffers per head)
 //   warps 4-7   softmax of head 0, warps 8-11 softmax of head 1: one row per thread,
 //               S read with tcgen05.ld, mask from the entry rectangle, online softmax
