@@ -233,7 +233,9 @@ int octo_decode_plan(octo_pool_t pool, const octo_cursor_t* cursors, int32_t n, 
  * at the end of the cursor's list.  When no cursor opens a page this is one kernel that
  * updates the plan in place; otherwise the entries, the CSC view, page offsets and touched
  * pages are rebuilt by device kernels from the old ones, and the split-KV runs and launch
- * orders from host copies kept with the plan.  It never waits for the device; the work is
+ * orders from host copies kept with the plan; the arrays replaced are kept with the plan
+ * and written by the next such advance, which allocates only when they are too small.
+ * It never waits for the device; the work is
  * queued on `stream`, ordered after the work queued on the stream that last used the plan.
  * OCTO_ESTATE, with the plan unchanged, when a cursor is not exactly one token longer, was
  * freed, has a mount at or after the point of its new token (its context then grows by

@@ -654,6 +654,7 @@ int finish_plan(octo_plan_s* pl, cudaStream_t s) {
   int32_t* d_cnt = pl->d_cnt;
   int32_t* d_scratch = pl->d_scratch;
   OCTO_RET(dalloc(pl, &pl->csc_perm, n_entries, s));
+  pl->csc_cap = (size_t)n_entries;
   // ---- CSC ----
   OCTO_RET(cuda_status(cudaMemsetAsync(d_cnt, 0, (size_t)pl->num_pages * 4, s)));
   if (n_entries > 0) {
@@ -707,6 +708,7 @@ int finish_plan(octo_plan_s* pl, cudaStream_t s) {
       if (!ttree.empty() && ttree[a] != ttree[b]) return ttree[a] < ttree[b];
       return toff[a + 1] - toff[a] > toff[b + 1] - toff[b];
     });
+    if (is_decode) pl->h_tord = tord;   // re-sorted incrementally by each advance
     const bool any_touched = pl->info.n_touched_pages > 0;
     // dK/dV work units: consecutive own pages of each segment, two at a time, among the
     // touched pages; a touched page without a touched partner runs alone
@@ -896,6 +898,8 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
   OCTO_TRY(dalloc(pl, &d_scratch, 8, s));
   OCTO_TRY(dalloc(pl, &pl->page_off, (size_t)pl->num_pages + 1, s));
   OCTO_TRY(dalloc(pl, &pl->touched, (size_t)pl->num_pages, s));
+  pl->poff_cap = (size_t)pl->num_pages + 1;
+  pl->touched_cap = (size_t)pl->num_pages;
   d_status = d_scratch;  // [0] status, [1] max tile entries, [2] max page entries, [3] touched, [4..5] pairs
   OCTO_TRY(cuda_status(cudaMemsetAsync(d_scratch, 0, 8 * sizeof(int32_t), s)));
   OCTO_TRY(cuda_status(cudaMemcpyAsync(d_segs, hseg.data(), hseg.size() * sizeof(DevSeg), cudaMemcpyHostToDevice, s)));
@@ -1069,6 +1073,7 @@ int compile_plan(octo_pool_s* pool, const int32_t* tile_segs_host, const int32_t
   pl->info.n_entries = n_entries;
   pl->info.max_tile_entries = hs[1];
   OCTO_TRY(dalloc(pl, &pl->entries, n_entries, s));
+  pl->entries_cap = (size_t)n_entries;
   if (n_tiles > 0) {
     k_fill<<<grid_t, 32 * wpb, 0, s>>>(w, pl->tile_seg, pl->tile_t0, pl->tile_rows, (int32_t)n_tiles, pl->tile_off,
                                        pl->entries, d_status);
@@ -1181,7 +1186,13 @@ int octo_decode_plan_advance(octo_plan_t pl, void* stream) {
   // split-KV runs of kSplitEntries entries per cursor: existing runs keep their first
   // entry (entries are only added at the end of a cursor's list); a cursor whose list was
   // a whole number of runs starts a new one on its fresh page
-  std::vector<int32_t> sp_tile, sp_e0, sp_e1, sp_first, cur0(n + 1, 0);
+  std::vector<int32_t>&sp_tile = pl->x_sp_tile, &sp_e0 = pl->x_sp_e0, &sp_e1 = pl->x_sp_e1,
+                      &sp_first = pl->x_sp_first, &cur0 = pl->x_cur0;
+  sp_tile.clear();
+  sp_e0.clear();
+  sp_e1.clear();
+  sp_first.clear();
+  cur0.assign(n + 1, 0);
   for (int32_t i = 0; i < n; i++) {
     cur0[i] = (int32_t)sp_tile.size();
     const int32_t old_runs = pl->h_cur0[i + 1] - pl->h_cur0[i];
@@ -1194,7 +1205,7 @@ int octo_decode_plan_advance(octo_plan_t pl, void* stream) {
   }
   const int32_t ns = (int32_t)sp_tile.size();
   cur0[n] = ns;
-  std::vector<int32_t> sp_order;
+  std::vector<int32_t>& sp_order = pl->x_sp_order;
   if (ns == pl->n_splits) {
     sp_order = pl->h_sp_order;   // same runs, same first pages: same launch order
   } else {
@@ -1203,10 +1214,25 @@ int octo_decode_plan_advance(octo_plan_t pl, void* stream) {
     std::stable_sort(sp_order.begin(), sp_order.end(),
                      [&](int32_t a, int32_t c) { return sp_first[a] < sp_first[c]; });
   }
-  std::vector<int32_t> tord(n);
-  for (int32_t t = 0; t < n; t++) tord[t] = t;
-  std::stable_sort(tord.begin(), tord.end(),
-                   [&](int32_t a, int32_t b) { return off[a + 1] - off[a] > off[b + 1] - off[b]; });
+  // tiles by entry count, most first, ties by cursor (the compile's stable sort): the
+  // previous order re-sorted by insertion, as only the cursors that opened a page moved
+  std::vector<int32_t>& tord = pl->h_tord;
+  if ((int32_t)tord.size() != n) {
+    tord.resize(n);
+    for (int32_t t = 0; t < n; t++) tord[t] = t;
+  }
+  {
+    auto before = [&](int32_t a, int32_t b) {
+      const int32_t ca = off[a + 1] - off[a], cb = off[b + 1] - off[b];
+      return ca > cb || (ca == cb && a < b);
+    };
+    for (int32_t i = 1; i < n; i++) {
+      const int32_t x = tord[i];
+      int32_t k = i;
+      for (; k > 0 && before(x, tord[k - 1]); k--) tord[k] = tord[k - 1];
+      tord[k] = x;
+    }
+  }
   // one upload: adv | tile_off | fresh pages | split cursor, first, end, order | first split
   // per cursor | tile order
   const size_t o_fp = 3 * (size_t)n + 1, o_st = o_fp + m, o_e0 = o_st + ns, o_e1 = o_e0 + ns,
@@ -1223,12 +1249,30 @@ int octo_decode_plan_advance(octo_plan_t pl, void* stream) {
   std::copy(tord.begin(), tord.end(), stage.begin() + o_to);
   const int32_t e_old = (int32_t)pl->info.n_entries, e_new = off[n];
   const int32_t t_old = pl->info.n_touched_pages;
+  // the arrays this advance writes: the ones the previous such advance replaced, when they
+  // are large enough (no allocation then), else new ones with some room to grow
   int32_t *buf = nullptr, *csc = nullptr, *poff = nullptr, *touched = nullptr;
   octo_entry* ent = nullptr;
+  size_t buf_cap = 0, ent_cap = 0, csc_cap = 0, poff_cap = 0, touched_cap = 0;
+  auto take = [&](auto*& spare, size_t& spare_cap, size_t need, auto*& out, size_t& out_cap) -> int {
+    if (spare && spare_cap >= need) {
+      out = spare;
+      out_cap = spare_cap;
+    } else {
+      if (spare) dfree(pl, spare, s);
+      out_cap = need + need / 8 + 256;
+      if (int st = dalloc(pl, &out, out_cap, s)) return st;
+    }
+    spare = nullptr;
+    spare_cap = 0;
+    return OCTO_OK;
+  };
   int st;
-  if ((st = dalloc(pl, &buf, total, s)) || (st = dalloc(pl, &ent, (size_t)e_new, s)) ||
-      (st = dalloc(pl, &csc, (size_t)e_new, s)) || (st = dalloc(pl, &poff, (size_t)pl->num_pages + 1, s)) ||
-      (st = dalloc(pl, &touched, (size_t)t_old + m, s)))
+  if ((st = take(pl->sp_buf, pl->sp_buf_cap, total, buf, buf_cap)) ||
+      (st = take(pl->sp_entries, pl->sp_entries_cap, (size_t)e_new, ent, ent_cap)) ||
+      (st = take(pl->sp_csc, pl->sp_csc_cap, (size_t)e_new, csc, csc_cap)) ||
+      (st = take(pl->sp_poff, pl->sp_poff_cap, (size_t)pl->num_pages + 1, poff, poff_cap)) ||
+      (st = take(pl->sp_touched, pl->sp_touched_cap, (size_t)t_old + m, touched, touched_cap)))
     return st;
   // pageable source: staged by the runtime before the call returns
   OCTO_CUDA(cudaMemcpyAsync(buf, stage.data(), total * 4, cudaMemcpyHostToDevice, s));
@@ -1244,17 +1288,33 @@ int octo_decode_plan_advance(octo_plan_t pl, void* stream) {
   k_touched_advance<<<(unsigned)((t_old + m + 255) / 256), 256, 0, s>>>(pl->touched, t_old, d_fp, m, touched);
   count_launch(4);
   OCTO_CUDA(cudaGetLastError());
-  // the replaced arrays go back in stream order (arrays that lived in the previous
-  // advance's buffer are not allocations of their own: dfree skips them)
-  for (void* p : {(void*)pl->entries, (void*)pl->csc_perm, (void*)pl->page_off, (void*)pl->touched,
-                  (void*)pl->tile_off, (void*)pl->split_tile, (void*)pl->split_e0, (void*)pl->split_e1,
-                  (void*)pl->split_order, (void*)pl->cur_split0, (void*)pl->tile_order, pl->adv_buf})
+  // the replaced small arrays of the plan's compile go back in stream order (the ones that
+  // lived in the previous advance's buffer are not allocations of their own: dfree skips
+  // them); the replaced entries, CSC, page offsets, touched pages and buffer become the
+  // next advance's spares, which it writes only after the work queued here
+  for (void* p : {(void*)pl->tile_off, (void*)pl->split_tile, (void*)pl->split_e0, (void*)pl->split_e1,
+                  (void*)pl->split_order, (void*)pl->cur_split0, (void*)pl->tile_order})
     if (p) dfree(pl, p, s);
+  pl->sp_buf = static_cast<int32_t*>(pl->adv_buf);
+  pl->sp_buf_cap = pl->buf_cap;
+  pl->sp_entries = pl->entries;
+  pl->sp_entries_cap = pl->entries_cap;
+  pl->sp_csc = pl->csc_perm;
+  pl->sp_csc_cap = pl->csc_cap;
+  pl->sp_poff = pl->page_off;
+  pl->sp_poff_cap = pl->poff_cap;
+  pl->sp_touched = pl->touched;
+  pl->sp_touched_cap = pl->touched_cap;
   pl->adv_buf = buf;
+  pl->buf_cap = buf_cap;
   pl->entries = ent;
+  pl->entries_cap = ent_cap;
   pl->csc_perm = csc;
+  pl->csc_cap = csc_cap;
   pl->page_off = poff;
+  pl->poff_cap = poff_cap;
   pl->touched = touched;
+  pl->touched_cap = touched_cap;
   pl->tile_off = d_off;
   pl->split_tile = buf + o_st;
   pl->split_e0 = buf + o_e0;
@@ -1264,12 +1324,12 @@ int octo_decode_plan_advance(octo_plan_t pl, void* stream) {
   pl->tile_order = buf + o_to;
   pl->n_splits = ns;
   pl->h_toff.assign(off, off + n + 1);
-  pl->h_sp_tile = std::move(sp_tile);
-  pl->h_sp_e0 = std::move(sp_e0);
-  pl->h_sp_e1 = std::move(sp_e1);
-  pl->h_sp_first = std::move(sp_first);
-  pl->h_sp_order = std::move(sp_order);
-  pl->h_cur0 = std::move(cur0);
+  pl->h_sp_tile.swap(sp_tile);
+  pl->h_sp_e0.swap(sp_e0);
+  pl->h_sp_e1.swap(sp_e1);
+  pl->h_sp_first.swap(sp_first);
+  pl->h_sp_order.swap(sp_order);
+  pl->h_cur0.swap(cur0);
   for (int32_t i = 0; i < n; i++) pl->cur_len[i] += 1;
   pl->info.n_entries = e_new;
   pl->info.max_tile_entries = mx;

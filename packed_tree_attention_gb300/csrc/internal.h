@@ -129,9 +129,19 @@ struct octo_plan_s {
   // advance by one token per cursor updates them without reading the device
   std::vector<int32_t> cur_seg, cur_len, h_toff;
   std::vector<int32_t> h_sp_tile, h_sp_e0, h_sp_e1, h_sp_first, h_sp_order, h_cur0;
+  // the advance's host-side counterparts: last time's split arrays (their storage is
+  // reused) and the decode plan's tile order, kept to re-sort it incrementally
+  std::vector<int32_t> x_sp_tile, x_sp_e0, x_sp_e1, x_sp_first, x_sp_order, x_cur0, h_tord;
   bool dup_cursors = false;          // a cursor listed twice (advance then refuses)
   std::vector<int32_t> h_stage;      // staging of the small arrays an advance uploads
   void* adv_buf = nullptr;           // device copy of the last advance's small arrays
+  // An advance that opens pages writes the entries, CSC, page offsets, touched pages and
+  // its small arrays into spare arrays and swaps them in; the arrays it replaced are the
+  // next such advance's spares (capacities in elements).
+  octo_entry* sp_entries = nullptr;
+  int32_t *sp_csc = nullptr, *sp_poff = nullptr, *sp_touched = nullptr, *sp_buf = nullptr;
+  size_t sp_entries_cap = 0, sp_csc_cap = 0, sp_poff_cap = 0, sp_touched_cap = 0, sp_buf_cap = 0;
+  size_t entries_cap = 0, csc_cap = 0, poff_cap = 0, touched_cap = 0, buf_cap = 0;   // current arrays
   cudaEvent_t order_ev = nullptr;    // orders an advance after work on another stream
   cudaStream_t last_stream = nullptr;  // stream of the last call that used the plan
 };
