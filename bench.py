@@ -620,9 +620,9 @@ FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 def recurrent_flops(n_chunks, H, D, C=64):
     """Executed FLOPs of the chunked gated delta rule (every chunk computed at full size):
     forward 3 C D^2 + 5 C^2 D + C^3 / 6 multiply-adds per (chunk, head), backward
-    9 C D^2 + 15 C^2 D."""
+    9 C D^2 + 14 C^2 D."""
     fwd = 2.0 * (3 * C * D * D + 5 * C * C * D + C ** 3 / 6) * n_chunks * H
-    bwd = 2.0 * (9 * C * D * D + 15 * C * C * D) * n_chunks * H
+    bwd = 2.0 * (9 * C * D * D + 14 * C * C * D) * n_chunks * H
     return fwd, bwd
 
 

@@ -121,10 +121,11 @@ __device__ __forceinline__ void cp_blk(float* dst, const float* __restrict__ src
   constexpr int Q = D / 4;
   for (int i = threadIdx.x; i < R * Q; i += kT) cp16(dst + (i / Q) * Lay<D>::LD + (i % Q) * 4, src + i * 4, true);
 }
-// columns [j0, j0 + 32) of a dense [C][D] block into dst [C][kL32]
-template <int D>
+// columns [j0, j0 + 32) of a dense [R][D] block into dst [R][kL32] (R = C, or all D rows
+// of a [D][D] state)
+template <int D, int R = kC>
 __device__ __forceinline__ void cp_blk32(float* dst, const float* __restrict__ src, int j0) {
-  for (int i = threadIdx.x; i < kC * 8; i += kT) cp16(dst + (i >> 3) * kL32 + (i & 7) * 4, src + (i >> 3) * D + j0 + (i & 7) * 4, true);
+  for (int i = threadIdx.x; i < R * 8; i += kT) cp16(dst + (i >> 3) * kL32 + (i & 7) * 4, src + (i >> 3) * D + j0 + (i & 7) * 4, true);
 }
 // a dense [C][C] block into dst [C][kLC]
 __device__ __forceinline__ void cp_cc(float* dst, const float* __restrict__ src) {
@@ -203,6 +204,97 @@ __device__ __forceinline__ void mm_tn(float (&acc)[R][NC], const float* A, int l
   }
 }
 
+// Two products that share one operand, which is then read from shared memory once for
+// both (the products are bound by shared-memory wavefronts, not by the FMA pipe):
+// acc1 += A1 B^T and acc2 += A2 B^T, as mm_nt
+template <int R, int NC>
+__device__ __forceinline__ void mm_nt2(float (&acc1)[R][NC], float (&acc2)[R][NC], const float* A1, const float* A2,
+                                       int lda, const float* B, int ldb, int K, int i0, int j0) {
+#pragma unroll 1
+  for (int k = 0; k < K; k += 4) {
+    float4 b[NC];
+#pragma unroll
+    for (int c = 0; c < NC; c++) b[c] = *reinterpret_cast<const float4*>(B + (j0 + 32 * c) * ldb + k);
+#pragma unroll
+    for (int u = 0; u < 2; u++) {
+      const float* A = u ? A2 : A1;
+      float(&acc)[R][NC] = u ? acc2 : acc1;
+#pragma unroll
+      for (int r = 0; r < R; r++) {
+        const float4 a = *reinterpret_cast<const float4*>(A + (i0 + r) * lda + k);
+#pragma unroll
+        for (int c = 0; c < NC; c++) {
+          acc[r][c] = fmaf(a.x, b[c].x, acc[r][c]);
+          acc[r][c] = fmaf(a.y, b[c].y, acc[r][c]);
+          acc[r][c] = fmaf(a.z, b[c].z, acc[r][c]);
+          acc[r][c] = fmaf(a.w, b[c].w, acc[r][c]);
+        }
+      }
+    }
+  }
+}
+
+// acc1 += A1 B and acc2 += A2 B, as mm_nn
+template <int R, int NC>
+__device__ __forceinline__ void mm_nn2(float (&acc1)[R][NC], float (&acc2)[R][NC], const float* A1, const float* A2,
+                                       int lda, const float* B, int ldb, int K, int i0, int j0) {
+#pragma unroll 1
+  for (int k = 0; k < K; k += 4) {
+    float4 a1[R], a2[R];
+#pragma unroll
+    for (int r = 0; r < R; r++) {
+      a1[r] = *reinterpret_cast<const float4*>(A1 + (i0 + r) * lda + k);
+      a2[r] = *reinterpret_cast<const float4*>(A2 + (i0 + r) * lda + k);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; kk++) {
+      float b[NC];
+#pragma unroll
+      for (int c = 0; c < NC; c++) b[c] = B[(k + kk) * ldb + j0 + 32 * c];
+#pragma unroll
+      for (int r = 0; r < R; r++) {
+        const float x1 = kk == 0 ? a1[r].x : kk == 1 ? a1[r].y : kk == 2 ? a1[r].z : a1[r].w;
+        const float x2 = kk == 0 ? a2[r].x : kk == 1 ? a2[r].y : kk == 2 ? a2[r].z : a2[r].w;
+#pragma unroll
+        for (int c = 0; c < NC; c++) {
+          acc1[r][c] = fmaf(x1, b[c], acc1[r][c]);
+          acc2[r][c] = fmaf(x2, b[c], acc2[r][c]);
+        }
+      }
+    }
+  }
+}
+
+// acc1 += A B1 and acc2 += A B2, as mm_nn
+template <int R, int NC>
+__device__ __forceinline__ void mm_nn_b2(float (&acc1)[R][NC], float (&acc2)[R][NC], const float* A, int lda,
+                                         const float* B1, const float* B2, int ldb, int K, int i0, int j0) {
+#pragma unroll 1
+  for (int k = 0; k < K; k += 4) {
+    float4 a[R];
+#pragma unroll
+    for (int r = 0; r < R; r++) a[r] = *reinterpret_cast<const float4*>(A + (i0 + r) * lda + k);
+#pragma unroll
+    for (int kk = 0; kk < 4; kk++) {
+      float b1[NC], b2[NC];
+#pragma unroll
+      for (int c = 0; c < NC; c++) {
+        b1[c] = B1[(k + kk) * ldb + j0 + 32 * c];
+        b2[c] = B2[(k + kk) * ldb + j0 + 32 * c];
+      }
+#pragma unroll
+      for (int r = 0; r < R; r++) {
+        const float x = kk == 0 ? a[r].x : kk == 1 ? a[r].y : kk == 2 ? a[r].z : a[r].w;
+#pragma unroll
+        for (int c = 0; c < NC; c++) {
+          acc1[r][c] = fmaf(x, b1[c], acc1[r][c]);
+          acc2[r][c] = fmaf(x, b2[c], acc2[r][c]);
+        }
+      }
+    }
+  }
+}
+
 template <int R, int NC>
 __device__ __forceinline__ void zero(float (&acc)[R][NC]) {
 #pragma unroll
@@ -241,6 +333,14 @@ template <int D>
 __device__ __forceinline__ void gram(float (&acc)[8][2], const float* X, const float* Y) {
   zero(acc);
   mm_nt(acc, X, Lay<D>::LD, Y, Lay<D>::LD, D, (threadIdx.x >> 5) * 8, threadIdx.x & 31);
+}
+// two of them with the same Y
+template <int D>
+__device__ __forceinline__ void gram2(float (&acc1)[8][2], float (&acc2)[8][2], const float* X1, const float* X2,
+                                      const float* Y) {
+  zero(acc1);
+  zero(acc2);
+  mm_nt2(acc1, acc2, X1, X2, Lay<D>::LD, Y, Lay<D>::LD, D, (threadIdx.x >> 5) * 8, threadIdx.x & 31);
 }
 
 // =====================================================================================
@@ -313,8 +413,7 @@ __global__ void __launch_bounds__(kT) k_rec_prep(RecParams p) {
   float w[8][NC], u[8][NC];
   zero(w);
   zero(u);
-  mm_nn(w, sMi, kLC, sK, LD, kC, ty * 8, tx);
-  mm_nn(u, sMi, kLC, sV, LD, kC, ty * 8, tx);
+  mm_nn_b2(w, u, sMi, kLC, sK, sV, LD, kC, ty * 8, tx);
   float* Wg = p.Wb + blk * kC * D;
   float* Ug = p.Ub + blk * kC * D;
 #pragma unroll
@@ -415,8 +514,8 @@ __global__ void __launch_bounds__(kT) k_rec_out(RecParams p) {
   extern __shared__ __align__(16) float sm[];
   float* sQ = sm;
   float* sKD = sQ + kC * LD;   // K, then Delta
-  float* sS = sKD + kC * LD;   // [32][LD] rows of S0
-  float* sB = sS + 32 * LD;    // [C][kLC]
+  float* sS = sKD + kC * LD;   // [D][kL32] a 32-column block of S0
+  float* sB = sS + D * kL32;   // [C][kLC]
   float* lg = sB + kC * kLC;
   const int ch = blockIdx.x / p.H, h = blockIdx.x % p.H;
   const int64_t row0 = p.chunk_info[2 * ch];
@@ -441,19 +540,24 @@ __global__ void __launch_bounds__(kT) k_rec_out(RecParams p) {
   }
   __syncthreads();
   cp_blk<D>(sKD, p.Db + blk * kC * D);
-  float out[8][NC];
   const float* S0g = p.S0 + blk * D * D;
-#pragma unroll
-  for (int js = 0; js < NC; js++) {
-    if (js) __syncthreads();
-    cp_blk<D, 32>(sS, S0g + (size_t)32 * js * D);
+  // Q S0^T by 32-column blocks of the contraction, every block adding to all of out
+  // (single-buffered: two CTAs share an SM)
+  float out[8][NC];
+  zero(out);
+#pragma unroll 1
+  for (int jd = 0; jd < NC; jd++) {
+    if (jd) __syncthreads();
+    cp_blk32<D, D>(sS, S0g, 32 * jd);
     cp_wait();
     __syncthreads();
-    float acc[8][1];
-    zero(acc);
-    mm_nt(acc, sQ, LD, sS, LD, D, ty * 8, tx);
+    mm_nt(out, sQ + 32 * jd, LD, sS, kL32, 32, ty * 8, tx);
+  }
 #pragma unroll
-    for (int r = 0; r < 8; r++) out[r][js] = acc[r][0] * expf(lg[ty * 8 + r]);
+  for (int r = 0; r < 8; r++) {
+    const float g = expf(lg[ty * 8 + r]);
+#pragma unroll
+    for (int c = 0; c < NC; c++) out[r][c] *= g;
   }
   mm_nn(out, sB, kLC, sKD, LD, kC, ty * 8, tx);
 #pragma unroll
@@ -634,9 +738,9 @@ __global__ void __launch_bounds__(kT) k_rec_grad_a(RecParams p) {
   float* sO = sQ + kC * LD;      // dO
   float* sX = sO + kC * LD;      // V, then X
   float* sY = sX + kC * LD;      // Gbar, then Y
-  float* sS = sY + kC * LD;      // [32][LD] rows of S0
-  float* sT = sS + 32 * LD;      // [32][LD] the same rows of G_C
-  float* sB = sT + 32 * LD;      // [C][kLC]: tril(G o Q K^T), then Minv, then A
+  float* sS = sY + kC * LD;      // [D][kL32] a 32-column block of S0
+  float* sT = sS + D * kL32;     // [D][kL32] the same columns of G_C
+  float* sB = sT + D * kL32;     // [C][kLC]: tril(G o Q K^T), then Minv, then A
   float* lg = sB + kC * kLC;
   float* be = lg + kC;
   float* al = be + kC;
@@ -652,9 +756,9 @@ __global__ void __launch_bounds__(kT) k_rec_grad_a(RecParams p) {
   cp_rows<D>(sO, p.dout, row0, rows, p.H, h);
   cp_rows<D>(sX, p.v, row0, rows, p.H, h);
   cp_commit();
-  cp_blk<D, 32>(sS, S0g);
+  cp_blk32<D, D>(sS, S0g, 0);
   cp_commit();
-  cp_blk<D, 32>(sT, GCg);
+  cp_blk32<D, D>(sT, GCg, 0);
   cp_commit();
   load_gates(lg, be, al, p.alpha, p.beta, row0, rows, p.H, h);
   cp_wait_group<2>();
@@ -675,45 +779,43 @@ __global__ void __launch_bounds__(kT) k_rec_grad_a(RecParams p) {
   for (int r = 0; r < 8; r++) pq[r] = pr[r] = pdb[r] = 0.f;
   const float* Dg = p.Db + blk * kC * D;
   const float lgC = lg[kC - 1];
-  // row block js of S0 in sS and of G_C in sT; block js + 1 of S0 is fetched while G_C's
-  // block js is used, and of G_C while S0's block js + 1 is used
-#pragma unroll
-  for (int js = 0; js < NC; js++) {
-    const int j = 32 * js + tx;
-    cp_wait_group<1>();   // S0 rows of block js
+  // K S0^T, Q S0^T and K G_C^T by 32-column blocks jd of the contraction (column block jd
+  // of S0 in sS, of G_C in sT); block jd + 1 of S0 is fetched while G_C's block jd is used,
+  // and of G_C while S0's block jd + 1 is used
+  float ks[8][NC], qs[8][NC], kg[8][NC];
+  zero(ks);
+  zero(qs);
+  zero(kg);
+#pragma unroll 1
+  for (int jd = 0; jd < NC; jd++) {
+    cp_wait_group<1>();   // S0 columns of block jd
     __syncthreads();
-    float ks[8][1], qs[8][1];
-    zero(ks);
-    zero(qs);
-    mm_nt(ks, sK, LD, sS, LD, D, ty * 8, tx);
-    mm_nt(qs, sQ, LD, sS, LD, D, ty * 8, tx);
-#pragma unroll
-    for (int r = 0; r < 8; r++) {
-      const int t = ty * 8 + r;
-      const float g = expf(lg[t]);
-      sX[t * LD + j] -= g * ks[r][0];
-      pq[r] = fmaf(sO[t * LD + j], g * qs[r][0], pq[r]);
-    }
-    cp_wait_group<0>();   // G_C rows of block js
+    mm_nt2(ks, qs, sK + 32 * jd, sQ + 32 * jd, LD, sS, kL32, 32, ty * 8, tx);
+    cp_wait_group<0>();   // G_C columns of block jd
     __syncthreads();
-    for (int i = threadIdx.x; i < 32 * D; i += kT)   // <G_C, S0> over these rows
-      gsum = fmaf(sS[(i / D) * LD + i % D], sT[(i / D) * LD + i % D], gsum);
+    for (int i = threadIdx.x; i < D * 32; i += kT)   // <G_C, S0> over these columns
+      gsum = fmaf(sS[(i >> 5) * kL32 + (i & 31)], sT[(i >> 5) * kL32 + (i & 31)], gsum);
     __syncthreads();
-    if (js + 1 < NC) cp_blk<D, 32>(sS, S0g + (size_t)32 * (js + 1) * D);
+    if (jd + 1 < NC) cp_blk32<D, D>(sS, S0g, 32 * (jd + 1));
     cp_commit();
-    float kg[8][1];
-    zero(kg);
-    mm_nt(kg, sK, LD, sT, LD, D, ty * 8, tx);
+    mm_nt(kg, sK + 32 * jd, LD, sT, kL32, 32, ty * 8, tx);
+    __syncthreads();
+    if (jd + 1 < NC) cp_blk32<D, D>(sT, GCg, 32 * (jd + 1));
+    cp_commit();
+  }
 #pragma unroll
-    for (int r = 0; r < 8; r++) {
-      const int t = ty * 8 + r;
-      const float rc = expf(lgC - lg[t]) * kg[r][0];
+  for (int r = 0; r < 8; r++) {
+    const int t = ty * 8 + r;
+    const float g = expf(lg[t]), rcf = expf(lgC - lg[t]);
+#pragma unroll
+    for (int c = 0; c < NC; c++) {
+      const int j = tx + 32 * c;
+      sX[t * LD + j] -= g * ks[r][c];
+      pq[r] = fmaf(sO[t * LD + j], g * qs[r][c], pq[r]);
+      const float rc = rcf * kg[r][c];
       sY[t * LD + j] = rc;
       pr[r] = fmaf(Dg[t * D + j], rc, pr[r]);
     }
-    __syncthreads();
-    if (js + 1 < NC) cp_blk<D, 32>(sT, GCg + (size_t)32 * (js + 1) * D);
-    cp_commit();
   }
   cp_wait_group<0>();
   __syncthreads();
@@ -821,7 +923,7 @@ __global__ void __launch_bounds__(kT) k_rec_grad_b(RecParams p) {
   float* sD = sO + kC * LD;      // Delta
   float* sY = sD + kC * LD;
   float* sL = sY + kC * LD;      // [C][kLC]: L; before that, with sA, two [32][LD] row blocks of S0 / G_C
-  float* sA = sL + kC * kLC;     // [C][kLC]: DA
+  float* sA = sL + kC * kLC;     // [C][kLC]: DA + DA^T
   float* lg = sA + kC * kLC;
   float* be = lg + kC;
   float* al = be + kC;
@@ -862,8 +964,7 @@ __global__ void __launch_bounds__(kT) k_rec_grad_b(RecParams p) {
     const float* blkp = slot[i & 1];
     const int js = i % NC;
     if (i < NC) {
-      mm_nn(gq, sO + 32 * js, LD, blkp, LD, 32, ty * 8, tx);
-      mm_nn(t1, sY + 32 * js, LD, blkp, LD, 32, ty * 8, tx);
+      mm_nn2(gq, t1, sO + 32 * js, sY + 32 * js, LD, blkp, LD, 32, ty * 8, tx);
     } else {
       mm_nn(t1, sD + 32 * js, LD, blkp, LD, 32, ty * 8, tx);
     }
@@ -890,10 +991,8 @@ __global__ void __launch_bounds__(kT) k_rec_grad_b(RecParams p) {
   }
   {
     float dod[8][2], yd[8][2], qk[8][2], kk[8][2];
-    gram<D>(dod, sO, sD);
-    gram<D>(yd, sY, sD);
-    gram<D>(qk, sQ, sK);
-    gram<D>(kk, sK, sK);
+    gram2<D>(dod, yd, sO, sY, sD);
+    gram2<D>(qk, kk, sQ, sK, sK);
     float csum[2] = {0.f, 0.f};
 #pragma unroll
     for (int r = 0; r < 8; r++) {
@@ -908,7 +1007,13 @@ __global__ void __launch_bounds__(kT) k_rec_grad_b(RecParams p) {
         rsum += z;
         csum[c] += z;
         sL[t * kLC + s] = G * dod[r][c];   // L = tril(G) o DoD
-        sA[t * kLC + s] = G * da;          // DA
+        // DA + DA^T (DA is strictly lower triangular)
+        if (s < t) {
+          sA[t * kLC + s] = G * da;
+          sA[s * kLC + t] = G * da;
+        } else if (s == t) {
+          sA[t * kLC + t] = 0.f;
+        }
       }
       rsum = warp_sum(rsum);
       if (tx == 0) dlg[t] = rsum;
@@ -922,10 +1027,8 @@ __global__ void __launch_bounds__(kT) k_rec_grad_b(RecParams p) {
     for (int w = 0; w < kT / 32; w++) c += cs[w * kC + threadIdx.x];
     dlg[threadIdx.x] -= c;
   }
-  mm_nn(gq, sL, kLC, sK, LD, kC, ty * 8, tx);
+  mm_nn2(gq, gk, sL, sA, kLC, sK, LD, kC, ty * 8, tx);   // L K, (DA + DA^T) K
   mm_tn(gk, sL, kLC, sQ, LD, kC, ty * 8, tx);
-  mm_nn(gk, sA, kLC, sK, LD, kC, ty * 8, tx);
-  mm_tn(gk, sA, kLC, sK, LD, kC, ty * 8, tx);
 #pragma unroll
   for (int r = 0; r < 8; r++) {
     const int t = ty * 8 + r;
@@ -969,7 +1072,7 @@ constexpr size_t smem_prep() { return (size_t)(2 * kC * Lay<D>::LD + 2 * kC * kL
 template <int D>
 constexpr size_t smem_scan_fwd() { return (size_t)(2 * kC * Lay<D>::LD + 32 * Lay<D>::LD + kC * kL32 + kC) * 4; }
 template <int D>
-constexpr size_t smem_out() { return (size_t)(2 * kC * Lay<D>::LD + 32 * Lay<D>::LD + kC * kLC + kC) * 4; }
+constexpr size_t smem_out() { return (size_t)(2 * kC * Lay<D>::LD + D * kL32 + kC * kLC + kC) * 4; }
 template <int D>
 constexpr size_t smem_prep_bwd() { return (size_t)(2 * kC * Lay<D>::LD + kC * kLC + kC) * 4; }
 template <int D>
@@ -977,7 +1080,7 @@ constexpr size_t smem_scan_bwd() {
   return (size_t)(2 * (kC * Lay<D>::LD + kC) + 2 * kC * Lay<D>::LD + 32 * Lay<D>::LD + 32 * kLC + kC * kL32) * 4;
 }
 template <int D>
-constexpr size_t smem_grad_a() { return (size_t)(5 * kC * Lay<D>::LD + 64 * Lay<D>::LD + kC * kLC + 3 * kC) * 4; }
+constexpr size_t smem_grad_a() { return (size_t)(5 * kC * Lay<D>::LD + 2 * D * kL32 + kC * kLC + 3 * kC) * 4; }
 template <int D>
 constexpr size_t smem_grad_b() {
   return (size_t)(5 * kC * Lay<D>::LD + 2 * kC * kLC + 4 * kC + (kT / 32) * kC) * 4;
