@@ -156,17 +156,17 @@ __device__ __forceinline__ void mm_nn(float (&acc)[R][NC], const float* A, int l
   }
 }
 
-// acc[r][c] += sum_k A[i0 + r][k] B[j0 + 32 c][k]      (B read by rows: a product with B^T)
-template <int R, int NC>
+// acc[r][c] += sum_k A[i0 + SI r][k] B[j0 + SJ c][k]      (B read by rows: a product with B^T)
+template <int R, int NC, int SI = 1, int SJ = 32>
 __device__ __forceinline__ void mm_nt(float (&acc)[R][NC], const float* A, int lda, const float* B, int ldb, int K,
                                       int i0, int j0) {
 #pragma unroll 2
   for (int k = 0; k < K; k += 4) {
     float4 a[R], b[NC];
 #pragma unroll
-    for (int r = 0; r < R; r++) a[r] = *reinterpret_cast<const float4*>(A + (i0 + r) * lda + k);
+    for (int r = 0; r < R; r++) a[r] = *reinterpret_cast<const float4*>(A + (i0 + SI * r) * lda + k);
 #pragma unroll
-    for (int c = 0; c < NC; c++) b[c] = *reinterpret_cast<const float4*>(B + (j0 + 32 * c) * ldb + k);
+    for (int c = 0; c < NC; c++) b[c] = *reinterpret_cast<const float4*>(B + (j0 + SJ * c) * ldb + k);
 #pragma unroll
     for (int r = 0; r < R; r++)
 #pragma unroll
@@ -197,6 +197,36 @@ __device__ __forceinline__ void mm_tn(float (&acc)[R][NC], const float* A, int l
     }
 #pragma unroll
     for (int c = 0; c < NC; c++) b[c] = B[k * ldb + j0 + 32 * c];
+#pragma unroll
+    for (int r = 0; r < R; r++)
+#pragma unroll
+      for (int c = 0; c < NC; c++) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+  }
+}
+
+// N consecutive floats (N = 2 or 4, 8- or 16-byte aligned) in one shared-memory read
+template <int N>
+__device__ __forceinline__ void ldv(float (&x)[N], const float* p) {
+  static_assert(N == 2 || N == 4, "vector width");
+  if constexpr (N == 4) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+  } else {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    x[0] = v.x, x[1] = v.y;
+  }
+}
+
+// acc[r][c] += sum_k A[k][i0 + r] B[k][j0 + c]: a thread's rows and columns are consecutive,
+// each read as one vector (a 2-D warp tile: lanes split both rows and columns)
+template <int R, int NC>
+__device__ __forceinline__ void mm_tn_v(float (&acc)[R][NC], const float* A, int lda, const float* B, int ldb, int K,
+                                        int i0, int j0) {
+#pragma unroll 4
+  for (int k = 0; k < K; k++) {
+    float a[R], b[NC];
+    ldv<R>(a, A + k * lda + i0);
+    ldv<NC>(b, B + k * ldb + j0);
 #pragma unroll
     for (int r = 0; r < R; r++)
 #pragma unroll
@@ -431,12 +461,14 @@ __global__ void __launch_bounds__(kT) k_rec_prep(RecParams p) {
 // The state passed chunk to chunk along the runs of one level: one CTA per (run, head,
 // 32-row block of S).  Per chunk: S0 saved, Delta = U - W S0^T (saved),
 // S = g_C S0 + Delta^T diag(g_C / g) K; at the run's end S is saved for the runs that
-// continue from it.
+// continue from it.  Both products use 2-D warp tiles (lanes split rows and columns, so a
+// warp reads a 16 x 16 or 16 x d/4 block of operands, not all columns of one of them).
 template <int D>
 __global__ void __launch_bounds__(kT) k_rec_scan_fwd(RecParams p, int32_t lvl0) {
-  // single-buffered on purpose: at 94 KB of shared memory two CTAs share an SM, and a
-  // level's chains finish in one round of CTAs instead of two
-  constexpr int LD = Lay<D>::LD, NC = Lay<D>::NC, NB = D / 32;
+  // single buffers (94 KB of shared memory: two CTAs share an SM), filled ahead all the
+  // same: the next chunk's W arrives during this chunk's second product, its U, lg and K
+  // during the next first product
+  constexpr int LD = Lay<D>::LD, NB = D / 32, NV = D / 32;
   extern __shared__ __align__(16) float sm[];
   float* sW = sm;
   float* sK = sW + kC * LD;
@@ -448,59 +480,86 @@ __global__ void __launch_bounds__(kT) k_rec_scan_fwd(RecParams p, int32_t lvl0) 
   const int32_t r0 = p.run_info[4 * run], r1 = p.run_info[4 * run + 1];
   const int32_t pr = p.run_info[4 * run + 2], c0 = p.run_info[4 * run + 3];
   const int nch = (r1 - r0 + kC - 1) / kC;
-  const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5, ly = (threadIdx.x >> 3) & 3, lx = threadIdx.x & 7;
   const int j0 = jb * 32;
+  // first product, Delta [C x 32]: warp (w >> 1, w & 1) a 16 x 16 block, rows 16 (w >> 1) +
+  // ly + 4 r, columns 16 (w & 1) + lx + 8 c
+  const int t1 = 16 * (w >> 1) + ly, s1 = 16 * (w & 1) + lx;
+  // second product, S [32 x D]: warp (w >> 2, w & 3) a 16 x D/4 block, rows 16 (w >> 2) +
+  // 4 ly + r, columns (D / 4) (w & 3) + NV lx + c
+  const int j2 = 16 * (w >> 2) + 4 * ly, k2 = (D / 4) * (w & 3) + NV * lx;
+  auto issue_w = [&](int ci) {
+    cp_blk<D>(sW, p.Wb + ((size_t)(c0 + ci) * p.H + h) * kC * D);
+    cp_commit();
+  };
+  auto issue_uk = [&](int ci) {
+    const int ch = c0 + ci;
+    const size_t blk = (size_t)ch * p.H + h;
+    cp_blk32<D>(sU, p.Ub + blk * kC * D, j0);
+    if (threadIdx.x < kC / 4) cp16(lg + threadIdx.x * 4, p.Lb + blk * kC + threadIdx.x * 4, true);
+    cp_rows<D>(sK, p.k, p.chunk_info[2 * ch], p.chunk_info[2 * ch + 1], p.H, h);
+    cp_commit();
+  };
   if (pr >= 0)
     cp_blk<D, 32>(sS, p.run_end + ((size_t)pr * p.H + h) * D * D + (size_t)j0 * D);
   else
     for (int i = threadIdx.x; i < 32 * LD; i += kT) sS[i] = 0.f;
+  if (nch > 0) {
+    issue_w(0);   // with the start state
+    issue_uk(0);
+  } else {
+    cp_commit();
+  }
   for (int ci = 0; ci < nch; ci++) {
-    const int ch = c0 + ci;
-    const size_t blk = (size_t)ch * p.H + h;
-    const int64_t row0 = p.chunk_info[2 * ch];
-    const int rows = p.chunk_info[2 * ch + 1];
-    cp_blk<D>(sW, p.Wb + blk * kC * D);
-    cp_blk32<D>(sU, p.Ub + blk * kC * D, j0);
-    if (threadIdx.x < kC / 4) cp16(lg + threadIdx.x * 4, p.Lb + blk * kC + threadIdx.x * 4, true);
-    cp_commit();
-    cp_rows<D>(sK, p.k, row0, rows, p.H, h);   // needed only after Delta: a group of its own
-    cp_commit();
-    cp_wait_group<1>();
+    const size_t blk = (size_t)(c0 + ci) * p.H + h;
+    cp_wait_group<1>();   // W (and the start state)
     __syncthreads();
     float* S0g = p.S0 + blk * D * D + (size_t)j0 * D;
     for (int i = threadIdx.x; i < 32 * D / 4; i += kT)
       *reinterpret_cast<float4*>(S0g + i * 4) = *reinterpret_cast<const float4*>(sS + (i / (D / 4)) * LD + (i % (D / 4)) * 4);
+    float acc[4][2];
+    zero(acc);
+    mm_nt<4, 2, 4, 8>(acc, sW, LD, sS, LD, D, t1, s1);   // (W S0^T)[t][j]
+    cp_wait_group<0>();   // U, lg, K
+    __syncthreads();      // every warp is past its reads of W
+    if (ci + 1 < nch) issue_w(ci + 1);
+    else cp_commit();
     {
-      float acc[8][1];
-      zero(acc);
-      mm_nt(acc, sW, LD, sS, LD, D, ty * 8, tx);   // (W S0^T)[t][j]
       const float gC = lg[kC - 1];
       float* Dg = p.Db + blk * kC * D;
 #pragma unroll
-      for (int r = 0; r < 8; r++) {
-        const int t = ty * 8 + r;
-        const float dl = sU[t * kL32 + tx] - acc[r][0];
-        Dg[t * D + j0 + tx] = dl;
-        sU[t * kL32 + tx] = dl * expf(gC - lg[t]);
+      for (int r = 0; r < 4; r++) {
+        const int t = t1 + 4 * r;
+        const float sc = expf(gC - lg[t]);
+#pragma unroll
+        for (int c = 0; c < 2; c++) {
+          const int j = s1 + 8 * c;
+          const float dl = sU[t * kL32 + j] - acc[r][c];
+          Dg[t * D + j0 + j] = dl;
+          sU[t * kL32 + j] = dl * sc;
+        }
       }
     }
-    cp_wait_group<0>();
     __syncthreads();
     {
-      float acc[4][NC];
-      zero(acc);
-      mm_tn(acc, sU, kL32, sK, LD, kC, ty * 4, tx);   // (Delta^T diag(g_C/g) K)[j][k]
+      float acc2[4][NV];
+      zero(acc2);
+      mm_tn_v(acc2, sU, kL32, sK, LD, kC, j2, k2);   // (Delta^T diag(g_C/g) K)[j][k]
       const float gC = expf(lg[kC - 1]);
 #pragma unroll
       for (int r = 0; r < 4; r++)
 #pragma unroll
-        for (int c = 0; c < NC; c++) {
-          float& x = sS[(ty * 4 + r) * LD + tx + 32 * c];
-          x = fmaf(gC, x, acc[r][c]);
+        for (int c = 0; c < NV; c++) {
+          float& x = sS[(j2 + r) * LD + k2 + c];
+          x = fmaf(gC, x, acc2[r][c]);
         }
     }
-    __syncthreads();
+    __syncthreads();      // U, lg, K read; S updated
+    if (ci + 1 < nch) issue_uk(ci + 1);
+    else cp_commit();
   }
+  cp_wait_group<0>();
+  __syncthreads();
   float* Eg = p.run_end + ((size_t)run * p.H + h) * D * D + (size_t)j0 * D;
   for (int i = threadIdx.x; i < 32 * D / 4; i += kT)
     *reinterpret_cast<float4*>(Eg + i * 4) = *reinterpret_cast<const float4*>(sS + (i / (D / 4)) * LD + (i % (D / 4)) * 4);
