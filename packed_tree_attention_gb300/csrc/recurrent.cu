@@ -156,6 +156,11 @@ __device__ __forceinline__ void mm_nn(float (&acc)[R][NC], const float* A, int l
   }
 }
 
+// component kk of a float4 (kk a compile-time constant after unrolling)
+__device__ __forceinline__ float f4c(const float4& v, int kk) {
+  return kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w;
+}
+
 // acc[r][c] += sum_k A[i0 + SI r][k] B[j0 + SJ c][k]      (B read by rows: a product with B^T)
 template <int R, int NC, int SI = 1, int SJ = 32>
 __device__ __forceinline__ void mm_nt(float (&acc)[R][NC], const float* A, int lda, const float* B, int ldb, int K,
@@ -167,15 +172,13 @@ __device__ __forceinline__ void mm_nt(float (&acc)[R][NC], const float* A, int l
     for (int r = 0; r < R; r++) a[r] = *reinterpret_cast<const float4*>(A + (i0 + SI * r) * lda + k);
 #pragma unroll
     for (int c = 0; c < NC; c++) b[c] = *reinterpret_cast<const float4*>(B + (j0 + SJ * c) * ldb + k);
+    // one component of the 4-step at a time: consecutive FMAs update different accumulators
 #pragma unroll
-    for (int r = 0; r < R; r++)
+    for (int kk = 0; kk < 4; kk++)
 #pragma unroll
-      for (int c = 0; c < NC; c++) {
-        acc[r][c] = fmaf(a[r].x, b[c].x, acc[r][c]);
-        acc[r][c] = fmaf(a[r].y, b[c].y, acc[r][c]);
-        acc[r][c] = fmaf(a[r].z, b[c].z, acc[r][c]);
-        acc[r][c] = fmaf(a[r].w, b[c].w, acc[r][c]);
-      }
+      for (int r = 0; r < R; r++)
+#pragma unroll
+        for (int c = 0; c < NC; c++) acc[r][c] = fmaf(f4c(a[r], kk), f4c(b[c], kk), acc[r][c]);
   }
 }
 
@@ -249,17 +252,15 @@ __device__ __forceinline__ void mm_nt2(float (&acc1)[R][NC], float (&acc2)[R][NC
     for (int u = 0; u < 2; u++) {
       const float* A = u ? A2 : A1;
       float(&acc)[R][NC] = u ? acc2 : acc1;
+      float4 a[R];
 #pragma unroll
-      for (int r = 0; r < R; r++) {
-        const float4 a = *reinterpret_cast<const float4*>(A + (i0 + r) * lda + k);
+      for (int r = 0; r < R; r++) a[r] = *reinterpret_cast<const float4*>(A + (i0 + r) * lda + k);
 #pragma unroll
-        for (int c = 0; c < NC; c++) {
-          acc[r][c] = fmaf(a.x, b[c].x, acc[r][c]);
-          acc[r][c] = fmaf(a.y, b[c].y, acc[r][c]);
-          acc[r][c] = fmaf(a.z, b[c].z, acc[r][c]);
-          acc[r][c] = fmaf(a.w, b[c].w, acc[r][c]);
-        }
-      }
+      for (int kk = 0; kk < 4; kk++)
+#pragma unroll
+        for (int r = 0; r < R; r++)
+#pragma unroll
+          for (int c = 0; c < NC; c++) acc[r][c] = fmaf(f4c(a[r], kk), f4c(b[c], kk), acc[r][c]);
     }
   }
 }
