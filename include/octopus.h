@@ -42,7 +42,7 @@ enum {
   OCTO_ESTATE = 3,   /* cursor is done, rewound away from, released, or freed */
   OCTO_ECUDA = 4,    /* a CUDA call failed; see octo_last_cuda_error() */
   OCTO_ETIMEOUT = 5, /* a bounded device wait expired; the kernel returned early */
-  OCTO_ENOTSUP = 6,  /* shape or dtype this build has no kernel for */
+  OCTO_ENOTSUP = 6,  /* shape or dtype the library has no kernel for */
   OCTO_ESCRATCH = 7  /* request needs more than the built-in scratch of octo_decode_noalloc */
 };
 
