@@ -365,6 +365,15 @@ __device__ __forceinline__ void gram(float (&acc)[8][2], const float* X, const f
   zero(acc);
   mm_nt(acc, X, Lay<D>::LD, Y, Lay<D>::LD, D, (threadIdx.x >> 5) * 8, threadIdx.x & 31);
 }
+// The same product with a 2-D warp tile: warp w a 16 x 32 block of the C x C result, the
+// thread rows gram_row(r) and columns gram_col(c) (a quarter of the operand reads of gram)
+__device__ __forceinline__ int gram_row(int r) { return 16 * (threadIdx.x >> 6) + ((threadIdx.x >> 3) & 3) + 4 * r; }
+__device__ __forceinline__ int gram_col(int c) { return 32 * ((threadIdx.x >> 5) & 1) + (threadIdx.x & 7) + 8 * c; }
+template <int D>
+__device__ __forceinline__ void gram_w(float (&acc)[4][4], const float* X, const float* Y) {
+  zero(acc);
+  mm_nt<4, 4, 4, 8>(acc, X, Lay<D>::LD, Y, Lay<D>::LD, D, gram_row(0), gram_col(0));
+}
 // two of them with the same Y
 template <int D>
 __device__ __forceinline__ void gram2(float (&acc1)[8][2], float (&acc2)[8][2], const float* X1, const float* X2,
@@ -403,13 +412,13 @@ __global__ void __launch_bounds__(kT) k_rec_prep(RecParams p) {
   cp_wait();
   __syncthreads();
   {
-    float acc[8][2];
-    gram<D>(acc, sK, sK);
+    float acc[4][4];
+    gram_w<D>(acc, sK, sK);
 #pragma unroll
-    for (int r = 0; r < 8; r++)
+    for (int r = 0; r < 4; r++)
 #pragma unroll
-      for (int c = 0; c < 2; c++) {
-        const int t = ty * 8 + r, s = tx + 32 * c;
+      for (int c = 0; c < 4; c++) {
+        const int t = gram_row(r), s = gram_col(c);
         sA[t * kLC + s] = s < t ? expf(lg[t] - lg[s]) * acc[r][c] : 0.f;
       }
   }
@@ -435,9 +444,11 @@ __global__ void __launch_bounds__(kT) k_rec_prep(RecParams p) {
   }
   __syncthreads();
   // rows of K scaled by beta g, of V by beta
+  if (threadIdx.x < kC) al[threadIdx.x] = be[threadIdx.x] * expf(lg[threadIdx.x]);   // alpha is not needed here
+  __syncthreads();
   for (int i = threadIdx.x; i < kC * D; i += kT) {
     const int t = i / D, c = i % D;
-    sK[t * LD + c] *= be[t] * expf(lg[t]);
+    sK[t * LD + c] *= al[t];
     sV[t * LD + c] *= be[t];
   }
   __syncthreads();
@@ -588,13 +599,13 @@ __global__ void __launch_bounds__(kT) k_rec_out(RecParams p) {
   cp_wait();
   __syncthreads();
   {
-    float acc[8][2];
-    gram<D>(acc, sQ, sKD);
+    float acc[4][4];
+    gram_w<D>(acc, sQ, sKD);
 #pragma unroll
-    for (int r = 0; r < 8; r++)
+    for (int r = 0; r < 4; r++)
 #pragma unroll
-      for (int c = 0; c < 2; c++) {
-        const int t = ty * 8 + r, s = tx + 32 * c;
+      for (int c = 0; c < 4; c++) {
+        const int t = gram_row(r), s = gram_col(c);
         sB[t * kLC + s] = s <= t ? expf(lg[t] - lg[s]) * acc[r][c] : 0.f;
       }
   }
@@ -653,13 +664,13 @@ __global__ void __launch_bounds__(kT) k_rec_prep_bwd(RecParams p) {
   cp_wait();
   __syncthreads();
   {
-    float acc[8][2];
-    gram<D>(acc, sQ, sKW);
+    float acc[4][4];
+    gram_w<D>(acc, sQ, sKW);
 #pragma unroll
-    for (int r = 0; r < 8; r++)
+    for (int r = 0; r < 4; r++)
 #pragma unroll
-      for (int c = 0; c < 2; c++) {
-        const int t = ty * 8 + r, s = tx + 32 * c;
+      for (int c = 0; c < 4; c++) {
+        const int t = gram_row(r), s = gram_col(c);
         sB[t * kLC + s] = s <= t ? -expf(lg[t] - lg[s]) * acc[r][c] : 0.f;
       }
   }
@@ -824,13 +835,13 @@ __global__ void __launch_bounds__(kT) k_rec_grad_a(RecParams p) {
   cp_wait_group<2>();
   __syncthreads();
   {
-    float acc[8][2];
-    gram<D>(acc, sQ, sK);
+    float acc[4][4];
+    gram_w<D>(acc, sQ, sK);
 #pragma unroll
-    for (int r = 0; r < 8; r++)
+    for (int r = 0; r < 4; r++)
 #pragma unroll
-      for (int c = 0; c < 2; c++) {
-        const int t = ty * 8 + r, s = tx + 32 * c;
+      for (int c = 0; c < 4; c++) {
+        const int t = gram_row(r), s = gram_col(c);
         sB[t * kLC + s] = s <= t ? expf(lg[t] - lg[s]) * acc[r][c] : 0.f;
       }
   }
@@ -915,14 +926,14 @@ __global__ void __launch_bounds__(kT) k_rec_grad_a(RecParams p) {
   }
   // A = strict lower G o K K^T, and Delta into Q's place
   {
-    float acc[8][2];
-    gram<D>(acc, sK, sK);
+    float acc[4][4];
+    gram_w<D>(acc, sK, sK);
     __syncthreads();
 #pragma unroll
-    for (int r = 0; r < 8; r++)
+    for (int r = 0; r < 4; r++)
 #pragma unroll
-      for (int c = 0; c < 2; c++) {
-        const int t = ty * 8 + r, s = tx + 32 * c;
+      for (int c = 0; c < 4; c++) {
+        const int t = gram_row(r), s = gram_col(c);
         sB[t * kLC + s] = s < t ? expf(lg[t] - lg[s]) * acc[r][c] : 0.f;
       }
     cp_blk<D>(sQ, Dg);
