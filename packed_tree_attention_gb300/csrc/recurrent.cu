@@ -700,13 +700,16 @@ __global__ void __launch_bounds__(kT) k_rec_prep_bwd(RecParams p) {
 // G = g_C G - (G K^T diag(g_C / g)) W + dO^T E.  The run's start gradient is saved.
 template <int D>
 __global__ void __launch_bounds__(kT) k_rec_scan_bwd(RecParams p, int32_t lvl0) {
-  constexpr int LD = Lay<D>::LD, NC = Lay<D>::NC, NB = D / 32;
+  // 104 KB of shared memory, so two CTAs share an SM (the levels of many runs take two
+  // rounds of CTAs, not three): one K buffer, refilled with the next chunk's K once this
+  // chunk's G K^T is formed, and W and E brought in one column half at a time
+  constexpr int LD = Lay<D>::LD, NB = D / 32, NH = D / 2, HL = NH + 4, NCH = NH / 32;
   extern __shared__ __align__(16) float sm[];
-  float* sKb = sm;                   // 2 x ([C][LD] K, [C] lg)
-  constexpr int kSetK = kC * LD + kC;
-  float* sW = sKb + 2 * kSetK;
-  float* sE = sW + kC * LD;
-  float* sG = sE + kC * LD;          // [32][LD]
+  float* sK = sm;                    // [C][LD] K
+  float* lg = sK + kC * LD;          // [C]
+  float* sW = lg + kC;               // [C][HL] a column half of W
+  float* sE = sW + kC * HL;          // [C][HL] the same half of E
+  float* sG = sE + kC * HL;          // [32][LD]
   float* sX = sG + 32 * LD;          // [32][kLC]
   float* sO = sX + 32 * kLC;         // [C][kL32] rows of dO, this block's columns
   const int li = blockIdx.x / (p.H * NB), h = (blockIdx.x / NB) % p.H, jb = blockIdx.x % NB;
@@ -715,15 +718,24 @@ __global__ void __launch_bounds__(kT) k_rec_scan_bwd(RecParams p, int32_t lvl0) 
   const int nch = (r1 - r0 + kC - 1) / kC;
   const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
   const int j0 = jb * 32;
-  auto issue_k = [&](int ci, int b) {
+  auto issue_k = [&](int ci) {
     const int ch = c0 + ci;
     const size_t blk = (size_t)ch * p.H + h;
-    float* set = sKb + b * kSetK;
-    cp_rows<D>(set, p.k, p.chunk_info[2 * ch], p.chunk_info[2 * ch + 1], p.H, h);
-    if (threadIdx.x < kC / 4) cp16(set + kC * LD + threadIdx.x * 4, p.Lb + blk * kC + threadIdx.x * 4, true);
+    cp_rows<D>(sK, p.k, p.chunk_info[2 * ch], p.chunk_info[2 * ch + 1], p.H, h);
+    if (threadIdx.x < kC / 4) cp16(lg + threadIdx.x * 4, p.Lb + blk * kC + threadIdx.x * 4, true);
     cp_commit();
   };
-  issue_k(nch - 1, (nch - 1) & 1);
+  // columns [NH hf, NH hf + NH) of the chunk's W and E (not committed)
+  auto issue_we = [&](size_t blk, int hf) {
+    const float* w = p.Wb + blk * kC * D + NH * hf;
+    const float* e = p.Ub + blk * kC * D + NH * hf;
+    for (int i = threadIdx.x; i < kC * NH / 4; i += kT) {
+      const int t = i / (NH / 4), cc = (i % (NH / 4)) * 4;
+      cp16(sW + t * HL + cc, w + t * D + cc, true);
+      cp16(sE + t * HL + cc, e + t * D + cc, true);
+    }
+  };
+  if (nch > 0) issue_k(nch - 1);
   for (int i = threadIdx.x; i < 32 * D; i += kT) {
     float x = 0.f;
     for (int c = p.child_off[run]; c < p.child_off[run + 1]; c++)
@@ -735,14 +747,12 @@ __global__ void __launch_bounds__(kT) k_rec_scan_bwd(RecParams p, int32_t lvl0) 
     const size_t blk = (size_t)ch * p.H + h;
     const int64_t row0 = p.chunk_info[2 * ch];
     const int rows = p.chunk_info[2 * ch + 1];
-    float* sK = sKb + (ci & 1) * kSetK;
-    float* lg = sK + kC * LD;
-    cp_blk<D>(sW, p.Wb + blk * kC * D);
-    cp_blk<D>(sE, p.Ub + blk * kC * D);
+    issue_we(blk, 0);
     cp_rows32<D>(sO, p.dout, row0, rows, p.H, h, j0);
     cp_commit();
     cp_wait_group<1>();   // this chunk's K and lg
     __syncthreads();
+    const float lgC = lg[kC - 1];   // kept: K's buffer takes the next chunk's K below
     float* Gg = p.Gb + blk * D * D + (size_t)j0 * D;
     for (int i = threadIdx.x; i < 32 * D / 4; i += kT)
       *reinterpret_cast<float4*>(Gg + i * 4) = *reinterpret_cast<const float4*>(sG + (i / (D / 4)) * LD + (i % (D / 4)) * 4);
@@ -750,34 +760,37 @@ __global__ void __launch_bounds__(kT) k_rec_scan_bwd(RecParams p, int32_t lvl0) 
       float acc[4][2];
       zero(acc);
       mm_nt(acc, sG, LD, sK, LD, D, ty * 4, tx);   // (G K^T)[j][t]
-      const float gC = lg[kC - 1];
 #pragma unroll
       for (int r = 0; r < 4; r++)
 #pragma unroll
         for (int c = 0; c < 2; c++) {
           const int t = tx + 32 * c;
-          sX[(ty * 4 + r) * kLC + t] = acc[r][c] * expf(gC - lg[t]);
+          sX[(ty * 4 + r) * kLC + t] = acc[r][c] * expf(lgC - lg[t]);
         }
     }
-    if (ci > 0) {
-      issue_k(ci - 1, (ci - 1) & 1);   // the other buffer: its last reader finished a chunk ago
-      cp_wait_group<1>();              // this chunk's W, E, dO
-    } else {
-      cp_wait_group<0>();
-    }
-    __syncthreads();
-    {
-      float acc[4][NC], acc2[4][NC];
+    cp_wait_group<0>();   // W and E, first half; dO
+    __syncthreads();      // every warp is past its reads of K and lg
+    if (ci > 0) issue_k(ci - 1);
+    const float gC = expf(lgC);
+#pragma unroll 1
+    for (int hf = 0; hf < 2; hf++) {
+      if (hf) {
+        __syncthreads();   // the first halves of W and E are read
+        issue_we(blk, 1);
+        cp_commit();
+        cp_wait_group<0>();
+        __syncthreads();
+      }
+      float acc[4][NCH], acc2[4][NCH];
       zero(acc);
       zero(acc2);
-      mm_nn(acc, sX, kLC, sW, LD, kC, ty * 4, tx);
-      mm_tn(acc2, sO, kL32, sE, LD, kC, ty * 4, tx);
-      const float gC = expf(lg[kC - 1]);
+      mm_nn(acc, sX, kLC, sW, HL, kC, ty * 4, tx);
+      mm_tn(acc2, sO, kL32, sE, HL, kC, ty * 4, tx);
 #pragma unroll
       for (int r = 0; r < 4; r++)
 #pragma unroll
-        for (int c = 0; c < NC; c++) {
-          float& x = sG[(ty * 4 + r) * LD + tx + 32 * c];
+        for (int c = 0; c < NCH; c++) {
+          float& x = sG[(ty * 4 + r) * LD + NH * hf + tx + 32 * c];
           x = gC * x - acc[r][c] + acc2[r][c];
         }
     }
@@ -1148,7 +1161,7 @@ template <int D>
 constexpr size_t smem_prep_bwd() { return (size_t)(2 * kC * Lay<D>::LD + kC * kLC + kC) * 4; }
 template <int D>
 constexpr size_t smem_scan_bwd() {
-  return (size_t)(2 * (kC * Lay<D>::LD + kC) + 2 * kC * Lay<D>::LD + 32 * Lay<D>::LD + 32 * kLC + kC * kL32) * 4;
+  return (size_t)(kC * Lay<D>::LD + kC + 2 * kC * (D / 2 + 4) + 32 * Lay<D>::LD + 32 * kLC + kC * kL32) * 4;
 }
 template <int D>
 constexpr size_t smem_grad_a() { return (size_t)(5 * kC * Lay<D>::LD + 2 * D * kL32 + kC * kLC + 3 * kC) * 4; }
