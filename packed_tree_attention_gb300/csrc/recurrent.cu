@@ -238,7 +238,7 @@ __device__ __forceinline__ void mm_tn_v(float (&acc)[R][NC], const float* A, int
 }
 
 // Two products that share one operand, which is then read from shared memory once for
-// both (the products are bound by shared-memory wavefronts, not by the FMA pipe):
+// both (half the shared-memory reads of that operand):
 // acc1 += A1 B^T and acc2 += A2 B^T, as mm_nt
 template <int R, int NC>
 __device__ __forceinline__ void mm_nt2(float (&acc1)[R][NC], float (&acc2)[R][NC], const float* A1, const float* A2,
