@@ -191,3 +191,30 @@ def test_episode_sampled_rows(lib):
         for t in range(len(path)):
             S = as_[t] * (S - bs[t] * np.outer(S @ ks[t], ks[t])) + bs[t] * np.outer(vs[t], ks[t])
         _close(o[r, h].cpu().numpy(), S @ qs[-1], "o row %d head %d (path of %d rows)" % (r, h, len(path)))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_repeat_over_a_dirty_workspace_is_bit_exact(lib, D):
+    """Deterministic and independent of what the workspace held: a second forward +
+    backward, after every workspace byte is set to 0xFF (a NaN pattern), gives the same
+    outputs bit for bit.  Runs ending at a fork point sum the start gradients of their
+    continuations in run order, never by atomics, and no kernel reads a workspace entry
+    that the call has not written."""
+    ep = synth.random_dag(811 + D, page_size=16, max_segments=14, max_len=200, n_roots=2)
+    pool, plan, _ = _setup(lib, ep)
+    N, H = plan.info["n_rows"], 3
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    tq, tk, tv, ta, tb, tdo = (dev(x) for x in _inputs(N, H, D, 5))
+    ws = torch.zeros(plan.recurrent_workspace_size(H, D), dtype=torch.uint8, device="cuda")
+    outs = []
+    for fill in (0, 255):
+        ws.fill_(fill)
+        o = torch.empty((N, H, D), device="cuda")
+        g = [torch.empty((N, H, D), device="cuda") for _ in range(3)] + [torch.empty((N, H), device="cuda") for _ in range(2)]
+        plan.recurrent_fwd(H, D, tq, tk, tv, ta, tb, o, ws)
+        plan.recurrent_bwd(H, D, tq, tk, tv, ta, tb, tdo, *g, ws)
+        plan.sync()
+        outs.append([o] + g)
+    for name, x, y in zip(("o", "dq", "dk", "dv", "dalpha", "dbeta"), outs[0], outs[1]):
+        assert torch.isfinite(x).all(), name
+        assert torch.equal(x, y), name
