@@ -426,3 +426,31 @@ def test_append_step_writes_like_single_appends(lib, oracle_mod, rope):
     assert torch.equal(pools[0][1], pools[1][1]) and torch.equal(pools[0][2], pools[1][2])
     for s in range(ep.n_segments):
         assert np.array_equal(pools[0][0].seg_pages(s), pools[1][0].seg_pages(s))
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,d,P", [("bf16", 4, 2, 128, 64), ("f32", 2, 1, 64, 16)])
+def test_backward_repeat_over_a_dirty_workspace_is_bit_exact(lib, oracle_mod, dtype, Hq, Hkv, d, P):
+    """A second backward over a workspace whose every byte was set to 0xFF (a NaN pattern)
+    gives the first one's dQ, dK, dV bit for bit: the readers of shared pages are summed in
+    a fixed order (no atomics) and no kernel reads workspace it has not written in the call.
+    bf16 with d 128 and pages of 64 runs the tensor-core kernels, fp32 the CUDA-core ones."""
+    ep = synth.random_dag(905, page_size=P, max_segments=12, max_len=300, n_roots=2)
+    r = Run(lib, oracle_mod, ep, Hq, Hkv, d, dtype, 9)
+    plan, _ = r.pack(128)
+    assert plan.kernel_path(Hq, 1) == (1 if dtype == "bf16" else 0)
+    r.fwd()
+    N = plan.info["n_rows"]
+    do = r.dev(r.dO)
+    ws = torch.empty(max(1, plan.attn_bwd_workspace_size(Hq)), dtype=torch.uint8, device="cuda")
+    outs = []
+    for fill in (0, 255):
+        ws.fill_(fill)
+        dq = torch.empty((N, Hq, d), dtype=torch.float32, device="cuda")
+        dk = torch.zeros((r.npages, Hkv, r.P, d), device="cuda")
+        dv = torch.zeros_like(dk)
+        plan.attn_bwd(Hq, r.q_dev, r.o_dev, r.lse_dev, do, dq, dk, dv, r.scale, ws)
+        plan.sync()
+        outs.append((dq, dk, dv))
+    for name, x, y in zip(("dQ", "dK", "dV"), outs[0], outs[1]):
+        assert torch.isfinite(x).all(), name
+        assert torch.equal(x, y), name
