@@ -454,3 +454,27 @@ def test_backward_repeat_over_a_dirty_workspace_is_bit_exact(lib, oracle_mod, dt
     for name, x, y in zip(("dQ", "dK", "dV"), outs[0], outs[1]):
         assert torch.isfinite(x).all(), name
         assert torch.equal(x, y), name
+
+
+def test_decode_repeat_over_a_dirty_workspace_is_bit_exact(lib, oracle_mod):
+    """Split-KV decode twice, the second time over a workspace whose every byte was set to
+    0xFF: the same output and LSE bit for bit (every split's partial is written before the
+    combine reads it, and the combine merges them in split order)."""
+    ep = synth.random_dag(933, page_size=64, max_segments=14, max_len=500, n_roots=2)
+    r = Run(lib, oracle_mod, ep, 8, 2, 128, "bf16", 4)
+    curs = [s for s in range(r.orc.n_segments) if r.orc.seg_info(s)["len"] > 0]
+    q = r.dev(synth.make_decode_q(len(curs), 8, 128, "bf16", 0.5, 13))
+    dp = r.pool.decode_plan(curs)
+    assert dp.kernel_path(8, 2) == 2
+    ws_n = dp.decode_workspace_size(8)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device="cuda")
+    outs = []
+    for fill in (0, 255):
+        ws.fill_(fill)
+        out = torch.empty((len(curs), 8, 128), dtype=r.tdt, device="cuda")
+        lse = torch.empty((len(curs), 8), dtype=torch.float32, device="cuda")
+        dp.decode(8, q, out, lse, r.scale, ws, ws_n)
+        dp.sync()
+        outs.append((out, lse))
+    assert torch.isfinite(outs[0][0].float()).all() and torch.isfinite(outs[0][1]).all()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
